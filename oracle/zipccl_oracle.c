@@ -1,0 +1,780 @@
+/*
+ * zipccl_oracle.c -- plain, slow, single-threaded CPU reference of the ZipCCL
+ * BF16 exponent-coding path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, imports or
+ * calls this file; it shares no source with the CUDA path.  Only the tests,
+ * the smoke check and the benchmark's CPU-baseline leg use it.
+ *
+ * What the method computes (ZipCCL: Efficient Lossless Data Compression of
+ * Communication Collectives for Accelerating LLM Training):
+ *   - abstract, technique (1): exponent coding that exploits the near-Gaussian
+ *     distribution of BF16 communication tensors, without online statistics;
+ *   - shd-paper summary, "key design": frequent exponents get short codes,
+ *     rare exponents long codes, derived from the Gaussian density;
+ *   - Fig. 6 caption: each BF16 value shrinks to about 11 bits (sign and the
+ *     7 mantissa bits stay raw, the exponent is coded);
+ *   - pith summary, "if this is right": lossless, every byte restored;
+ *   - Fig. 3 / Fig. 5: ReduceScatter = receive compressed peer chunks,
+ *     decompress and reduce.
+ * The pages fix no stream format, code construction or scale rule.  The
+ * readings taken here are listed where they are used ("reading:").
+ *
+ * Stream format v1 (little-endian), as written by zo_compress:
+ *   chunk  = header(32) | u32 tile_off[n_tiles] zero-padded to 16 | tiles
+ *   header = u32 magic 0x4C43435A | u16 version 1 | u8 tile_log2 15 |
+ *            u8 seg_log2 10 | u64 n_elems | u32 n_tiles | u8 base |
+ *            u8 flags 0 | i16 q | u8 lens[8] (symbol 2i low nibble, 2i+1 high)
+ *   tile   = u32 mode (0 coded, 1 raw) | u32 n_t | u32 exp_bytes | u32 0 |
+ *            s/m plane: n_t bytes, byte i = sign<<7 | mantissa, padded to 16 |
+ *            exponent region padded to 16:
+ *              raw:   n_t exponent bytes in element order
+ *              coded: u16 seg_words[32] | 32 segments of u32 words
+ *   element i of a tile belongs to segment ((i mod 256) / 8); a segment lists
+ *   its elements in increasing i.  Symbol x = e - base for 0 <= x <= 14, else
+ *   ESC (15) followed by the 8 raw bits of e.  Bits are packed LSB-first into
+ *   little-endian u32 words; a canonical codeword is emitted MSB-first, i.e.
+ *   stored bit-reversed.  Segments are zero-padded to a word.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ZO_MAGIC 0x4C43435Au
+#define ZO_VERSION 1
+#define ZO_TILE 32768u
+#define ZO_ROW 256u
+#define ZO_LANE_ELEMS 8u
+#define ZO_SEGS 32u
+#define ZO_NSYM 16
+#define ZO_WINDOW 15
+#define ZO_ESC 15
+#define ZO_LMAX 10
+#define ZO_CHUNK_HDR 32u
+#define ZO_TILE_HDR 16u
+#define ZO_SEGTAB 64u
+
+enum { ZO_OK = 0, ZO_ERR_INVALID_ARG = 1, ZO_ERR_CAPACITY = 2, ZO_ERR_CORRUPT = 3,
+       ZO_ERR_VERSION = 4 };
+
+static uint64_t pad16(uint64_t x) { return (x + 15u) & ~(uint64_t)15u; }
+
+/* ------------------------------------------------------------------------ */
+/* Closed-form exponent pmf of X ~ N(0, sigma^2)                             */
+/* ------------------------------------------------------------------------ */
+/*
+ * The biased BF16 exponent is e for |x| in [2^(e-127), 2^(e-126)) when
+ * 1 <= e <= 254, and 0 for |x| < 2^-126 (zero and subnormals).  For a centred
+ * Gaussian P(|X| < t) = erf(t / (sigma sqrt 2)), so the pmf is a difference of
+ * erf values.  Reading: the binade edges are taken unrounded (the data are
+ * values already in BF16), and e = 255 gets no mass.
+ */
+void zo_exponent_pmf(double sigma, double *p)
+{
+    double s = sigma * sqrt(2.0);
+    int e;
+    p[0] = erf(ldexp(1.0, -126) / s);
+    for (e = 1; e <= 254; e++)
+        p[e] = erf(ldexp(1.0, e - 126) / s) - erf(ldexp(1.0, e - 127) / s);
+    p[255] = 0.0;
+}
+
+double zo_entropy_bits(const double *p, int n)
+{
+    double h = 0.0;
+    int i;
+    for (i = 0; i < n; i++)
+        if (p[i] > 0.0)
+            h -= p[i] * log2(p[i]);
+    return h;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Length-limited optimal prefix code: package-merge (Larmore & Hirschberg)  */
+/* ------------------------------------------------------------------------ */
+/*
+ * Each symbol contributes one "coin" per level 1..L with the symbol's weight.
+ * Starting from the deepest level, adjacent pairs of the sorted list are
+ * packaged and merged with the level's own coins; the cheapest 2n-2 entries of
+ * the final list are selected and a symbol's code length is the number of
+ * selected entries containing it.  Ties in the merge put the plain coin before
+ * a package; the initial order is weight ascending, then symbol ascending.
+ */
+typedef struct {
+    double w;
+    int cnt[ZO_NSYM];
+} zo_pm_item;
+
+int zo_package_merge(const double *w, int n, int L, int *lens)
+{
+    zo_pm_item base[ZO_NSYM], cur[2 * ZO_NSYM], pk[ZO_NSYM], nxt[2 * ZO_NSYM];
+    int order[ZO_NSYM];
+    int i, j, lvl, ncur, npk, nn;
+    if (n < 2 || n > ZO_NSYM || L < 1 || (1 << L) < n)
+        return ZO_ERR_INVALID_ARG;
+    for (i = 0; i < n; i++)
+        order[i] = i;
+    /* insertion sort: weight ascending, then symbol ascending */
+    for (i = 1; i < n; i++) {
+        int t = order[i];
+        j = i - 1;
+        while (j >= 0 && (w[order[j]] > w[t] || (w[order[j]] == w[t] && order[j] > t))) {
+            order[j + 1] = order[j];
+            j--;
+        }
+        order[j + 1] = t;
+    }
+    for (i = 0; i < n; i++) {
+        memset(&base[i], 0, sizeof(base[i]));
+        base[i].w = w[order[i]];
+        base[i].cnt[order[i]] = 1;
+    }
+    memcpy(cur, base, sizeof(zo_pm_item) * (size_t)n);
+    ncur = n;
+    for (lvl = L; lvl > 1; lvl--) {
+        int a = 0, b = 0, s;
+        npk = 0;
+        for (i = 0; i + 1 < ncur; i += 2) {
+            pk[npk].w = cur[i].w + cur[i + 1].w;
+            for (s = 0; s < ZO_NSYM; s++)
+                pk[npk].cnt[s] = cur[i].cnt[s] + cur[i + 1].cnt[s];
+            npk++;
+        }
+        nn = 0;
+        while (a < n || b < npk) {
+            if (b >= npk || (a < n && base[a].w <= pk[b].w))
+                nxt[nn++] = base[a++];
+            else
+                nxt[nn++] = pk[b++];
+        }
+        memcpy(cur, nxt, sizeof(zo_pm_item) * (size_t)nn);
+        ncur = nn;
+    }
+    for (i = 0; i < n; i++)
+        lens[i] = 0;
+    for (i = 0; i < 2 * n - 2; i++)
+        for (j = 0; j < n; j++)
+            lens[j] += cur[i].cnt[j];
+    return ZO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Phase tables                                                              */
+/* ------------------------------------------------------------------------ */
+/*
+ * Reading: the code is built for sigma = 2^(q/16); the integer q is the scale.
+ * Over the normal range the pmf only shifts by floor(q/16) binades, so the
+ * code lengths depend on the phase r = q mod 16 alone.  The window is the 15
+ * consecutive exponents of largest total mass (lowest start on ties); symbol
+ * 15 (ESC) carries the remaining mass.  Lengths: package-merge with L = 10.
+ * base_off is the window start minus 127 at q = r.
+ */
+void zo_phase_table(int r, int *base_off, int *lens)
+{
+    double p[256], w[ZO_NSYM], best = -1.0, mass, sum = 0.0;
+    int b, i, bb = 0;
+    zo_exponent_pmf(pow(2.0, (double)r / 16.0), p);
+    for (b = 0; b + ZO_WINDOW <= 255; b++) {
+        mass = 0.0;
+        for (i = 0; i < ZO_WINDOW; i++)
+            mass += p[b + i];
+        if (mass > best) {
+            best = mass;
+            bb = b;
+        }
+    }
+    for (i = 0; i < ZO_WINDOW; i++) {
+        w[i] = p[bb + i];
+        sum += w[i];
+    }
+    w[ZO_ESC] = 1.0 - sum;
+    *base_off = bb - 127;
+    zo_package_merge(w, ZO_NSYM, ZO_LMAX, lens);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scale selection without online statistics                                 */
+/* ------------------------------------------------------------------------ */
+/*
+ * Reading (the pages give no rule): for X ~ N(0, sigma^2) the mean biased
+ * exponent is log2(sigma) + 127 - c0 with c0 = 1/2 + (gamma + ln 2)/(2 ln 2)
+ * = 1.41637..., frozen as 1.4164 = 3541/2500.  The chunk's exponents are
+ * sampled at fixed positions (all elements when n <= 4096, else 64 blocks of
+ * 64 consecutive elements starting at floor(b n / 64)); e = 0 and e = 255 are
+ * skipped.  q = round-half-up(16 (S/K - 127 + c0)), evaluated in integers:
+ *   q = floor((40000 (S - 127 K) + 57906 K) / (2500 K)).
+ * K = 0 gives q = 0.
+ */
+static int64_t floor_div(int64_t a, int64_t b)
+{
+    int64_t q = a / b;
+    if ((a % b != 0) && ((a < 0) != (b < 0)))
+        q -= 1;
+    return q;
+}
+
+static int q_from_sums(int64_t S, int64_t K)
+{
+    if (K == 0)
+        return 0;
+    return (int)floor_div(40000 * (S - 127 * K) + 57906 * K, 2500 * K);
+}
+
+int zo_select_q(const uint16_t *x, uint64_t n)
+{
+    int64_t S = 0, K = 0;
+    uint64_t i, b;
+    if (n <= 4096) {
+        for (i = 0; i < n; i++) {
+            int e = (x[i] >> 7) & 0xFF;
+            if (e != 0 && e != 255) {
+                S += e;
+                K++;
+            }
+        }
+    } else {
+        for (b = 0; b < 64; b++) {
+            uint64_t start = (b * n) / 64;
+            for (i = start; i < start + 64; i++) {
+                int e = (x[i] >> 7) & 0xFF;
+                if (e != 0 && e != 255) {
+                    S += e;
+                    K++;
+                }
+            }
+        }
+    }
+    return q_from_sums(S, K);
+}
+
+/* explicit sigma: q = round-half-up(16 log2 sigma), clamped to int16 */
+int zo_q_from_sigma(double sigma)
+{
+    double v = floor(16.0 * log2(sigma) + 0.5);
+    if (v < -32768.0)
+        v = -32768.0;
+    if (v > 32767.0)
+        v = 32767.0;
+    return (int)v;
+}
+
+/* window start for scale q: floor(q/16) + 127 + base_off[q mod 16], clamped
+ * to [0, 240] so that the window stays inside [0, 254]. */
+int zo_base_for_q(int q, const int *base_off_table)
+{
+    int k = (int)floor_div(q, 16);
+    int r = q - 16 * k;
+    int b = k + 127 + base_off_table[r];
+    if (b < 0)
+        b = 0;
+    if (b > 240)
+        b = 240;
+    return b;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Canonical code                                                            */
+/* ------------------------------------------------------------------------ */
+/* Codes assigned in (length, symbol) order; code values are MSB-first. */
+static void canonical_codes(const int *lens, uint32_t *codes)
+{
+    int order[ZO_NSYM], i, j, n = 0, len;
+    uint32_t code = 0;
+    int prev_len = 0;
+    for (len = 1; len <= ZO_LMAX; len++)
+        for (i = 0; i < ZO_NSYM; i++)
+            if (lens[i] == len)
+                order[n++] = i;
+    for (j = 0; j < n; j++) {
+        int s = order[j];
+        if (j > 0)
+            code = (code + 1) << (lens[s] - prev_len);
+        codes[s] = code;
+        prev_len = lens[s];
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Bit writer / reader (one bit at a time, LSB-first in u32 words)          */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    uint32_t *words;
+    uint64_t nbits;
+} zo_bitw;
+
+static void bw_put(zo_bitw *bw, uint32_t bit)
+{
+    uint64_t wi = bw->nbits >> 5;
+    if ((bw->nbits & 31) == 0)
+        bw->words[wi] = 0;
+    bw->words[wi] |= (bit & 1u) << (bw->nbits & 31);
+    bw->nbits++;
+}
+
+typedef struct {
+    const uint8_t *bytes;
+    uint64_t nbits_total;
+    uint64_t pos;
+} zo_bitr;
+
+static int br_get(zo_bitr *br, uint32_t *bit)
+{
+    if (br->pos >= br->nbits_total)
+        return 0;
+    *bit = (br->bytes[br->pos >> 3] >> (br->pos & 7)) & 1u;
+    br->pos++;
+    return 1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Little-endian field helpers                                               */
+/* ------------------------------------------------------------------------ */
+static void put_u16(uint8_t *p, uint32_t v) { p[0] = (uint8_t)v; p[1] = (uint8_t)(v >> 8); }
+static void put_u32(uint8_t *p, uint32_t v)
+{
+    int i;
+    for (i = 0; i < 4; i++)
+        p[i] = (uint8_t)(v >> (8 * i));
+}
+static void put_u64(uint8_t *p, uint64_t v)
+{
+    int i;
+    for (i = 0; i < 8; i++)
+        p[i] = (uint8_t)(v >> (8 * i));
+}
+static uint32_t get_u16(const uint8_t *p) { return (uint32_t)p[0] | ((uint32_t)p[1] << 8); }
+static uint32_t get_u32(const uint8_t *p)
+{
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+static uint64_t get_u64(const uint8_t *p)
+{
+    uint64_t v = 0;
+    int i;
+    for (i = 7; i >= 0; i--)
+        v = (v << 8) | p[i];
+    return v;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sizes                                                                     */
+/* ------------------------------------------------------------------------ */
+static uint64_t n_tiles_of(uint64_t n) { return (n + ZO_TILE - 1) / ZO_TILE; }
+
+/* Worst case: every tile raw. */
+uint64_t zo_max_compressed_bytes(const uint64_t *chunk_elems, uint32_t n_chunks)
+{
+    uint64_t total = 0, t, c;
+    for (c = 0; c < n_chunks; c++) {
+        uint64_t n = chunk_elems[c], T = n_tiles_of(n);
+        total += ZO_CHUNK_HDR + pad16(4 * T);
+        for (t = 0; t < T; t++) {
+            uint64_t nt = (t + 1 < T) ? ZO_TILE : n - t * ZO_TILE;
+            total += ZO_TILE_HDR + 2 * pad16(nt);
+        }
+    }
+    return total;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Compression                                                               */
+/* ------------------------------------------------------------------------ */
+/* Encode one tile of nt elements at out; returns its size in bytes. */
+static uint64_t encode_tile(const uint16_t *x, uint64_t nt, int base, const int *lens,
+                            const uint32_t *codes, uint8_t *out)
+{
+    uint64_t i, j, r0, t8, seg_bits_total = 0, exp_bytes, off;
+    uint32_t seg_words[ZO_SEGS];
+    uint64_t sm_off = ZO_TILE_HDR, ex_off = ZO_TILE_HDR + pad16(nt);
+    uint32_t *words = (uint32_t *)calloc(ZO_TILE, sizeof(uint32_t)); /* >= worst case / 4 */
+    uint32_t *segbuf = (uint32_t *)calloc(ZO_TILE, sizeof(uint32_t));
+    uint64_t nwords = 0;
+    int mode;
+
+    /* sign/mantissa plane */
+    for (i = 0; i < nt; i++)
+        out[sm_off + i] = (uint8_t)(((x[i] >> 8) & 0x80) | (x[i] & 0x7F));
+    for (i = nt; i < pad16(nt); i++)
+        out[sm_off + i] = 0;
+
+    /* exponent segments */
+    for (j = 0; j < ZO_SEGS; j++) {
+        zo_bitw bw;
+        uint64_t w;
+        bw.words = segbuf;
+        bw.nbits = 0;
+        /* segment j: positions row * 256 + 8 j + t, t = 0..7, in row order */
+        for (r0 = 0; r0 < nt; r0 += ZO_ROW) {
+          for (t8 = 0; t8 < ZO_LANE_ELEMS; t8++) {
+            int e, sym, L, b;
+            i = r0 + j * ZO_LANE_ELEMS + t8;
+            if (i >= nt)
+                break;
+            e = (x[i] >> 7) & 0xFF;
+            sym = (e - base >= 0 && e - base < ZO_WINDOW) ? e - base : ZO_ESC;
+            L = lens[sym];
+            for (b = L - 1; b >= 0; b--) /* codeword MSB first */
+                bw_put(&bw, (codes[sym] >> b) & 1u);
+            if (sym == ZO_ESC)
+                for (b = 0; b < 8; b++) /* raw exponent LSB first */
+                    bw_put(&bw, ((uint32_t)e >> b) & 1u);
+          }
+        }
+        seg_bits_total += bw.nbits;
+        seg_words[j] = (uint32_t)((bw.nbits + 31) / 32);
+        for (w = 0; w < seg_words[j]; w++)
+            words[nwords + w] = segbuf[w];
+        nwords += seg_words[j];
+    }
+    (void)seg_bits_total;
+
+    /* coded only when strictly smaller than raw exponent bytes */
+    mode = (ZO_SEGTAB + 4 * nwords < nt) ? 0 : 1;
+    if (mode == 0) {
+        exp_bytes = ZO_SEGTAB + 4 * nwords;
+        for (j = 0; j < ZO_SEGS; j++)
+            put_u16(out + ex_off + 2 * j, seg_words[j]);
+        for (i = 0; i < nwords; i++)
+            put_u32(out + ex_off + ZO_SEGTAB + 4 * i, words[i]);
+    } else {
+        exp_bytes = nt;
+        for (i = 0; i < nt; i++)
+            out[ex_off + i] = (uint8_t)((x[i] >> 7) & 0xFF);
+    }
+    for (off = ex_off + exp_bytes; off < ex_off + pad16(exp_bytes); off++)
+        out[off] = 0;
+    put_u32(out + 0, (uint32_t)mode);
+    put_u32(out + 4, (uint32_t)nt);
+    put_u32(out + 8, (uint32_t)exp_bytes);
+    put_u32(out + 12, 0);
+    free(words);
+    free(segbuf);
+    return ex_off + pad16(exp_bytes);
+}
+
+/*
+ * in: n BF16 words; chunk c holds the next chunk_elems[c] of them.
+ * sigma_hint: NULL or per chunk; a value > 0 fixes sigma, otherwise the scale
+ * is selected from the data.  out receives the chunks back to back;
+ * offsets[c] is chunk c's byte offset and offsets[n_chunks] the total.
+ */
+int zo_compress(const uint16_t *in, uint64_t n, const uint64_t *chunk_elems, uint32_t n_chunks,
+                const float *sigma_hint, uint8_t *out, uint64_t cap, uint64_t *offsets)
+{
+    int base_off[16], lens_tab[16][ZO_NSYM];
+    uint64_t c, pos = 0, elem = 0, sum = 0;
+    int r;
+    if (n_chunks == 0 || (n > 0 && in == NULL) || out == NULL || offsets == NULL)
+        return ZO_ERR_INVALID_ARG;
+    for (c = 0; c < n_chunks; c++)
+        sum += chunk_elems[c];
+    if (sum != n)
+        return ZO_ERR_INVALID_ARG;
+    if (cap < zo_max_compressed_bytes(chunk_elems, n_chunks))
+        return ZO_ERR_CAPACITY;
+    for (r = 0; r < 16; r++)
+        zo_phase_table(r, &base_off[r], lens_tab[r]);
+
+    for (c = 0; c < n_chunks; c++) {
+        uint64_t nc = chunk_elems[c], T = n_tiles_of(nc), t, tpos;
+        const uint16_t *x = in + elem;
+        int q, base, i;
+        const int *lens;
+        uint32_t codes[ZO_NSYM];
+        uint8_t *ch = out + pos;
+
+        if (sigma_hint != NULL && sigma_hint[c] > 0.0f)
+            q = zo_q_from_sigma((double)sigma_hint[c]);
+        else
+            q = zo_select_q(x, nc);
+        base = zo_base_for_q(q, base_off);
+        lens = lens_tab[(int)(q - 16 * floor_div(q, 16))];
+        canonical_codes(lens, codes);
+
+        put_u32(ch + 0, ZO_MAGIC);
+        put_u16(ch + 4, ZO_VERSION);
+        ch[6] = 15;
+        ch[7] = 10;
+        put_u64(ch + 8, nc);
+        put_u32(ch + 16, (uint32_t)T);
+        ch[20] = (uint8_t)base;
+        ch[21] = 0;
+        put_u16(ch + 22, (uint32_t)(uint16_t)(int16_t)q);
+        for (i = 0; i < 8; i++)
+            ch[24 + i] = (uint8_t)(lens[2 * i] | (lens[2 * i + 1] << 4));
+        memset(ch + ZO_CHUNK_HDR, 0, pad16(4 * T));
+        tpos = ZO_CHUNK_HDR + pad16(4 * T);
+        for (t = 0; t < T; t++) {
+            uint64_t nt = (t + 1 < T) ? ZO_TILE : nc - t * ZO_TILE;
+            put_u32(ch + ZO_CHUNK_HDR + 4 * t, (uint32_t)tpos);
+            tpos += encode_tile(x + t * ZO_TILE, nt, base, lens, codes, ch + tpos);
+        }
+        offsets[c] = pos;
+        pos += tpos;
+        elem += nc;
+    }
+    offsets[n_chunks] = pos;
+    return ZO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Decompression                                                             */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    int count[ZO_LMAX + 1];
+    uint32_t first[ZO_LMAX + 1];
+    int offset[ZO_LMAX + 1];
+    int sorted[ZO_NSYM];
+} zo_decoder;
+
+/* Canonical decoding tables; fails unless the lengths form a complete code. */
+static int build_decoder(const int *lens, zo_decoder *d)
+{
+    int i, len, n = 0;
+    uint64_t kraft = 0;
+    uint32_t code = 0;
+    for (i = 0; i < ZO_NSYM; i++) {
+        if (lens[i] < 1 || lens[i] > ZO_LMAX)
+            return ZO_ERR_CORRUPT;
+        kraft += (uint64_t)1 << (ZO_LMAX - lens[i]);
+    }
+    if (kraft != ((uint64_t)1 << ZO_LMAX))
+        return ZO_ERR_CORRUPT;
+    for (len = 0; len <= ZO_LMAX; len++) {
+        d->count[len] = 0;
+        for (i = 0; i < ZO_NSYM; i++)
+            if (lens[i] == len)
+                d->count[len]++;
+    }
+    for (len = 1; len <= ZO_LMAX; len++) {
+        d->offset[len] = n;
+        for (i = 0; i < ZO_NSYM; i++)
+            if (lens[i] == len)
+                d->sorted[n++] = i;
+        d->first[len] = code;
+        code = (code + (uint32_t)d->count[len]) << 1;
+    }
+    return ZO_OK;
+}
+
+/* Read one symbol bit by bit: the code grows MSB-first until it falls inside
+ * the canonical range of its length. */
+static int decode_symbol(zo_bitr *br, const zo_decoder *d, int *sym)
+{
+    uint32_t code = 0, bit;
+    int len;
+    for (len = 1; len <= ZO_LMAX; len++) {
+        if (!br_get(br, &bit))
+            return ZO_ERR_CORRUPT;
+        code = (code << 1) | bit;
+        if (d->count[len] > 0 && code >= d->first[len] &&
+            code - d->first[len] < (uint32_t)d->count[len]) {
+            *sym = d->sorted[d->offset[len] + (int)(code - d->first[len])];
+            return ZO_OK;
+        }
+    }
+    return ZO_ERR_CORRUPT;
+}
+
+/* Decode one chunk (chunk_bytes long) into out; *n_out receives n_elems. */
+static int decode_chunk(const uint8_t *ch, uint64_t chunk_bytes, uint16_t *out, uint64_t max_elems,
+                        uint64_t *n_out)
+{
+    uint64_t nc, T, t;
+    int lens[ZO_NSYM], base, i, st;
+    zo_decoder dec;
+    if (chunk_bytes < ZO_CHUNK_HDR || get_u32(ch) != ZO_MAGIC)
+        return ZO_ERR_CORRUPT;
+    if (get_u16(ch + 4) != ZO_VERSION || ch[6] != 15 || ch[7] != 10)
+        return ZO_ERR_VERSION;
+    nc = get_u64(ch + 8);
+    T = get_u32(ch + 16);
+    if (T != n_tiles_of(nc) || nc > max_elems)
+        return ZO_ERR_CORRUPT;
+    if (ZO_CHUNK_HDR + pad16(4 * T) > chunk_bytes)
+        return ZO_ERR_CORRUPT;
+    base = ch[20];
+    for (i = 0; i < 8; i++) {
+        lens[2 * i] = ch[24 + i] & 15;
+        lens[2 * i + 1] = ch[24 + i] >> 4;
+    }
+    st = build_decoder(lens, &dec);
+    if (st != ZO_OK)
+        return st;
+    for (t = 0; t < T; t++) {
+        uint64_t nt = (t + 1 < T) ? ZO_TILE : nc - t * ZO_TILE;
+        uint64_t toff = get_u32(ch + ZO_CHUNK_HDR + 4 * t), ex_off, exp_bytes, j, k, r0, t8;
+        const uint8_t *tile = ch + toff;
+        uint16_t *y = out + t * ZO_TILE;
+        uint32_t mode;
+        if (toff + ZO_TILE_HDR > chunk_bytes)
+            return ZO_ERR_CORRUPT;
+        mode = get_u32(tile);
+        if (get_u32(tile + 4) != nt)
+            return ZO_ERR_CORRUPT;
+        exp_bytes = get_u32(tile + 8);
+        ex_off = ZO_TILE_HDR + pad16(nt);
+        if (toff + ex_off + pad16(exp_bytes) > chunk_bytes)
+            return ZO_ERR_CORRUPT;
+        /* sign and mantissa first */
+        for (k = 0; k < nt; k++) {
+            uint32_t sm = tile[ZO_TILE_HDR + k];
+            y[k] = (uint16_t)(((sm & 0x80) << 8) | (sm & 0x7F));
+        }
+        if (mode == 1) {
+            if (exp_bytes != nt)
+                return ZO_ERR_CORRUPT;
+            for (k = 0; k < nt; k++)
+                y[k] |= (uint16_t)((uint32_t)tile[ex_off + k] << 7);
+        } else if (mode == 0) {
+            uint64_t wsum = 0, wpos = 0;
+            for (j = 0; j < ZO_SEGS; j++)
+                wsum += get_u16(tile + ex_off + 2 * j);
+            if (exp_bytes != ZO_SEGTAB + 4 * wsum)
+                return ZO_ERR_CORRUPT;
+            for (j = 0; j < ZO_SEGS; j++) {
+                zo_bitr br;
+                uint64_t nw = get_u16(tile + ex_off + 2 * j);
+                br.bytes = tile + ex_off + ZO_SEGTAB + 4 * wpos;
+                br.nbits_total = 32 * nw;
+                br.pos = 0;
+                for (r0 = 0; r0 < nt; r0 += ZO_ROW)
+                for (t8 = 0; t8 < ZO_LANE_ELEMS; t8++) {
+                    int sym;
+                    uint32_t e;
+                    k = r0 + j * ZO_LANE_ELEMS + t8;
+                    if (k >= nt)
+                        break;
+                    st = decode_symbol(&br, &dec, &sym);
+                    if (st != ZO_OK)
+                        return st;
+                    if (sym == ZO_ESC) {
+                        uint32_t bit;
+                        int b;
+                        e = 0;
+                        for (b = 0; b < 8; b++) {
+                            if (!br_get(&br, &bit))
+                                return ZO_ERR_CORRUPT;
+                            e |= bit << b;
+                        }
+                    } else {
+                        e = (uint32_t)(base + sym);
+                    }
+                    y[k] |= (uint16_t)(e << 7);
+                }
+                wpos += nw;
+            }
+        } else {
+            return ZO_ERR_CORRUPT;
+        }
+    }
+    *n_out = nc;
+    return ZO_OK;
+}
+
+int zo_decompress(const uint8_t *stream, const uint64_t *offsets, uint32_t n_chunks, uint16_t *out,
+                  uint64_t n)
+{
+    uint64_t c, elem = 0;
+    if (n_chunks == 0 || stream == NULL || offsets == NULL || (n > 0 && out == NULL))
+        return ZO_ERR_INVALID_ARG;
+    for (c = 0; c < n_chunks; c++) {
+        uint64_t got = 0;
+        int st;
+        if (offsets[c + 1] < offsets[c])
+            return ZO_ERR_CORRUPT;
+        st = decode_chunk(stream + offsets[c], offsets[c + 1] - offsets[c], out + elem, n - elem,
+                          &got);
+        if (st != ZO_OK)
+            return st;
+        elem += got;
+    }
+    return elem == n ? ZO_OK : ZO_ERR_CORRUPT;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Receive side of ReduceScatter: decode k peer chunks, fp32 sum, BF16 out   */
+/* ------------------------------------------------------------------------ */
+static float bf16_to_float(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/*
+ * fp32 -> bf16, round to nearest, ties to even, written out as a choice
+ * between the two neighbouring BF16 values; overflow past the midpoint above
+ * the largest finite value gives infinity.  Reading: every NaN becomes the
+ * canonical quiet NaN 0x7FC0.
+ */
+uint16_t zo_float_to_bf16_rne(float f)
+{
+    uint32_t u, lo, hi;
+    double v, vlo, vhi, dlo, dhi;
+    memcpy(&u, &f, 4);
+    if (isnan(f))
+        return 0x7FC0;
+    lo = u >> 16;
+    if ((lo << 16) == u)
+        return (uint16_t)lo;
+    hi = lo + 1;
+    v = fabs((double)f);
+    vlo = fabs((double)bf16_to_float((uint16_t)lo));
+    if ((hi & 0x7FFF) == 0x7F80)
+        vhi = ldexp(1.0, 128); /* unbounded-exponent neighbour */
+    else
+        vhi = fabs((double)bf16_to_float((uint16_t)hi));
+    dlo = v - vlo;
+    dhi = vhi - v;
+    if (dlo < dhi)
+        return (uint16_t)lo;
+    if (dhi < dlo)
+        return (uint16_t)hi;
+    return (uint16_t)((lo & 1u) ? hi : lo);
+}
+
+/*
+ * peers[p] points at a complete compressed chunk of peer_bytes[p] bytes, all
+ * holding n elements.  out[i] = bf16_rne(((x0[i] + x1[i]) + x2[i]) ... ) with
+ * fp32 additions in rank order.
+ */
+int zo_decompress_reduce(const uint8_t *const *peers, const uint64_t *peer_bytes, uint32_t k,
+                         uint64_t n, uint16_t *out)
+{
+    uint16_t *tmp;
+    float *acc;
+    uint64_t i;
+    uint32_t p;
+    if (k == 0 || peers == NULL || peer_bytes == NULL || (n > 0 && out == NULL))
+        return ZO_ERR_INVALID_ARG;
+    tmp = (uint16_t *)malloc(sizeof(uint16_t) * (n ? n : 1));
+    acc = (float *)malloc(sizeof(float) * (n ? n : 1));
+    for (p = 0; p < k; p++) {
+        uint64_t got = 0;
+        int st = decode_chunk(peers[p], peer_bytes[p], tmp, n, &got);
+        if (st == ZO_OK && got != n)
+            st = ZO_ERR_CORRUPT;
+        if (st != ZO_OK) {
+            free(tmp);
+            free(acc);
+            return st;
+        }
+        for (i = 0; i < n; i++) {
+            if (p == 0)
+                acc[i] = bf16_to_float(tmp[i]);
+            else
+                acc[i] = acc[i] + bf16_to_float(tmp[i]);
+        }
+    }
+    for (i = 0; i < n; i++)
+        out[i] = zo_float_to_bf16_rne(acc[i]);
+    free(tmp);
+    free(acc);
+    return ZO_OK;
+}
+
+/* Version of the stream format this reference writes and reads. */
+int zo_format_version(void) { return ZO_VERSION; }

@@ -1,0 +1,368 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+None of these compares the oracle with itself: each check uses a library
+routine (scipy's normal distribution, numpy float32 arithmetic, torch's BF16
+cast), a closed form, an exhaustive optimum, an independent stream reader
+(tests/zstream.py) or a figure printed on the pages.
+
+Passages: "ZipCCL: Efficient Lossless Data Compression of Communication
+Collectives for Accelerating LLM Training" -- abstract (exponent coding of
+near-Gaussian tensors, no online statistics; lossless), shd-paper summary key
+design (short codes for frequent exponents, from the Gaussian density),
+Fig. 6 caption (about 11 bits per value, up to 31% smaller), Fig. 3 / Fig. 5
+(ReduceScatter receive side: decompress then reduce).
+"""
+from __future__ import annotations
+
+import heapq
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy import special, stats
+
+import oracle
+import workloads
+import zstream
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def golden(name):
+    vals = {}
+    with open(os.path.join(HERE, "golden", name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, v = line.split()
+                vals[k] = float(v)
+    return vals
+
+
+def bf16_to_f32(x: np.ndarray) -> np.ndarray:
+    return (x.astype(np.uint32) << 16).view(np.float32)
+
+
+# ----------------------------------------------------------------- pmf / entropy
+def scipy_pmf(sigma):
+    """P(biased exponent = e) for N(0, sigma^2) from scipy: 2 (Phi(b) - Phi(a)) on each binade,
+    taken through scipy's erf below 1 standard deviation and its survival function above."""
+    r2 = math.sqrt(2.0)
+    p = np.zeros(256)
+    p[0] = special.erf(2.0 ** -126 / sigma / r2)
+    for e in range(1, 255):
+        a, b = 2.0 ** (e - 127) / sigma, 2.0 ** (e - 126) / sigma
+        if b < 1.0:
+            p[e] = special.erf(b / r2) - special.erf(a / r2)
+        else:
+            p[e] = 2.0 * (stats.norm.sf(a) - stats.norm.sf(b))
+    return p
+
+
+@pytest.mark.parametrize("sigma", [1e-3, 0.02, 1.0, 1.37, 300.0, 2.0 ** -100])
+def test_pmf_matches_scipy_normal(sigma):
+    p = oracle.exponent_pmf(sigma)
+    q = scipy_pmf(sigma)
+    # erf differences: absolute accuracy ~1e-16 everywhere, relative 1e-9 on the bulk of the mass
+    assert np.all(np.abs(p - q) < 1e-15)
+    big = q > 1e-6
+    assert np.allclose(p[big], q[big], rtol=1e-9, atol=0)
+    assert abs(p.sum() - 1.0) < 1e-12
+
+
+def test_entropy_is_scale_invariant_and_in_closed_form_band():
+    # over the normal range the pmf only shifts with log2(sigma): H depends on the phase alone
+    hs = []
+    for r in range(64):
+        s = 2.0 ** (r / 64)
+        h = oracle.entropy_bits(oracle.exponent_pmf(s))
+        h2 = oracle.entropy_bits(oracle.exponent_pmf(s * 2.0 ** -20))
+        assert abs(h - h2) < 1e-9
+        q = scipy_pmf(s)
+        hq = -np.sum(q[q > 0] * np.log2(q[q > 0]))
+        assert abs(h - hq) < 1e-8
+        hs.append(h)
+    assert 2.5420 < min(hs) and max(hs) < 2.5465
+    h002 = oracle.entropy_bits(oracle.exponent_pmf(0.02))
+    assert abs(h002 - 2.5453) < 1e-4
+    p = oracle.exponent_pmf(0.02)
+    assert int(np.argmax(p)) == 121 and abs(p[121] - 0.3165) < 1e-4
+
+
+# ------------------------------------------------------------ code construction
+def optimal_limited_cost(w, L):
+    """Exact minimum of sum w_i l_i over all length vectors with Kraft <= 1, l_i <= L (DP)."""
+    units = 1 << L
+    INF = float("inf")
+    dp = [INF] * (units + 1)
+    dp[0] = 0.0
+    for wi in w:
+        nd = [INF] * (units + 1)
+        for k in range(units + 1):
+            if dp[k] == INF:
+                continue
+            for l in range(1, L + 1):
+                k2 = k + (1 << (L - l))
+                if k2 <= units and dp[k] + wi * l < nd[k2]:
+                    nd[k2] = dp[k] + wi * l
+        dp = nd
+    return min(dp)
+
+
+def huffman_cost(w):
+    h = [(x, i) for i, x in enumerate(w)]
+    heapq.heapify(h)
+    cost, n = 0.0, len(w)
+    while len(h) > 1:
+        a, b = heapq.heappop(h), heapq.heappop(h)
+        cost += a[0] + b[0]
+        heapq.heappush(h, (a[0] + b[0], n))
+        n += 1
+    return cost
+
+
+def kraft(lens, L=10):
+    return sum(2 ** (L - l) for l in lens)
+
+
+def test_phase_tables_complete_and_optimal():
+    offs, tabs = oracle.phase_tables()
+    for r in range(16):
+        lens = tabs[r]
+        assert len(lens) == 16 and all(1 <= l <= 10 for l in lens)
+        assert kraft(lens) == 1024, "a complete prefix code"
+        p = scipy_pmf(2.0 ** (r / 16))
+        b = offs[r] + 127
+        w = list(p[b:b + 15]) + [1.0 - p[b:b + 15].sum()]
+        cost = sum(wi * li for wi, li in zip(w, lens))
+        assert abs(cost - optimal_limited_cost(w, 10)) < 1e-12
+        # window = 15 consecutive exponents of largest mass
+        masses = [p[s:s + 15].sum() for s in range(0, 241)]
+        assert b == int(np.argmax(masses))
+        # the code sits within 0.06 bits of the entropy of the Gaussian exponent
+        h = -np.sum(p[p > 0] * np.log2(p[p > 0]))
+        assert 0 < cost + w[15] * 8 - h < 0.06
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_package_merge_optimal_on_random_weights(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(2, 17))
+    w = list(rng.dirichlet(np.full(n, 0.3)) + 1e-9)
+    L = int(max(math.ceil(math.log2(n)), rng.integers(2, 8)))
+    lens = oracle.package_merge(w, L)
+    assert kraft(lens, L) <= (1 << L) and max(lens) <= L
+    cost = sum(a * b for a, b in zip(w, lens))
+    assert abs(cost - optimal_limited_cost(w, L)) < 1e-12
+    big = oracle.package_merge(w, 16) if n <= 16 else None
+    if big is not None and max(big) < 16:
+        assert abs(sum(a * b for a, b in zip(w, big)) - huffman_cost(w)) < 1e-12
+
+
+def test_phase_tables_robust_to_tiny_weight_perturbation():
+    # the frozen lengths do not sit on a knife edge: 1e-9 relative noise in the pmf changes nothing
+    offs, tabs = oracle.phase_tables()
+    rng = np.random.default_rng(7)
+    for r in range(16):
+        p = oracle.exponent_pmf(2.0 ** (r / 16))
+        b = offs[r] + 127
+        w = np.array(list(p[b:b + 15]) + [1.0 - p[b:b + 15].sum()])
+        for _ in range(5):
+            wp = w * (1.0 + 1e-9 * rng.standard_normal(16))
+            assert oracle.package_merge(wp, 10) == tabs[r]
+
+
+# ------------------------------------------------------------ scale selection
+def test_scale_constant_closed_form():
+    # mean of floor(log2|Z|) over a uniform phase = E[log2|Z|] - 1/2, E[log2|Z|] = -(gamma + ln 2)/(2 ln 2)
+    c0 = 0.5 + (np.euler_gamma + math.log(2)) / (2 * math.log(2))
+    assert abs(c0 - 3541 / 2500) < 5e-5
+    # and it matches the closed-form pmf averaged over the phase
+    vals = []
+    for r in range(32):
+        s = 2.0 ** (r / 32)
+        p = scipy_pmf(s)
+        m = np.sum(np.arange(1, 255) * p[1:255]) / p[1:255].sum()
+        vals.append(127 + math.log2(s) - m)
+    assert abs(np.mean(vals) - c0) < 1e-4
+
+
+@pytest.mark.parametrize("sigma", [1e-6, 1e-3, 0.02, 1.0, 7.0, 100.0])
+def test_select_q_tracks_sigma(sigma):
+    x = workloads.gaussian_bf16(1 << 18, sigma, 5, int(sigma * 1e6) % 1000)
+    q = oracle.select_q(x)
+    assert abs(q - 16 * math.log2(sigma)) <= 2.0
+    assert oracle.q_from_sigma(sigma) == math.floor(16 * math.log2(sigma) + 0.5)
+
+
+def test_select_q_small_and_special_chunks():
+    assert oracle.select_q(np.zeros(100, np.uint16)) == 0          # nothing but zeros
+    assert oracle.select_q(np.full(10, 0x7F80, np.uint16)) == 0    # nothing but inf
+    x = np.full(7, 0x3F80, np.uint16)                              # 1.0: e = 127
+    # q = round(16 (127 - 127 + c0)) = round(22.6624) = 23
+    assert oracle.select_q(x) == 23
+
+
+def test_base_clamped_to_valid_window():
+    assert oracle.base_for_q(-32768) == 0
+    assert oracle.base_for_q(32767) == 240
+    offs, _ = oracle.phase_tables()
+    assert oracle.base_for_q(0) == 127 + offs[0]
+    assert oracle.base_for_q(-90) == math.floor(-90 / 16) + 127 + offs[(-90) % 16]
+
+
+# ------------------------------------------------------------ round trips
+def roundtrip(x, chunk_elems=None, hint=None, parse=True):
+    s, offs = oracle.compress(x, chunk_elems, hint)
+    y = oracle.decompress(s, offs, x.size)
+    assert np.array_equal(y, x)
+    if parse:
+        chunks = zstream.parse_stream(s, offs)
+        got = np.concatenate([c.values for c in chunks]) if chunks else np.zeros(0, np.uint16)
+        assert np.array_equal(got, x), "independent reader disagrees with the input"
+    assert len(s) <= oracle.max_compressed_bytes(chunk_elems or [x.size])
+    return s, offs
+
+
+def test_all_bf16_patterns_roundtrip():
+    w = workloads.all_patterns()
+    roundtrip(w.x)
+
+
+def test_patterns_spliced_into_gaussian_take_the_escape():
+    g = workloads.gaussian_bf16(1 << 20, 0.02, 11)
+    pos = np.random.default_rng(3).choice(g.size, 65536, replace=False)
+    g[pos] = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    s, offs = roundtrip(g, parse=False)
+    ch = zstream.parse_chunk(s)
+    assert all(t.mode == 0 for t in ch.tiles), "coded mode carries every exponent through ESC"
+    assert sum(t.escapes for t in ch.tiles) > 30000
+    assert np.array_equal(ch.values, g)
+
+
+@pytest.mark.parametrize("n", [0, 1, 7, 8, 9, 255, 256, 257, 2047, 32767, 32768, 32769, 65536 + 300])
+def test_edge_sizes(n):
+    x = workloads.gaussian_bf16(n, 0.5, 21, n)
+    roundtrip(x)
+
+
+@pytest.mark.parametrize("fill", [0x0000, 0x8000, 0x7FC0, 0xFFFF, 0x7F80, 0xFF80, 0x0001, 0x807F])
+def test_constant_special_chunks(fill):
+    x = np.full(40000, fill, np.uint16)
+    roundtrip(x)
+
+
+def test_denormal_only_chunk():
+    rng = np.random.default_rng(4)
+    x = rng.integers(0, 128, size=50000).astype(np.uint16) | (rng.integers(0, 2, 50000).astype(np.uint16) << 15)
+    roundtrip(x)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_ragged_chunk_mixes(seed):
+    w = workloads.random_chunks(seed, n_chunks=int(3 + seed), max_elems=70000)
+    hints = None
+    if seed % 2:
+        hints = [s if i % 2 else 0.0 for i, s in enumerate(w.sigma)]
+    roundtrip(w.x, w.chunk_elems, hints)
+
+
+def test_uniform_patterns_go_raw_with_bounded_expansion():
+    x = np.random.default_rng(9).integers(0, 65536, size=100000, dtype=np.uint16)
+    s, offs = roundtrip(x)
+    ch = zstream.parse_chunk(s)
+    assert all(t.mode == 1 for t in ch.tiles)
+    assert len(s) <= 2 * x.size + 32 + 16 + 4 * 16 + 32 * len(ch.tiles)
+
+
+# ------------------------------------------------------------ sizes and ratio
+def test_size_identity_pr1():
+    w = workloads.pr1()
+    s, offs = oracle.compress(w.x)
+    ch = zstream.parse_chunk(s)
+    lens = ch.lens
+    e = (w.x >> 7) & 0xFF
+    sym = e.astype(np.int64) - ch.base
+    sym[(sym < 0) | (sym > 14)] = 15
+    Lx = np.array(lens)[sym] + np.where(sym == 15, 8, 0)
+    total_payload = 0
+    for t, tile in enumerate(ch.tiles):
+        assert tile.mode == 0
+        seg = ((np.arange(tile.n) % 256) // 8)
+        tl = Lx[t * 32768: t * 32768 + tile.n]
+        for j in range(32):
+            bits = int(tl[seg == j].sum())
+            assert tile.seg_bits_used[j] == bits
+            assert tile.seg_words[j] == (bits + 31) // 32
+            total_payload += bits
+    # total = payload (word-rounded per segment) + s/m plane + documented metadata
+    expect = 32 + zstream.pad16(4 * len(ch.tiles))
+    for tile in ch.tiles:
+        expect += 16 + zstream.pad16(tile.n) + zstream.pad16(64 + 4 * sum(tile.seg_words))
+    assert len(s) == expect
+    word_bits = sum(32 * sum(t.seg_words) for t in ch.tiles)
+    assert 0 <= word_bits - total_payload < 32 * 32 * len(ch.tiles)
+
+
+def test_pr1_entropy_and_bits_per_value():
+    w = workloads.pr1()
+    e = ((w.x >> 7) & 0xFF).astype(np.int64)
+    cnt = np.bincount(e, minlength=256) / e.size
+    h_emp = -np.sum(cnt[cnt > 0] * np.log2(cnt[cnt > 0]))
+    p = scipy_pmf(0.02)
+    h = -np.sum(p[p > 0] * np.log2(p[p > 0]))
+    assert abs(h_emp - h) / h < 0.01
+    s, _ = oracle.compress(w.x)
+    bpv = 8.0 * len(s) / w.n
+    assert bpv <= 1.01 * (8.0 + h)
+    g = golden("paper_figures.txt")
+    assert bpv < g["bits_per_value_upper"]
+    assert 100.0 * (1.0 - len(s) / (2 * w.n)) > g["size_reduction_percent"]
+
+
+# ------------------------------------------------------------ decompress_reduce
+def torch_bf16_rne(f32: np.ndarray) -> np.ndarray:
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(f32, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_rne_matches_torch_cast():
+    rng = np.random.default_rng(12)
+    u = rng.integers(0, 2 ** 32, size=20000, dtype=np.uint64).astype(np.uint32)
+    # force ties and near-overflow cases
+    u[:2000] = (u[:2000] & 0xFFFF0000) | 0x8000
+    u[2000:2100] = 0x7F7F8000 + np.arange(100, dtype=np.uint32)
+    f = u.view(np.float32)
+    ours = np.array([oracle.float_to_bf16_rne(float(v)) for v in f], dtype=np.uint16)
+    ref = torch_bf16_rne(f)
+    nan = np.isnan(f)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.all(ours[nan] == 0x7FC0)
+
+
+def test_reduce_matches_numpy_float32_left_fold():
+    rng = np.random.default_rng(13)
+    k, n = 5, 40000
+    xs = [workloads.gaussian_bf16(n, 10.0 ** rng.uniform(-3, 1), 77, p) for p in range(k)]
+    xs[2][:50] = np.array([0x7F80, 0xFF80, 0x7FC1, 0x0001, 0x8001] * 10, np.uint16)
+    chunks = [oracle.compress(x)[0] for x in xs]
+    out = oracle.decompress_reduce(chunks, n)
+    acc = bf16_to_f32(xs[0]).copy()
+    for p in range(1, k):
+        acc = (acc + bf16_to_f32(xs[p])).astype(np.float32)
+    ref = torch_bf16_rne(acc)
+    nan = np.isnan(acc)
+    assert np.array_equal(out[~nan], ref[~nan])
+    assert np.all(out[nan] == 0x7FC0)
+
+
+def test_reduce_k1_is_decode_and_negation_cancels():
+    x = workloads.gaussian_bf16(50000, 0.3, 31)
+    s, _ = oracle.compress(x)
+    assert np.array_equal(oracle.decompress_reduce([s], x.size), x)
+    neg = x ^ np.uint16(0x8000)
+    s2, _ = oracle.compress(neg)
+    y = oracle.decompress_reduce([s, s2], x.size)
+    assert np.all(y == 0)
