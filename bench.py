@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 ZipCCL BF16 exponent-coding hot path.
+
+Workload (one step = every stage of the path once): the gradient bucket of
+67,108,864 BF16 values from N(0, 1e-3^2) in 8 per-destination chunks is
+compressed (scale select + encode with look-back offsets) and decompressed,
+and 8 peer chunks of 8,388,608 values each (independently seeded, received
+compressed) are decompressed and summed in fp32 into one BF16 shard.
+
+Metric: GB/s of uncompressed BF16 through the step (2 bytes per value
+compressed + 2 per value decompressed + 2 per peer value reduced) per second
+of device time; the per-stage rates, the compression ratio and the dominant
+kernel's fraction of the measured HBM bandwidth ride along.  Inputs are
+resident in HBM when timing starts; L2 is flushed before every timed step.
+``e2e`` times the same step through the public API with pinned host buffers
+and the host<->device copies inside the timed region.
+
+``--impl reference`` times the plain single-threaded CPU oracle on a bounded
+sample of the same workload instead.
+
+Launch: ``python bench.py [--gpus N --steps K --warmup W]``; for N > 1 under
+torchrun, each rank runs its own bucket (weak scaling, no collective: the
+chunks are independent), and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "compress/decompress GB/s (uncompressed bf16) and % of HBM roofline; compression ratio"
+UNIT = "GB/s"
+N_BUCKET = 67_108_864
+RANKS = 8
+PEER_N = 8_388_608
+K_PEERS = 8
+L2_FLUSH_BYTES = 2 * 129 * 1024 * 1024
+KERNELS_PER_STEP = 6  # select, encode, decode-prep, decode, reduce-prep, reduce
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def workload_config(n_gpus: int) -> dict:
+    return {
+        "workload": "gradient bucket: 67,108,864 bf16 from N(0, 1e-3^2) in 8 per-destination chunks "
+                    "(compress + decompress) + decompress_reduce of 8 peer chunks x 8,388,608 (fp32 sum, rank order)",
+        "n_elems": N_BUCKET, "chunks": RANKS, "reduce_peers": K_PEERS, "reduce_elems": PEER_N,
+        "parallelism": f"replicas x{n_gpus} (independent buckets, no collective)",
+        "l2": "flushed before every timed step (256 MiB write)",
+    }
+
+
+def peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "src": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "src": "fallback"}
+
+
+def sources_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "lossless_bf16_tensor_zipccl_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on these sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        e = d.get(kernel)
+        if e and e.get("sources_sha") == sources_sha():
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ reference arm / CPU baseline
+def oracle_sample(seed_offset: int = 0):
+    """A bounded sample of the workload for the CPU oracle: one 8,388,608-value
+    chunk of the bucket (compress + decompress) and the reduce of 8 peers over
+    1,048,576 values each."""
+    import oracle
+    import workloads
+    oracle.lib()
+    x = workloads.gaussian_bf16(N_BUCKET // RANKS, 1e-3, 100 + seed_offset, 0)
+    peers = [workloads.gaussian_bf16(1 << 20, 1e-3, 100 + seed_offset, 1000 + p) for p in range(K_PEERS)]
+    peer_chunks = [oracle.compress(p)[0] for p in peers]
+    return x, peer_chunks
+
+
+def oracle_step(x, peer_chunks) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    s, offs = oracle.compress(x)
+    oracle.decompress(s, offs, x.size)
+    oracle.decompress_reduce(peer_chunks, 1 << 20)
+    return time.perf_counter() - t0
+
+
+def oracle_sample_bytes() -> int:
+    return 2 * (N_BUCKET // RANKS) * 2 + 2 * K_PEERS * (1 << 20)
+
+
+SAMPLE_DESC = ("oracle compress + decompress of one 8,388,608-value chunk of the bucket and decompress_reduce "
+               "of 8 peers x 1,048,576 values; same distribution, GB/s of uncompressed bf16")
+
+
+def cpu_baseline(repeats: int = 3) -> dict:
+    x, pc = oracle_sample()
+    ts = [oracle_step(x, pc) for _ in range(repeats)]
+    t = statistics.median(ts)
+    return {"value": oracle_sample_bytes() / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": SAMPLE_DESC + f"; median of {repeats}"}
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    x, pc = oracle_sample()
+    for _ in range(args.warmup):
+        oracle_step(x, pc)
+    ts = [oracle_step(x, pc) for _ in range(args.steps)]
+    total = sum(ts)
+    value = oracle_sample_bytes() * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16/u8 (integer coding), f32 reduce",
+        "data": "synthetic (seeded numpy PCG64)", "config": workload_config(args.gpus),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": SAMPLE_DESC},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank: int, world: int):
+    import torch
+
+    import lossless_bf16_tensor_zipccl_gb300 as zc
+    import workloads
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    zc.load()
+    seed = 100 + 10007 * rank
+    wl = workloads.gradient(seed=seed)
+    peers = workloads.gradient_peers(seed=seed)
+    chunk_elems = wl.chunk_elems
+    x = torch.from_numpy(wl.x.view(np.int16)).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    # received peer chunks: each peer's chunk compressed on its own (prepared outside timing)
+    peer_chunks = []
+    for p in peers:
+        c = zc.compress(torch.from_numpy(p.view(np.int16)).to(dev))
+        peer_chunks.append(c.data[: c.nbytes()].clone())
+    peer_bytes = [int(t.numel()) for t in peer_chunks]
+
+    cap = zc.zipccl_max_compressed_bytes(chunk_elems)
+    out = torch.empty(cap, dtype=torch.uint8, device=dev)
+    offs = torch.empty(len(chunk_elems) + 1, dtype=torch.int64, device=dev)
+    ws_c = torch.empty(zc.zipccl_compress_workspace_bytes(chunk_elems), dtype=torch.uint8, device=dev)
+    ws_d = torch.empty(zc.zipccl_decompress_workspace_bytes(N_BUCKET, RANKS), dtype=torch.uint8, device=dev)
+    ws_r = torch.empty(zc.zipccl_reduce_workspace_bytes(K_PEERS), dtype=torch.uint8, device=dev)
+    dec = torch.empty(N_BUCKET, dtype=torch.int16, device=dev)
+    red = torch.empty(PEER_N, dtype=torch.int16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def check(st, what):
+        if st != zc.OK:
+            raise zc.ZipcclError(st, what)
+
+    def do_compress():
+        check(zc.zipccl_compress(x.data_ptr(), N_BUCKET, chunk_elems, None, out.data_ptr(), cap, offs.data_ptr(),
+                                 ws_c.data_ptr(), ws_c.numel(), sp), "compress")
+
+    def do_decompress():
+        check(zc.zipccl_decompress(out.data_ptr(), offs.data_ptr(), RANKS, dec.data_ptr(), N_BUCKET,
+                                   ws_d.data_ptr(), ws_d.numel(), sp), "decompress")
+
+    def do_reduce():
+        check(zc.zipccl_decompress_reduce([t.data_ptr() for t in peer_chunks], peer_bytes, K_PEERS, PEER_N,
+                                          red.data_ptr(), ws_r.data_ptr(), ws_r.numel(), sp), "reduce")
+
+    stages = [("compress", do_compress), ("decompress", do_decompress), ("decompress_reduce", do_reduce)]
+    for _ in range(args.warmup):
+        for _, f in stages:
+            f()
+    torch.cuda.synchronize(dev)
+    for ws in (ws_c, ws_d, ws_r):
+        st = zc.zipccl_get_device_status(ws.data_ptr(), sp)
+        if st != zc.OK:
+            raise zc.ZipcclError(st, "device status after warm-up")
+    if not torch.equal(dec, x):
+        raise RuntimeError("round trip mismatch in the benchmark")
+    comp_bytes = int(offs[-1].item())
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)          # untimed: L2 flush
+            ev[i][0].record(stream)
+            for j, (_, f) in enumerate(stages):
+                f()
+                ev[i][j + 1].record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    stage_ms = {name: [ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)]
+                for j, (name, _) in enumerate(stages)}
+    step_ms = [sum(stage_ms[n][i] for n, _ in stages) for i in range(args.steps)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    unc = {"compress": 2 * N_BUCKET, "decompress": 2 * N_BUCKET, "decompress_reduce": 2 * K_PEERS * PEER_N}
+    algo = {"compress": 2 * N_BUCKET + comp_bytes, "decompress": comp_bytes + 2 * N_BUCKET,
+            "decompress_reduce": sum(peer_bytes) + 2 * PEER_N}
+    step_bytes = sum(unc.values())
+    value = world * step_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    pk = peaks()
+    stage_info = {}
+    for name, _ in stages:
+        ms = sum(stage_ms[name]) / args.steps
+        stage_info[name] = {"ms": ms, "gbs_uncompressed": unc[name] / (ms * 1e-3) / 1e9,
+                            "hbm_gbs_algorithmic": algo[name] / (ms * 1e-3) / 1e9,
+                            "hbm_frac_of_measured": algo[name] / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
+    dom = max(stage_info, key=lambda k: stage_info[k]["ms"])
+    kernel_of = {"compress": "zc_encode_kernel", "decompress": "zc_decode_kernel", "decompress_reduce": "zc_reduce_kernel"}
+    ach = stage_info[dom]["hbm_gbs_algorithmic"]
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, zc, torch, dev, wl, peer_chunks, peer_bytes, comp_bytes)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u16/u8 (integer coding), f32 reduce", "data": "synthetic (seeded numpy PCG64)",
+        "config": workload_config(world),
+        "compression_ratio": comp_bytes / (2 * N_BUCKET), "bits_per_value": 8 * comp_bytes / N_BUCKET,
+        "stages": stage_info,
+        "roofline": {"bound": "hbm", "kernel": kernel_of[dom], "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / pk["hbm_gbs"], "traffic": traffic_for(kernel_of[dom]),
+                     "peak_src": pk["src"], "timing": "CUDA events around the C-ABI call (includes its prep kernel)"},
+        "clocks": clk.summary(),
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure_e2e(args, zc, torch, dev, wl, peer_chunks, peer_bytes, comp_bytes):
+    """Same step through the torch-level public API with pinned host buffers."""
+    h_x = torch.from_numpy(wl.x.view(np.int16)).pin_memory()
+    h_peers = [t.cpu().pin_memory() for t in peer_chunks]
+    h_stream = torch.empty(comp_bytes, dtype=torch.uint8).pin_memory()
+    h_offs = torch.empty(RANKS + 1, dtype=torch.int64).pin_memory()
+    h_dec = torch.empty(N_BUCKET, dtype=torch.int16).pin_memory()
+    h_red = torch.empty(PEER_N, dtype=torch.int16).pin_memory()
+    d_x = torch.empty(N_BUCKET, dtype=torch.int16, device=dev)
+    d_peers = [torch.empty_like(t, device=dev) for t in h_peers]
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        d_x.copy_(h_x, non_blocking=True)
+        for d, h in zip(d_peers, h_peers):
+            d.copy_(h, non_blocking=True)
+        c = zc.compress(d_x, wl.chunk_elems)
+        y = zc.decompress(c)
+        r = zc.decompress_reduce(d_peers, PEER_N)
+        h_offs.copy_(c.offsets, non_blocking=True)
+        h_stream.copy_(c.data[:comp_bytes], non_blocking=True)
+        h_dec.copy_(y.view(torch.int16), non_blocking=True)
+        h_red.copy_(r.view(torch.int16), non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.steps
+    if int(h_offs[-1]) != comp_bytes or not torch.equal(h_dec, h_x):
+        raise RuntimeError("e2e round trip mismatch")
+    h2d = 2 * N_BUCKET + sum(peer_bytes)
+    d2h = comp_bytes + 8 * (RANKS + 1) + 2 * N_BUCKET + 2 * PEER_N
+    step_bytes = 2 * N_BUCKET + 2 * N_BUCKET + 2 * K_PEERS * PEER_N
+    return {"value": step_bytes / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

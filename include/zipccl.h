@@ -1,0 +1,138 @@
+/*
+ * zipccl.h -- C ABI of the GB300 (sm_103a) ZipCCL BF16 exponent-coding path.
+ *
+ * The operations follow "ZipCCL: Efficient Lossless Data Compression of
+ * Communication Collectives for Accelerating LLM Training":
+ *   - abstract, technique (1) and the shd-paper summary's key design: BF16
+ *     communication tensors are near-Gaussian, so the 8-bit exponent is
+ *     entropy-coded with a code derived from the Gaussian density, with no
+ *     online statistics;  Fig. 6 caption: sign and mantissa stay raw and a
+ *     value shrinks to about 11 bits;
+ *   - abstract, technique (2): GPU compressor/decompressor kernels with a
+ *     communication-aware data layout -- here one self-contained compressed
+ *     chunk per destination rank, back to back in one buffer;
+ *   - Fig. 3 and Fig. 5 captions: the receive side of zipcclReduceScatter
+ *     decompresses the peers' chunks and reduces them.
+ * The stream format (v1) is defined by this library; the pages fix none.
+ *
+ * Conventions for every call:
+ *   - Pointers named d_* are device memory on the current CUDA device, owned
+ *     by the caller.  The library allocates and frees nothing on the device.
+ *   - d_* base pointers must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void*.  Calls are asynchronous and
+ *     stream-ordered; they never synchronize unless the name says so.
+ *   - Argument errors are returned synchronously, before any launch.
+ *   - Data-dependent errors (a corrupt stream, a look-back that timed out)
+ *     are recorded by the kernels in a status word at the start of the
+ *     workspace; zipccl_get_device_status reads it.  Each compress,
+ *     decompress or decompress_reduce call clears it first, so read it after
+ *     the call you want to check.  On such an error outputs are undefined
+ *     but every access stays inside the caller's buffers.
+ *   - A workspace must not be shared by calls that may run concurrently.
+ */
+#ifndef ZIPCCL_H
+#define ZIPCCL_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ZIPCCL_OK = 0,
+    ZIPCCL_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, sum mismatch */
+    ZIPCCL_ERR_CAPACITY = 2,    /* output or workspace smaller than required */
+    ZIPCCL_ERR_CORRUPT = 3,     /* stream fails validation (device status) */
+    ZIPCCL_ERR_VERSION = 4,     /* stream written by another format version */
+    ZIPCCL_ERR_TIMEOUT = 5,     /* a bounded device wait gave up (device status) */
+    ZIPCCL_ERR_CUDA = 6         /* a CUDA runtime call failed */
+} zipccl_status;
+
+/* Format version written and read by this library (1). */
+int zipccl_format_version(void);
+
+/* Static, human-readable name of a status code. */
+const char *zipccl_status_string(int status);
+
+/*
+ * Exact worst-case compressed size of a chunk layout: every tile stored with
+ * raw exponents (bounded expansion).  chunk_elems: host array of n_chunks
+ * element counts.  *out_bytes receives the bound.  Host only.
+ */
+zipccl_status zipccl_max_compressed_bytes(const uint64_t *chunk_elems, uint32_t n_chunks,
+                                          uint64_t *out_bytes);
+
+/* Workspace bytes needed by zipccl_compress for this chunk layout. Host only. */
+zipccl_status zipccl_compress_workspace_bytes(const uint64_t *chunk_elems, uint32_t n_chunks,
+                                              uint64_t *out_bytes);
+
+/* Workspace bytes needed by zipccl_decompress for n elements in n_chunks chunks. */
+zipccl_status zipccl_decompress_workspace_bytes(uint64_t n, uint32_t n_chunks, uint64_t *out_bytes);
+
+/* Workspace bytes needed by zipccl_decompress_reduce for k peers. */
+zipccl_status zipccl_reduce_workspace_bytes(uint32_t k, uint64_t *out_bytes);
+
+/*
+ * Compress n BF16 words (d_in, bit patterns as uint16) split into n_chunks
+ * per-destination chunks: chunk c is the next chunk_elems[c] words (host
+ * array, sum == n, n_chunks >= 1, each chunk < 2^31 words; empty chunks are
+ * allowed and produce a header-only chunk).
+ * sigma_hint: host array of n_chunks floats or NULL.  A value > 0 fixes the
+ * Gaussian scale of that chunk's code; otherwise the scale is taken from a
+ * fixed sample of the chunk's exponents (no histogram pass).
+ * d_out receives the chunks back to back, each a self-contained stream that
+ * can be sent alone; out_capacity must be >= zipccl_max_compressed_bytes.
+ * d_chunk_offsets (device, n_chunks + 1 uint64) receives each chunk's byte
+ * offset in d_out and, last, the total size.  d_ws: workspace of at least
+ * zipccl_compress_workspace_bytes bytes.
+ */
+zipccl_status zipccl_compress(const uint16_t *d_in, uint64_t n, const uint64_t *chunk_elems,
+                              uint32_t n_chunks, const float *sigma_hint, void *d_out,
+                              uint64_t out_capacity, uint64_t *d_chunk_offsets, void *d_ws,
+                              uint64_t ws_bytes, void *stream);
+
+/*
+ * Decompress n_chunks chunks from d_stream into n BF16 words at d_out,
+ * bit-identical to the compressed input.  d_chunk_offsets (device,
+ * n_chunks + 1) are the offsets compress wrote; the stream must hold
+ * d_chunk_offsets[n_chunks] bytes.  The chunks' element counts are read from
+ * their headers and must sum to n (else ZIPCCL_ERR_CORRUPT in the device
+ * status).  d_ws: at least zipccl_decompress_workspace_bytes bytes.
+ */
+zipccl_status zipccl_decompress(const void *d_stream, const uint64_t *d_chunk_offsets,
+                                uint32_t n_chunks, uint16_t *d_out, uint64_t n, void *d_ws,
+                                uint64_t ws_bytes, void *stream);
+
+/*
+ * Receive side of a reduce-scatter: d_peer_chunks is a host array of k
+ * (1 <= k <= 16) device pointers, in rank order, each to one compressed
+ * chunk of n elements and peer_chunk_bytes[p] bytes (host array).
+ * d_out[i] = bf16_rne(((x0[i] + x1[i]) + x2[i]) ... + x_{k-1}[i]) with every
+ * addition in fp32 (round to nearest even, subnormals kept); a NaN result is
+ * written as 0x7FC0.  d_ws: at least zipccl_reduce_workspace_bytes bytes.
+ */
+zipccl_status zipccl_decompress_reduce(const void *const *d_peer_chunks,
+                                       const uint64_t *peer_chunk_bytes, uint32_t k, uint64_t n,
+                                       uint16_t *d_out, void *d_ws, uint64_t ws_bytes,
+                                       void *stream);
+
+/*
+ * Synchronizes `stream`, then returns the status the kernels of the last call
+ * on this workspace recorded (ZIPCCL_OK, ZIPCCL_ERR_CORRUPT,
+ * ZIPCCL_ERR_VERSION, ZIPCCL_ERR_TIMEOUT), or ZIPCCL_ERR_CUDA.
+ */
+zipccl_status zipccl_get_device_status(const void *d_ws, void *stream);
+
+/*
+ * The code this library builds for scale phase r = q mod 16 (0..15): the
+ * window start relative to floor(q/16) + 127 and the 16 code lengths
+ * (symbols 0..14 = window exponents, 15 = escape).  Host only.
+ */
+zipccl_status zipccl_codebook_phase(int phase, int *base_offset, uint8_t *lens16);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZIPCCL_H */

@@ -1,0 +1,278 @@
+"""GB300 (sm_103a) ZipCCL BF16 exponent coding: Python binding of libzipccl.
+
+"ZipCCL: Efficient Lossless Data Compression of Communication Collectives for
+Accelerating LLM Training" (abstract; Fig. 3, 5, 6 captions): BF16 tensors are
+compressed losslessly by entropy-coding their exponents with a code derived
+from the Gaussian law; sign and mantissa stay raw; each destination rank's
+chunk is a self-contained stream; the receive side of a reduce-scatter
+decompresses k peer chunks and sums them.
+
+This module only marshals arguments to the C ABI in ``include/zipccl.h``.
+Every step of compression and decompression runs in the library's CUDA
+kernels; there is no CPU path.  PyTorch provides device memory and streams.
+
+Low-level names mirror the C ABI (``zipccl_compress`` ...) and take raw
+pointers; ``compress`` / ``decompress`` / ``decompress_reduce`` are the same
+calls on torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+__all__ = [
+    "ZipcclError", "load", "library_path", "zipccl_format_version", "zipccl_status_string",
+    "zipccl_max_compressed_bytes", "zipccl_compress_workspace_bytes", "zipccl_decompress_workspace_bytes",
+    "zipccl_reduce_workspace_bytes", "zipccl_compress", "zipccl_decompress", "zipccl_decompress_reduce",
+    "zipccl_get_device_status", "zipccl_codebook_phase", "compress", "decompress", "decompress_reduce",
+    "Compressed", "EXPORTED_SYMBOLS",
+]
+
+OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_CORRUPT, ERR_VERSION, ERR_TIMEOUT, ERR_CUDA = range(7)
+EXPORTED_SYMBOLS = [
+    "zipccl_format_version", "zipccl_status_string", "zipccl_max_compressed_bytes",
+    "zipccl_compress_workspace_bytes", "zipccl_decompress_workspace_bytes", "zipccl_reduce_workspace_bytes",
+    "zipccl_compress", "zipccl_decompress", "zipccl_decompress_reduce", "zipccl_get_device_status",
+    "zipccl_codebook_phase",
+]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class ZipcclError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {_status_name(status)} ({status})")
+        self.status = status
+
+
+def _status_name(st: int) -> str:
+    try:
+        return load().zipccl_status_string(int(st)).decode()
+    except Exception:  # pragma: no cover - only when the library itself is unusable
+        return "status"
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libzipccl.so (building it with nvcc when missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if build_if_missing:
+            path = _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libzipccl is not built ({path}); run lossless_bf16_tensor_zipccl_gb300/build.py")
+        L = ctypes.CDLL(path)
+        u64, u32, vp = ctypes.c_uint64, ctypes.c_uint32, ctypes.c_void_p
+        u64p = ctypes.POINTER(ctypes.c_uint64)
+        L.zipccl_format_version.restype = ctypes.c_int
+        L.zipccl_format_version.argtypes = []
+        L.zipccl_status_string.restype = ctypes.c_char_p
+        L.zipccl_status_string.argtypes = [ctypes.c_int]
+        for name in ("zipccl_max_compressed_bytes", "zipccl_compress_workspace_bytes"):
+            f = getattr(L, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [u64p, u32, u64p]
+        L.zipccl_decompress_workspace_bytes.restype = ctypes.c_int
+        L.zipccl_decompress_workspace_bytes.argtypes = [u64, u32, u64p]
+        L.zipccl_reduce_workspace_bytes.restype = ctypes.c_int
+        L.zipccl_reduce_workspace_bytes.argtypes = [u32, u64p]
+        L.zipccl_compress.restype = ctypes.c_int
+        L.zipccl_compress.argtypes = [vp, u64, u64p, u32, ctypes.POINTER(ctypes.c_float), vp, u64, vp, vp, u64, vp]
+        L.zipccl_decompress.restype = ctypes.c_int
+        L.zipccl_decompress.argtypes = [vp, vp, u32, vp, u64, vp, u64, vp]
+        L.zipccl_decompress_reduce.restype = ctypes.c_int
+        L.zipccl_decompress_reduce.argtypes = [ctypes.POINTER(vp), u64p, u32, u64, vp, vp, u64, vp]
+        L.zipccl_get_device_status.restype = ctypes.c_int
+        L.zipccl_get_device_status.argtypes = [vp, vp]
+        L.zipccl_codebook_phase.restype = ctypes.c_int
+        L.zipccl_codebook_phase.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_uint8)]
+        _lib = L
+        return L
+
+
+def _u64_array(vals):
+    arr = (ctypes.c_uint64 * max(1, len(vals)))(*[int(v) for v in vals])
+    return arr
+
+
+def _check(st: int, what: str) -> None:
+    if st != OK:
+        raise ZipcclError(st, what)
+
+
+# ------------------------------------------------------------------ C ABI mirrors
+def zipccl_format_version() -> int:
+    return int(load().zipccl_format_version())
+
+
+def zipccl_status_string(status: int) -> str:
+    return load().zipccl_status_string(int(status)).decode()
+
+
+def zipccl_max_compressed_bytes(chunk_elems) -> int:
+    out = ctypes.c_uint64()
+    _check(load().zipccl_max_compressed_bytes(_u64_array(chunk_elems), len(chunk_elems), ctypes.byref(out)),
+           "zipccl_max_compressed_bytes")
+    return int(out.value)
+
+
+def zipccl_compress_workspace_bytes(chunk_elems) -> int:
+    out = ctypes.c_uint64()
+    _check(load().zipccl_compress_workspace_bytes(_u64_array(chunk_elems), len(chunk_elems), ctypes.byref(out)),
+           "zipccl_compress_workspace_bytes")
+    return int(out.value)
+
+
+def zipccl_decompress_workspace_bytes(n: int, n_chunks: int) -> int:
+    out = ctypes.c_uint64()
+    _check(load().zipccl_decompress_workspace_bytes(int(n), int(n_chunks), ctypes.byref(out)),
+           "zipccl_decompress_workspace_bytes")
+    return int(out.value)
+
+
+def zipccl_reduce_workspace_bytes(k: int) -> int:
+    out = ctypes.c_uint64()
+    _check(load().zipccl_reduce_workspace_bytes(int(k), ctypes.byref(out)), "zipccl_reduce_workspace_bytes")
+    return int(out.value)
+
+
+def zipccl_compress(d_in: int, n: int, chunk_elems, sigma_hint, d_out: int, out_capacity: int,
+                    d_chunk_offsets: int, d_ws: int, ws_bytes: int, stream: int) -> int:
+    hint = None
+    if sigma_hint is not None:
+        hint = (ctypes.c_float * len(sigma_hint))(*[float(v) for v in sigma_hint])
+    return int(load().zipccl_compress(d_in, n, _u64_array(chunk_elems), len(chunk_elems), hint, d_out,
+                                      out_capacity, d_chunk_offsets, d_ws, ws_bytes, stream))
+
+
+def zipccl_decompress(d_stream: int, d_chunk_offsets: int, n_chunks: int, d_out: int, n: int, d_ws: int,
+                      ws_bytes: int, stream: int) -> int:
+    return int(load().zipccl_decompress(d_stream, d_chunk_offsets, n_chunks, d_out, n, d_ws, ws_bytes, stream))
+
+
+def zipccl_decompress_reduce(d_peer_chunks, peer_chunk_bytes, k: int, n: int, d_out: int, d_ws: int,
+                             ws_bytes: int, stream: int) -> int:
+    ptrs = (ctypes.c_void_p * max(1, len(d_peer_chunks)))(*[int(p) for p in d_peer_chunks])
+    return int(load().zipccl_decompress_reduce(ptrs, _u64_array(peer_chunk_bytes), k, n, d_out, d_ws, ws_bytes,
+                                               stream))
+
+
+def zipccl_get_device_status(d_ws: int, stream: int) -> int:
+    return int(load().zipccl_get_device_status(d_ws, stream))
+
+
+def zipccl_codebook_phase(phase: int) -> tuple[int, list[int]]:
+    off = ctypes.c_int()
+    lens = (ctypes.c_uint8 * 16)()
+    _check(load().zipccl_codebook_phase(int(phase), ctypes.byref(off), lens), "zipccl_codebook_phase")
+    return off.value, list(lens)
+
+
+# ------------------------------------------------------------------ torch level
+class Compressed:
+    """A compressed buffer: chunks back to back in ``data`` (uint8, device) and
+    their byte offsets in ``offsets`` (int64 view of uint64, n_chunks + 1)."""
+
+    def __init__(self, data, offsets, n: int, chunk_elems):
+        self.data = data
+        self.offsets = offsets
+        self.n = int(n)
+        self.chunk_elems = [int(c) for c in chunk_elems]
+
+    @property
+    def n_chunks(self) -> int:
+        return len(self.chunk_elems)
+
+    def nbytes(self) -> int:
+        return int(self.offsets[-1].item())
+
+    def chunk(self, c: int):
+        o = self.offsets.cpu()
+        return self.data[int(o[c]): int(o[c + 1])]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _words(x):
+    torch = _torch()
+    if x.dtype == torch.bfloat16:
+        x = x.view(torch.int16)
+    if x.dtype not in (torch.int16, torch.uint16):
+        raise TypeError("expected a bfloat16 (or 16-bit word) tensor")
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("expected a contiguous CUDA tensor")
+    return x.reshape(-1)
+
+
+def _ws(nbytes: int, device, ws=None):
+    torch = _torch()
+    if ws is not None and ws.numel() >= nbytes:
+        return ws
+    return torch.empty(max(256, nbytes), dtype=torch.uint8, device=device)
+
+
+def compress(x, chunk_elems=None, sigma_hint=None, out=None, offsets=None, ws=None, stream=None) -> Compressed:
+    """Compress a BF16 CUDA tensor into per-chunk self-contained streams."""
+    torch = _torch()
+    w = _words(x)
+    n = w.numel()
+    chunk_elems = [n] if chunk_elems is None else [int(c) for c in chunk_elems]
+    cap = zipccl_max_compressed_bytes(chunk_elems)
+    if out is None or out.numel() < cap:
+        out = torch.empty(max(16, cap), dtype=torch.uint8, device=w.device)
+    if offsets is None:
+        offsets = torch.empty(len(chunk_elems) + 1, dtype=torch.int64, device=w.device)
+    wsb = zipccl_compress_workspace_bytes(chunk_elems)
+    ws = _ws(wsb, w.device, ws)
+    st = zipccl_compress(w.data_ptr(), n, chunk_elems, sigma_hint, out.data_ptr(), out.numel(),
+                         offsets.data_ptr(), ws.data_ptr(), ws.numel(), _stream_ptr(stream))
+    _check(st, "zipccl_compress")
+    return Compressed(out, offsets, n, chunk_elems)
+
+
+def decompress(c: Compressed, out=None, ws=None, stream=None):
+    """Decompress into a bfloat16 tensor of c.n elements (bit-identical)."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(max(1, c.n), dtype=torch.bfloat16, device=c.data.device)[: c.n]
+    wsb = zipccl_decompress_workspace_bytes(c.n, c.n_chunks)
+    ws = _ws(wsb, c.data.device, ws)
+    st = zipccl_decompress(c.data.data_ptr(), c.offsets.data_ptr(), c.n_chunks, out.data_ptr(), c.n,
+                           ws.data_ptr(), ws.numel(), _stream_ptr(stream))
+    _check(st, "zipccl_decompress")
+    return out
+
+
+def decompress_reduce(peer_chunks, n: int, out=None, ws=None, stream=None):
+    """Receive side of a reduce-scatter: decode k peer chunks (uint8 CUDA
+    tensors, rank order) and sum them in fp32 -> bfloat16[n]."""
+    torch = _torch()
+    k = len(peer_chunks)
+    dev = peer_chunks[0].device
+    if out is None:
+        out = torch.empty(max(1, n), dtype=torch.bfloat16, device=dev)[:n]
+    wsb = zipccl_reduce_workspace_bytes(k)
+    ws = _ws(wsb, dev, ws)
+    st = zipccl_decompress_reduce([p.data_ptr() for p in peer_chunks], [p.numel() for p in peer_chunks], k, n,
+                                  out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_ptr(stream))
+    _check(st, "zipccl_decompress_reduce")
+    return out

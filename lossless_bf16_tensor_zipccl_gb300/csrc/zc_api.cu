@@ -1,0 +1,281 @@
+// zc_api.cu -- the C ABI declared in include/zipccl.h: argument checks,
+// workspace layout and kernel launches.  Nothing here allocates device
+// memory or synchronizes (except zipccl_get_device_status).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <memory>
+
+#include "../../include/zipccl.h"
+#include "zc_codebook.h"
+#include "zc_device.cuh"
+#include "zc_format.h"
+#include "zc_kernels.h"
+
+namespace zc {
+namespace {
+
+constexpr uint64_t kMaxChunkElems = (1ull << 31) - 1;
+
+uint64_t pad256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct EncLayout {
+  uint64_t n_items;
+  uint64_t off_chunks, off_item_chunk, off_state, total;
+};
+
+EncLayout enc_layout(const uint64_t* ce, uint32_t nc) {
+  EncLayout L{};
+  for (uint32_t c = 0; c < nc; ++c) {
+    const uint64_t t = tiles_of(ce[c]);
+    L.n_items += t ? t : 1;
+  }
+  L.off_chunks = sizeof(WsHeader);
+  L.off_item_chunk = L.off_chunks + pad256(sizeof(EncChunk) * (uint64_t)nc);
+  L.off_state = L.off_item_chunk + pad256(4 * L.n_items);
+  L.total = L.off_state + pad256(8 * L.n_items);
+  return L;
+}
+
+struct DecLayout {
+  uint64_t off_chunks, off_item_start, off_luts, total;
+};
+
+DecLayout dec_layout(uint32_t nc) {
+  DecLayout L{};
+  L.off_chunks = sizeof(WsHeader);
+  L.off_item_start = L.off_chunks + pad256(sizeof(DecChunk) * (uint64_t)nc);
+  L.off_luts = L.off_item_start + pad256(4 * ((uint64_t)nc + 1));
+  L.total = L.off_luts + (uint64_t)nc * kLutEntries * sizeof(uint2);
+  return L;
+}
+
+uint64_t red_ws(uint32_t k) {
+  return sizeof(WsHeader) + pad256(sizeof(DecChunk) * (uint64_t)k) + (uint64_t)k * kLutEntries * sizeof(uint2);
+}
+
+zipccl_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ZIPCCL_OK : ZIPCCL_ERR_CUDA; }
+
+// Worst-case bytes of one chunk: header, table, every tile raw.
+bool chunk_bound(uint64_t n, uint64_t* out) {
+  if (n > kMaxChunkElems) return false;
+  const uint64_t T = tiles_of(n);
+  uint64_t b = chunk_hdr_bytes(T);
+  if (T) {
+    b += (T - 1) * (kTileHdr + 2ull * kTile);
+    b += kTileHdr + 2 * pad16(n - (T - 1) * kTile);
+  }
+  *out = b;
+  return true;
+}
+
+}  // namespace
+}  // namespace zc
+
+using namespace zc;
+
+extern "C" {
+
+int zipccl_format_version(void) { return (int)kVersion; }
+
+const char* zipccl_status_string(int s) {
+  switch (s) {
+    case ZIPCCL_OK: return "ok";
+    case ZIPCCL_ERR_INVALID_ARG: return "invalid argument";
+    case ZIPCCL_ERR_CAPACITY: return "buffer too small";
+    case ZIPCCL_ERR_CORRUPT: return "corrupt stream";
+    case ZIPCCL_ERR_VERSION: return "unsupported stream version";
+    case ZIPCCL_ERR_TIMEOUT: return "device wait timed out";
+    case ZIPCCL_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+zipccl_status zipccl_max_compressed_bytes(const uint64_t* chunk_elems, uint32_t n_chunks, uint64_t* out_bytes) {
+  if (!out_bytes || !chunk_elems || n_chunks == 0) return ZIPCCL_ERR_INVALID_ARG;
+  uint64_t total = 0;
+  for (uint32_t c = 0; c < n_chunks; ++c) {
+    uint64_t b;
+    if (!chunk_bound(chunk_elems[c], &b)) return ZIPCCL_ERR_INVALID_ARG;
+    total += b;
+  }
+  *out_bytes = total;
+  return ZIPCCL_OK;
+}
+
+zipccl_status zipccl_compress_workspace_bytes(const uint64_t* chunk_elems, uint32_t n_chunks, uint64_t* out_bytes) {
+  if (!out_bytes || !chunk_elems || n_chunks == 0) return ZIPCCL_ERR_INVALID_ARG;
+  for (uint32_t c = 0; c < n_chunks; ++c)
+    if (chunk_elems[c] > kMaxChunkElems) return ZIPCCL_ERR_INVALID_ARG;
+  *out_bytes = enc_layout(chunk_elems, n_chunks).total;
+  return ZIPCCL_OK;
+}
+
+zipccl_status zipccl_decompress_workspace_bytes(uint64_t n, uint32_t n_chunks, uint64_t* out_bytes) {
+  (void)n;
+  if (!out_bytes || n_chunks == 0) return ZIPCCL_ERR_INVALID_ARG;
+  *out_bytes = dec_layout(n_chunks).total;
+  return ZIPCCL_OK;
+}
+
+zipccl_status zipccl_reduce_workspace_bytes(uint32_t k, uint64_t* out_bytes) {
+  if (!out_bytes || k == 0 || k > kMaxPeers) return ZIPCCL_ERR_INVALID_ARG;
+  *out_bytes = red_ws(k);
+  return ZIPCCL_OK;
+}
+
+zipccl_status zipccl_compress(const uint16_t* d_in, uint64_t n, const uint64_t* chunk_elems, uint32_t n_chunks,
+                              const float* sigma_hint, void* d_out, uint64_t out_capacity,
+                              uint64_t* d_chunk_offsets, void* d_ws, uint64_t ws_bytes, void* stream) {
+  if (!chunk_elems || n_chunks == 0 || !d_out || !d_chunk_offsets || !d_ws) return ZIPCCL_ERR_INVALID_ARG;
+  if ((n > 0 && !d_in) || !aligned(d_in, 16) || !aligned(d_out, 16) || !aligned(d_chunk_offsets, 8) ||
+      !aligned(d_ws, 256))
+    return ZIPCCL_ERR_INVALID_ARG;
+  uint64_t sum = 0, bound = 0;
+  for (uint32_t c = 0; c < n_chunks; ++c) {
+    uint64_t b;
+    if (!chunk_bound(chunk_elems[c], &b)) return ZIPCCL_ERR_INVALID_ARG;
+    sum += chunk_elems[c];
+    bound += b;
+  }
+  if (sum != n) return ZIPCCL_ERR_INVALID_ARG;
+  const EncLayout L = enc_layout(chunk_elems, n_chunks);
+  if (L.n_items >= (1ull << 31)) return ZIPCCL_ERR_INVALID_ARG;
+  if (out_capacity < bound || ws_bytes < L.total) return ZIPCCL_ERR_CAPACITY;
+
+  const PhaseTable* tabs = phase_tables();
+  uint8_t* ws = static_cast<uint8_t*>(d_ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::unique_ptr<SelectArgs> sa(new SelectArgs);
+  memset(sa.get(), 0, sizeof(SelectArgs));
+  sa->in = d_in;
+  sa->chunks = reinterpret_cast<EncChunk*>(ws + L.off_chunks);
+  sa->item_chunk = reinterpret_cast<uint32_t*>(ws + L.off_item_chunk);
+  sa->item_state = reinterpret_cast<uint64_t*>(ws + L.off_state);
+  sa->hdr = reinterpret_cast<WsHeader*>(ws);
+  for (int r = 0; r < 16; ++r) {
+    sa->base_off[r] = tabs[r].base_offset;
+    sa->lens[r] = tabs[r].lens_packed;
+  }
+  uint64_t elem = 0, item = 0;
+  for (uint32_t c0 = 0; c0 < n_chunks; c0 += kSelectBatch) {
+    const uint32_t cnt = (n_chunks - c0) < kSelectBatch ? (n_chunks - c0) : kSelectBatch;
+    sa->chunk0 = c0;
+    sa->count = cnt;
+    for (uint32_t i = 0; i < cnt; ++i) {
+      const uint64_t nc = chunk_elems[c0 + i];
+      const uint64_t T = tiles_of(nc);
+      SelectChunkArg& a = sa->c[i];
+      a.elem_start = elem;
+      a.n = nc;
+      a.first_item = (uint32_t)item;
+      a.n_tiles = (uint32_t)T;
+      a.has_hint = 0;
+      a.q_hint = 0;
+      if (sigma_hint && sigma_hint[c0 + i] > 0.0f) {
+        double v = floor(16.0 * log2((double)sigma_hint[c0 + i]) + 0.5);
+        v = v < -32768.0 ? -32768.0 : (v > 32767.0 ? 32767.0 : v);
+        a.q_hint = (int32_t)v;
+        a.has_hint = 1;
+      }
+      elem += nc;
+      item += T ? T : 1;
+    }
+    const cudaError_t e = launch_select(*sa, s);
+    if (e != cudaSuccess) return ZIPCCL_ERR_CUDA;
+  }
+  EncodeArgs ea;
+  ea.in = d_in;
+  ea.out = static_cast<uint8_t*>(d_out);
+  ea.cap = out_capacity;
+  ea.offsets = d_chunk_offsets;
+  ea.chunks = sa->chunks;
+  ea.item_chunk = sa->item_chunk;
+  ea.item_state = sa->item_state;
+  ea.hdr = sa->hdr;
+  ea.n_chunks = n_chunks;
+  ea.n_items = (uint32_t)L.n_items;
+  return cuda_status(launch_encode(ea, (uint32_t)L.n_items, s));
+}
+
+zipccl_status zipccl_decompress(const void* d_stream, const uint64_t* d_chunk_offsets, uint32_t n_chunks,
+                                uint16_t* d_out, uint64_t n, void* d_ws, uint64_t ws_bytes, void* stream) {
+  if (!d_stream || !d_chunk_offsets || n_chunks == 0 || !d_ws || (n > 0 && !d_out)) return ZIPCCL_ERR_INVALID_ARG;
+  if (!aligned(d_stream, 16) || !aligned(d_chunk_offsets, 8) || !aligned(d_out, 16) || !aligned(d_ws, 256))
+    return ZIPCCL_ERR_INVALID_ARG;
+  const uint64_t max_items = tiles_of(n) + n_chunks;
+  if (max_items >= (1ull << 31)) return ZIPCCL_ERR_INVALID_ARG;
+  const DecLayout L = dec_layout(n_chunks);
+  if (ws_bytes < L.total) return ZIPCCL_ERR_CAPACITY;
+  uint8_t* ws = static_cast<uint8_t*>(d_ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(WsHeader), s);
+  if (e != cudaSuccess) return ZIPCCL_ERR_CUDA;
+  DprepArgs pa;
+  pa.stream = static_cast<const uint8_t*>(d_stream);
+  pa.offsets = d_chunk_offsets;
+  pa.chunks = reinterpret_cast<DecChunk*>(ws + L.off_chunks);
+  pa.item_start = reinterpret_cast<uint32_t*>(ws + L.off_item_start);
+  pa.luts = reinterpret_cast<uint2*>(ws + L.off_luts);
+  pa.hdr = reinterpret_cast<WsHeader*>(ws);
+  pa.n_chunks = n_chunks;
+  pa.max_items = (uint32_t)max_items;
+  pa.n = n;
+  DecodeArgs da;
+  da.stream = pa.stream;
+  da.chunks = pa.chunks;
+  da.item_start = pa.item_start;
+  da.luts = pa.luts;
+  da.out = d_out;
+  da.hdr = pa.hdr;
+  da.n_chunks = n_chunks;
+  return cuda_status(launch_decode(pa, da, (uint32_t)max_items, s));
+}
+
+zipccl_status zipccl_decompress_reduce(const void* const* d_peer_chunks, const uint64_t* peer_chunk_bytes, uint32_t k,
+                                       uint64_t n, uint16_t* d_out, void* d_ws, uint64_t ws_bytes, void* stream) {
+  if (!d_peer_chunks || !peer_chunk_bytes || k == 0 || k > kMaxPeers || !d_ws || (n > 0 && !d_out))
+    return ZIPCCL_ERR_INVALID_ARG;
+  if (!aligned(d_out, 16) || !aligned(d_ws, 256) || n > kMaxChunkElems) return ZIPCCL_ERR_INVALID_ARG;
+  ReduceArgs ra;
+  memset(&ra, 0, sizeof(ra));
+  for (uint32_t p = 0; p < k; ++p) {
+    if (!d_peer_chunks[p] || !aligned(d_peer_chunks[p], 16)) return ZIPCCL_ERR_INVALID_ARG;
+    ra.peers[p] = static_cast<const uint8_t*>(d_peer_chunks[p]);
+    ra.bytes[p] = peer_chunk_bytes[p];
+  }
+  if (ws_bytes < red_ws(k)) return ZIPCCL_ERR_CAPACITY;
+  uint8_t* ws = static_cast<uint8_t*>(d_ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(WsHeader), s);
+  if (e != cudaSuccess) return ZIPCCL_ERR_CUDA;
+  ra.hdr = reinterpret_cast<WsHeader*>(ws);
+  ra.chunks = reinterpret_cast<DecChunk*>(ws + sizeof(WsHeader));
+  ra.luts = reinterpret_cast<uint2*>(ws + sizeof(WsHeader) + pad256(sizeof(DecChunk) * (uint64_t)k));
+  ra.out = d_out;
+  ra.n = n;
+  ra.k = k;
+  return cuda_status(launch_reduce(ra, s));
+}
+
+zipccl_status zipccl_get_device_status(const void* d_ws, void* stream) {
+  if (!d_ws) return ZIPCCL_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ZIPCCL_ERR_CUDA;
+  uint32_t st = 0;
+  if (cudaMemcpy(&st, d_ws, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return ZIPCCL_ERR_CUDA;
+  return static_cast<zipccl_status>(st);
+}
+
+zipccl_status zipccl_codebook_phase(int phase, int* base_offset, uint8_t* lens16) {
+  if (phase < 0 || phase > 15 || !base_offset || !lens16) return ZIPCCL_ERR_INVALID_ARG;
+  const PhaseTable& t = phase_tables()[phase];
+  *base_offset = t.base_offset;
+  for (int s = 0; s < kNsym; ++s) lens16[s] = t.lens[s];
+  return ZIPCCL_OK;
+}
+
+}  // extern "C"

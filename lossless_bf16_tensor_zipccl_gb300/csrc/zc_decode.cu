@@ -1,0 +1,440 @@
+// zc_decode.cu -- decompressor and fused decompress + reduce kernels, sm_103a.
+//
+// "ZipCCL: Efficient Lossless Data Compression of Communication Collectives
+// for Accelerating LLM Training":
+//   - Fig. 6 caption: the GPU decompressor restores each value from its raw
+//     sign/mantissa byte and its decoded exponent;  pith summary: lossless,
+//     every byte restored;
+//   - Fig. 3 / Fig. 5 captions: zipcclReduceScatter receives the peers'
+//     compressed chunks, then decompresses and reduces them ->
+//     zc_reduce_kernel decodes the same tile of k peer chunks and sums in fp32
+//     in rank order, with no bf16 round trip through global memory.
+//
+// Decoding is table-driven: one 1024-entry table per chunk (built from the
+// code lengths in the chunk header) returns up to five symbols per lookup.
+// Each lane of a warp decodes one segment; the 32 segments of a tile are
+// interleaved 8 elements at a time, so a warp's loads of sign/mantissa bytes
+// and stores of BF16 words stay coalesced while each lane runs its own
+// bitstream.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zc_device.cuh"
+#include "zc_kernels.h"
+
+namespace zc {
+
+__device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ uint64_t ld_u64(const uint8_t* p) { return *reinterpret_cast<const uint64_t*>(p); }
+
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Header checks shared by both prep kernels; returns 0 or a status code.
+struct HeaderInfo {
+  uint64_t n;
+  uint32_t n_tiles;
+  uint32_t base;
+  uint64_t lens;
+};
+
+__device__ uint32_t check_header(const uint8_t* ch, uint64_t bytes, HeaderInfo& h) {
+  if (bytes < kChunkHdr) return kStCorrupt;
+  if (ld_u32(ch) != kMagic) return kStCorrupt;
+  const uint32_t w1 = ld_u32(ch + 4);
+  if ((w1 & 0xFFFFu) != kVersion || ((w1 >> 16) & 0xFFu) != kTileLog2 || (w1 >> 24) != kSegLog2) return kStVersion;
+  h.n = ld_u64(ch + 8);
+  h.n_tiles = ld_u32(ch + 16);
+  h.base = ch[20];
+  h.lens = ld_u64(ch + 24);
+  if (h.n >= (1ull << 40) || h.n_tiles != tiles_of(h.n)) return kStCorrupt;
+  if (chunk_hdr_bytes(h.n_tiles) > bytes || h.base > 240 || !lens_complete(h.lens)) return kStCorrupt;
+  return 0;
+}
+
+// Location of tile k of a chunk, validated against the chunk's extent.
+struct TileView {
+  const uint8_t* tile;
+  uint32_t mode, exp_off, exp_bytes;
+  uint32_t wstart, words;  // this lane's segment (coded tiles)
+};
+
+__device__ bool open_tile(const uint8_t* ch, uint64_t bytes, uint32_t n_tiles, uint32_t k, uint32_t nt,
+                          uint32_t lane, TileView& tv) {
+  const uint64_t toff = ld_u32(ch + kChunkHdr + 4ull * k);
+  if ((toff & 15) || toff < chunk_hdr_bytes(n_tiles) || toff + kTileHdr > bytes) return false;
+  const uint8_t* t = ch + toff;
+  const uint4 h = *reinterpret_cast<const uint4*>(t);
+  tv.tile = t;
+  tv.mode = h.x;
+  tv.exp_bytes = h.z;
+  tv.exp_off = kTileHdr + (uint32_t)pad16(nt);
+  if (h.y != nt || h.x > 1 || toff + tv.exp_off + pad16(h.z) > bytes) return false;
+  tv.wstart = tv.words = 0;
+  if (tv.mode == 1) return h.z == nt;
+  if (h.z < kSegTab || ((h.z - kSegTab) & 3)) return false;
+  const uint32_t w = reinterpret_cast<const uint16_t*>(t + tv.exp_off)[lane];
+  uint32_t incl = w;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= (uint32_t)o) incl += y;
+  }
+  tv.wstart = incl - w;
+  tv.words = w;
+  return __shfl_sync(kFull, incl, 31) == (h.z - kSegTab) / 4;
+}
+
+__device__ __forceinline__ uint2 load_bytes8(const uint8_t* p, uint32_t cnt) {
+  if (cnt == 8) return ld_stream_v2(p);
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    if (t < (int)cnt) {
+      const uint32_t b = p[t];
+      if (t < 4) lo |= b << (8 * t);
+      else hi |= b << (8 * (t - 4));
+    }
+  }
+  return make_uint2(lo, hi);
+}
+
+// Decode one 8-element lane group of row r into 4 words (8 BF16).
+struct RowSource {
+  TileView tv;
+  LaneDecoder dec;
+  uint32_t nt, lane;
+
+  __device__ __forceinline__ void start(const uint2* lut, uint32_t base) {
+    if (lane == 0) bulk_prefetch_l2(tv.tile, (uint32_t)(tv.exp_off + pad16(tv.exp_bytes)));
+    if (tv.mode == 0)
+      dec.init(reinterpret_cast<const uint32_t*>(tv.tile + tv.exp_off + kSegTab) + tv.wstart, tv.words, lut, base);
+  }
+
+  __device__ __forceinline__ uint32_t count(uint32_t r) const {
+    const uint32_t i0 = r * kRow + lane * kLaneElems;
+    return nt > i0 ? min(8u, nt - i0) : 0u;
+  }
+
+  __device__ __forceinline__ uint4 row(uint32_t r, uint2 sm) {
+    const uint32_t i0 = r * kRow + lane * kLaneElems;
+    const uint32_t cnt = count(r);
+    uint32_t lo = 0, hi = 0;
+    if (tv.mode == 0) {
+      dec.fill(cnt);
+      dec.take8(lo, hi);
+    } else {
+      const uint2 e = load_bytes8(tv.tile + tv.exp_off + i0, cnt);
+      lo = e.x;
+      hi = e.y;
+    }
+    const uint2 a = merge4(lo, sm.x), b = merge4(hi, sm.y);
+    return make_uint4(a.x, a.y, b.x, b.y);
+  }
+
+  __device__ __forceinline__ uint2 sm(uint32_t r) const {
+    return load_bytes8(tv.tile + kTileHdr + r * kRow + lane * kLaneElems, count(r));
+  }
+};
+
+__device__ __forceinline__ void store_row(uint16_t* y, uint32_t cnt, bool vec, uint4 v) {
+  if (cnt == 8 && vec) {
+    *reinterpret_cast<uint4*>(y) = v;
+  } else {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      if (t < (int)cnt) y[t] = (uint16_t)(w[t >> 1] >> (16 * (t & 1)));
+  }
+}
+
+// ---------------------------------------------------------------- decompress
+// Block c < n_chunks: validate chunk c's header, build its table.  Block
+// n_chunks: prefix sums of element counts and tile counts over all chunks.
+__global__ void __launch_bounds__(256) zc_dprep_kernel(DprepArgs a) {
+  const uint32_t tid = threadIdx.x;
+  if (blockIdx.x < a.n_chunks) {
+    const uint32_t c = blockIdx.x;
+    const uint64_t o0 = a.offsets[c], o1 = a.offsets[c + 1], total = a.offsets[a.n_chunks];
+    HeaderInfo h;
+    uint32_t st = (o1 < o0 || o1 > total || (o0 & 15)) ? kStCorrupt : check_header(a.stream + o0, o1 - o0, h);
+    if (st) {
+      if (tid == 0) {
+        set_status(a.hdr, st);
+        a.chunks[c].ok = 0;
+      }
+      return;
+    }
+    build_lut(h.lens, a.luts + (size_t)c * kLutEntries);
+    if (tid == 0) {
+      DecChunk& d = a.chunks[c];
+      d.stream_off = o0;
+      d.bytes = o1 - o0;
+      d.n = h.n;
+      d.n_tiles = h.n_tiles;
+      d.base = h.base;
+      d.ok = 1;
+    }
+    return;
+  }
+  // scan block
+  __shared__ unsigned long long s_n[8], s_t[8];
+  __shared__ int s_bad;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  const uint32_t lane = tid & 31, warp = tid >> 5;
+  uint64_t carry_n = 0, carry_t = 0;
+  for (uint32_t c0 = 0; c0 < a.n_chunks; c0 += 256) {
+    const uint32_t c = c0 + tid;
+    uint64_t nc = 0, tc = 0;
+    if (c < a.n_chunks) {
+      const uint64_t o0 = a.offsets[c], o1 = a.offsets[c + 1];
+      if (o1 >= o0 + kChunkHdr && o1 <= a.offsets[a.n_chunks] && !(o0 & 15) && ld_u32(a.stream + o0) == kMagic) {
+        nc = ld_u64(a.stream + o0 + 8);
+        if (nc > a.n) {
+          nc = 0;
+          s_bad = 1;
+        }
+        tc = tiles_of(nc);
+      } else {
+        s_bad = 1;
+      }
+    }
+    uint64_t in = nc, it = tc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t yn = __shfl_up_sync(kFull, in, o), yt = __shfl_up_sync(kFull, it, o);
+      if (lane >= (uint32_t)o) {
+        in += yn;
+        it += yt;
+      }
+    }
+    if (lane == 31) {
+      s_n[warp] = in;
+      s_t[warp] = it;
+    }
+    __syncthreads();
+    uint64_t wn = 0, wt = 0, bn = 0, bt = 0;
+    for (uint32_t w = 0; w < 8; ++w) {
+      if (w < warp) {
+        wn += s_n[w];
+        wt += s_t[w];
+      }
+      bn += s_n[w];
+      bt += s_t[w];
+    }
+    if (c < a.n_chunks) {
+      a.chunks[c].elem_start = carry_n + wn + in - nc;
+      a.item_start[c] = (uint32_t)(carry_t + wt + it - tc);
+    }
+    carry_n += bn;
+    carry_t += bt;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    a.item_start[a.n_chunks] = (uint32_t)min(carry_t, (uint64_t)a.max_items);
+    a.hdr->total_items = (uint32_t)min(carry_t, (uint64_t)a.max_items);
+    if (s_bad || carry_n != a.n || carry_t > a.max_items) set_status(a.hdr, kStCorrupt);
+  }
+}
+
+constexpr int kDecWarps = 4;
+
+// One warp per tile.
+__global__ void __launch_bounds__(kDecWarps * 32) zc_decode_kernel(DecodeArgs a) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t item = blockIdx.x * kDecWarps + (threadIdx.x >> 5);
+  // lane 0 reads the status once and the warp follows it together
+  uint32_t bad = lane == 0 ? *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) : 0u;
+  bad = __shfl_sync(kFull, bad, 0);
+  if (bad) return;
+  if (item >= a.hdr->total_items) return;
+  uint32_t lo = 0, hi = a.n_chunks;  // largest c with item_start[c] <= item
+  while (hi - lo > 1) {
+    const uint32_t mid = (lo + hi) >> 1;
+    if (a.item_start[mid] <= item) lo = mid;
+    else hi = mid;
+  }
+  const uint32_t c = lo;
+  const DecChunk d = a.chunks[c];
+  const uint32_t k = item - a.item_start[c];
+  if (!d.ok || k >= d.n_tiles) {
+    if (lane == 0) set_status(a.hdr, kStCorrupt);
+    return;
+  }
+  const uint32_t nt = (uint32_t)min((uint64_t)kTile, d.n - (uint64_t)k * kTile);
+  const uint8_t* ch = a.stream + d.stream_off;
+  RowSource src;
+  src.nt = nt;
+  src.lane = lane;
+  if (!open_tile(ch, d.bytes, d.n_tiles, k, nt, lane, src.tv)) {
+    if (lane == 0) set_status(a.hdr, kStCorrupt);
+    return;
+  }
+  src.start(a.luts + (size_t)c * kLutEntries, d.base);
+  const uint64_t e0 = d.elem_start + (uint64_t)k * kTile;
+  uint16_t* y = a.out + e0;
+  const bool vec = (e0 & 7) == 0;
+  const uint32_t rows = (nt + kRow - 1) / kRow;
+  // sign/mantissa bytes run 4 rows ahead of the decoder
+  uint2 q0 = src.sm(0), q1 = src.sm(1), q2 = src.sm(2), q3 = src.sm(3);
+  for (uint32_t r = 0; r < rows; r += 4) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t rr = r + j;
+      if (rr < rows) {
+        uint2 cur = j == 0 ? q0 : (j == 1 ? q1 : (j == 2 ? q2 : q3));
+        const uint2 nxt = src.sm(rr + 4);
+        if (j == 0) q0 = nxt;
+        else if (j == 1) q1 = nxt;
+        else if (j == 2) q2 = nxt;
+        else q3 = nxt;
+        const uint32_t cnt = src.count(rr);
+        const uint4 v = src.row(rr, cur);
+        if (cnt) store_row(y + rr * kRow + lane * kLaneElems, cnt, vec, v);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- reduce
+__global__ void __launch_bounds__(256) zc_rprep_kernel(ReduceArgs a) {
+  const uint32_t p = blockIdx.x;
+  HeaderInfo h;
+  uint32_t st = check_header(a.peers[p], a.bytes[p], h);
+  if (!st && h.n != a.n) st = kStCorrupt;
+  if (st) {
+    if (threadIdx.x == 0) {
+      set_status(a.hdr, st);
+      a.chunks[p].ok = 0;
+    }
+    return;
+  }
+  build_lut(h.lens, a.luts + (size_t)p * kLutEntries);
+  if (threadIdx.x == 0) {
+    DecChunk& d = a.chunks[p];
+    d.stream_off = 0;
+    d.bytes = a.bytes[p];
+    d.n = h.n;
+    d.n_tiles = h.n_tiles;
+    d.base = h.base;
+    d.elem_start = 0;
+    d.ok = 1;
+  }
+}
+
+__device__ __forceinline__ uint32_t f32_to_bf16_rne(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0u;
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return u >> 16;
+}
+
+__device__ __forceinline__ void add_bf16x2(float& a0, float& a1, uint32_t w) {
+  a0 = __fadd_rn(a0, __uint_as_float(w << 16));
+  a1 = __fadd_rn(a1, __uint_as_float(w & 0xFFFF0000u));
+}
+
+// One block per tile, one warp per peer.  Rows are decoded 16 at a time into
+// shared memory (peer-major), then every thread folds 8 elements across the
+// peers in rank order.
+constexpr uint32_t kRedRows = 16;
+
+__global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
+  extern __shared__ __align__(16) uint16_t sbuf[];  // k x kRedRows x kRow
+  const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5, tid = threadIdx.x;
+  const uint32_t t = blockIdx.x;
+  const uint32_t nthreads = 32 * a.k;
+  __shared__ int s_bad;
+  // one read of the status word per block, so every thread takes the same path
+  if (tid == 0) s_bad = *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0;
+  __syncthreads();
+  if (s_bad) return;
+  const uint32_t nt = (uint32_t)min((uint64_t)kTile, a.n - (uint64_t)t * kTile);
+  const DecChunk d = a.chunks[p];
+  RowSource src;
+  src.nt = nt;
+  src.lane = lane;
+  bool ok = d.ok && open_tile(a.peers[p], d.bytes, d.n_tiles, t, nt, lane, src.tv);
+  if (!ok && lane == 0) {
+    s_bad = 1;
+    set_status(a.hdr, kStCorrupt);
+  }
+  __syncthreads();
+  if (s_bad) return;  // uniform
+  src.start(a.luts + (size_t)p * kLutEntries, d.base);
+  uint16_t* mine = sbuf + (size_t)p * kRedRows * kRow;
+  const uint32_t rows = (nt + kRow - 1) / kRow;
+  uint16_t* y = a.out + (uint64_t)t * kTile;
+  for (uint32_t r0 = 0; r0 < rows; r0 += kRedRows) {
+    const uint32_t rend = min(rows, r0 + kRedRows);
+    uint2 q = src.sm(r0);
+    for (uint32_t r = r0; r < rend; ++r) {
+      const uint2 cur = q;
+      q = src.sm(r + 1 < rend ? r + 1 : rend);
+      const uint4 v = src.row(r, cur);
+      *reinterpret_cast<uint4*>(mine + (r - r0) * kRow + lane * kLaneElems) = v;
+    }
+    __syncthreads();
+    const uint32_t m = min(kRedRows * kRow, nt - r0 * kRow);
+    for (uint32_t e = tid * 8; e < m; e += nthreads * 8) {
+      float acc[8];
+      {
+        const uint4 v = *reinterpret_cast<const uint4*>(sbuf + e);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = __uint_as_float(w[i] << 16);
+          acc[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+      }
+      for (uint32_t pp = 1; pp < a.k; ++pp) {
+        const uint4 v = *reinterpret_cast<const uint4*>(sbuf + (size_t)pp * kRedRows * kRow + e);
+        add_bf16x2(acc[0], acc[1], v.x);
+        add_bf16x2(acc[2], acc[3], v.y);
+        add_bf16x2(acc[4], acc[5], v.z);
+        add_bf16x2(acc[6], acc[7], v.w);
+      }
+      uint4 o;
+      o.x = f32_to_bf16_rne(acc[0]) | (f32_to_bf16_rne(acc[1]) << 16);
+      o.y = f32_to_bf16_rne(acc[2]) | (f32_to_bf16_rne(acc[3]) << 16);
+      o.z = f32_to_bf16_rne(acc[4]) | (f32_to_bf16_rne(acc[5]) << 16);
+      o.w = f32_to_bf16_rne(acc[6]) | (f32_to_bf16_rne(acc[7]) << 16);
+      store_row(y + r0 * kRow + e, min(8u, m - e), true, o);
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- launchers
+static int g_red_attr_done[64];
+
+cudaError_t launch_decode(const DprepArgs& prep, const DecodeArgs& args, uint32_t max_items, cudaStream_t s) {
+  zc_dprep_kernel<<<prep.n_chunks + 1, 256, 0, s>>>(prep);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || max_items == 0) return e;
+  zc_decode_kernel<<<(max_items + kDecWarps - 1) / kDecWarps, kDecWarps * 32, 0, s>>>(args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(const ReduceArgs& args, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int smem_max = (int)(kMaxPeers * kRedRows * kRow * sizeof(uint16_t));
+  if (dev >= 0 && dev < 64 && !g_red_attr_done[dev]) {
+    e = cudaFuncSetAttribute(zc_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    if (e != cudaSuccess) return e;
+    g_red_attr_done[dev] = 1;
+  }
+  zc_rprep_kernel<<<args.k, 256, 0, s>>>(args);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || args.n == 0) return e;
+  const uint32_t tiles = (uint32_t)tiles_of(args.n);
+  const size_t smem = (size_t)args.k * kRedRows * kRow * sizeof(uint16_t);
+  zc_reduce_kernel<<<tiles, 32 * args.k, smem, s>>>(args);
+  return cudaGetLastError();
+}
+
+}  // namespace zc

@@ -1,0 +1,421 @@
+// zc_encode.cu -- compressor kernels for sm_103a.
+//
+// "ZipCCL: Efficient Lossless Data Compression of Communication Collectives
+// for Accelerating LLM Training":
+//   - abstract, technique (1): exponent coding from the Gaussian law with no
+//     online statistics -> zc_select_kernel takes the scale from a fixed
+//     sample (one integer sum), never a histogram of the tensor;
+//   - abstract, technique (2) and Fig. 5 / Fig. 6 captions: GPU compressor
+//     with designed memory access, overlap of compression with memory
+//     traffic, few launches, communication-aware layout -> one fused kernel
+//     per tile computes lengths, packs bits in shared memory, finds its
+//     output offset by decoupled look-back over the flat tile list of all
+//     per-destination chunks, and writes the tile image with one TMA bulk
+//     store;
+//   - Fig. 7 caption (shared-memory data layout): the tile image is staged in
+//     shared memory as header | sign/mantissa plane | exponent region.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zc_device.cuh"
+#include "zc_kernels.h"
+
+namespace zc {
+
+// ---------------------------------------------------------------- scale select
+__device__ __forceinline__ int64_t floor_div_pos(int64_t a, int64_t b) {  // b > 0
+  return a >= 0 ? a / b : -((-a + b - 1) / b);
+}
+
+// One block per chunk.  The code is built for sigma = 2^(q/16).  With a hint
+// q is given; otherwise the mean biased exponent of a fixed sample (all
+// elements when n <= 4096, else 64 blocks of 64 consecutive elements at
+// floor(b n / 64)), skipping e = 0 and e = 255, gives
+//   q = round-half-up(16 (mean - 127 + 1.4164)),
+// 1.4164 being 1/2 + (gamma + ln 2)/(2 ln 2): the mean of floor(log2 |Z|)
+// below log2(sigma) for a centred Gaussian.
+__global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ SelectArgs a) {
+  const SelectChunkArg ca = a.c[blockIdx.x];
+  const uint32_t ci = a.chunk0 + blockIdx.x;
+  __shared__ long long s_sum[8], s_cnt[8];
+  __shared__ int s_q;
+  if (ci == 0 && threadIdx.x == 0) {
+    a.hdr->status = 0;
+    a.hdr->counter = 0;
+  }
+  if (ca.has_hint) {
+    if (threadIdx.x == 0) s_q = ca.q_hint;
+  } else {
+    const uint16_t* x = a.in + ca.elem_start;
+    long long S = 0, K = 0;
+    if (ca.n <= 4096) {
+      for (uint64_t i = threadIdx.x; i < ca.n; i += blockDim.x) {
+        const uint32_t e = (x[i] >> 7) & 0xFFu;
+        if (e != 0 && e != 255) { S += e; ++K; }
+      }
+    } else {
+      for (uint32_t s = threadIdx.x; s < 4096; s += blockDim.x) {
+        const uint64_t b = s >> 6, off = s & 63;
+        const uint32_t e = (x[(b * ca.n) / 64 + off] >> 7) & 0xFFu;
+        if (e != 0 && e != 255) { S += e; ++K; }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      S += __shfl_xor_sync(kFull, S, o);
+      K += __shfl_xor_sync(kFull, K, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+      s_sum[threadIdx.x >> 5] = S;
+      s_cnt[threadIdx.x >> 5] = K;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      long long ts = 0, tk = 0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) { ts += s_sum[w]; tk += s_cnt[w]; }
+      s_q = tk ? (int)floor_div_pos(40000ll * (ts - 127ll * tk) + 57906ll * tk, 2500ll * tk) : 0;
+    }
+  }
+  __syncthreads();
+  const int q = s_q;
+  const int kq = (int)floor_div_pos(q, 16);
+  const int r = q - 16 * kq;
+  int base = kq + 127 + a.base_off[r];
+  base = base < 0 ? 0 : (base > 240 ? 240 : base);
+  if (threadIdx.x == 0) {
+    EncChunk ec;
+    ec.elem_start = ca.elem_start;
+    ec.n = ca.n;
+    ec.first_item = ca.first_item;
+    ec.n_tiles = ca.n_tiles;
+    ec.q = q;
+    ec.base = (uint32_t)base;
+    ec.lens = a.lens[r];
+    ec.start_slot = 0;
+    ec.pad[0] = ec.pad[1] = 0;
+    a.chunks[ci] = ec;
+  }
+  const uint32_t items = ca.n_tiles ? ca.n_tiles : 1u;
+  for (uint32_t i = threadIdx.x; i < items; i += blockDim.x) {
+    a.item_chunk[ca.first_item + i] = ci;
+    a.item_state[ca.first_item + i] = 0;
+  }
+}
+
+// ---------------------------------------------------------------- encode
+// Shared memory: tile image (header | sign/mantissa plane | exponent region)
+// | staged exponent bytes | encode table (256 x u32) | partial bit counts.
+constexpr uint32_t kImgBytes = kTileHdr + kTile + kTile;
+constexpr uint32_t kEncSmem = kImgBytes + kTile + 256 * 4 + 256 * 4;
+constexpr int kEncThreads = 256;  // 8 warps; warp w owns rows 16w..16w+15
+
+// Decoupled look-back over the flat tile list (warp-wide).  Each tile
+// publishes its byte count (aggregate), then its inclusive prefix.  Returns
+// the exclusive prefix; sets err on a timed-out wait or an upstream error.
+__device__ uint64_t lookback(uint64_t* state, uint32_t item, uint32_t lane, bool& err) {
+  uint64_t excl = 0;
+  int64_t pred = (int64_t)item - 1;
+  uint64_t t0 = 0;
+  bool waiting = false;
+  while (true) {
+    const int64_t idx = pred - (int64_t)lane;
+    const uint64_t s = idx >= 0 ? ld_acquire_u64(state + idx) : kFlagInc;
+    const uint32_t flag = (uint32_t)(s >> kFlagShift);
+    const uint32_t not_ready = __ballot_sync(kFull, flag == 0);
+    const uint32_t stop = __ballot_sync(kFull, flag >= 2);
+    const uint32_t lim = stop ? (uint32_t)(__ffs(stop) - 1) : 31u;
+    const uint32_t upto = lim == 31 ? kFull : ((2u << lim) - 1u);
+    if (not_ready & upto) {
+      // lane 0's clock decides for the whole warp, so all lanes leave together
+      const uint64_t now = globaltimer_ns();
+      if (!waiting) {
+        waiting = true;
+        t0 = now;
+      }
+      if (__shfl_sync(kFull, (now - t0 > kWaitLimitNs) ? 1u : 0u, 0)) {
+        err = true;
+        return 0;
+      }
+      __nanosleep(64);
+      continue;
+    }
+    if (__ballot_sync(kFull, flag == 3) & upto) {
+      err = true;
+      return 0;
+    }
+    uint64_t v = lane <= lim ? (s & kValMask) : 0;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    excl += v;
+    if (stop) return excl;
+    pred -= 32;
+  }
+}
+
+__global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* img = smem;
+  uint8_t* exps = smem + kImgBytes;  // exponent bytes in element order
+  uint32_t* tab = reinterpret_cast<uint32_t*>(smem + kImgBytes + kTile);
+  uint32_t* part = tab + 256;
+  __shared__ uint32_t s_item, s_mode, s_err, s_size;
+  __shared__ uint32_t s_wstart[32];
+  __shared__ unsigned long long s_goff;
+
+  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    s_item = atomicAdd(&a.hdr->counter, 1u);  // tiles start in claim order
+    s_err = 0;
+  }
+  __syncthreads();
+  const uint32_t item = s_item;
+  const uint32_t c = a.item_chunk[item];
+  const EncChunk ci = a.chunks[c];
+  const uint32_t k = item - ci.first_item;
+  const uint32_t nt = ci.n_tiles ? (uint32_t)min((uint64_t)kTile, ci.n - (uint64_t)k * kTile) : 0u;
+  const uint64_t elem0 = ci.elem_start + (uint64_t)k * kTile;
+  const uint16_t* x = a.in + elem0;
+  const bool vec = (elem0 & 7) == 0;
+  const uint32_t base = ci.base;
+  const uint32_t sm_pad = (uint32_t)pad16(nt);
+  const uint32_t exp_off = kTileHdr + sm_pad;
+
+  // Encode table: entry for exponent value tid = reversed codeword | length << 24;
+  // an escape entry carries the 8 raw exponent bits after the codeword.
+  {
+    const int xs = (int)tid - (int)base;
+    const int sym = (xs >= 0 && xs < kWindow) ? xs : kEsc;
+    const int L = (int)((ci.lens >> (4 * sym)) & 15);
+    const uint32_t rev = bit_reverse(canonical_code(ci.lens, sym), L);
+    tab[tid] = sym == kEsc ? ((rev | (tid << L)) | ((uint32_t)(L + 8) << 24)) : (rev | ((uint32_t)L << 24));
+  }
+  // Zero the padding of the sign/mantissa plane and the whole exponent area
+  // (coded words are OR-ed in).
+  if (tid < 16 && nt + tid < sm_pad) {
+    img[kTileHdr + nt + tid] = 0;
+    exps[nt + tid] = 0;
+  }
+  for (uint32_t o = tid * 16; o < sm_pad; o += kEncThreads * 16)
+    *reinterpret_cast<uint4*>(img + exp_off + o) = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+
+  // Phase A: 16-B loads, split into sign/mantissa bytes (image) and exponent
+  // bytes (staging); sum the code lengths.
+  uint32_t bits = 0;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const uint32_t i0 = (warp * 16 + r) * kRow + lane * kLaneElems;
+    const uint32_t cnt = nt > i0 ? min(8u, nt - i0) : 0u;
+    uint32_t w[4];
+    if (cnt == 8 && vec) {
+      const uint4 v = ld_stream_v4(x + i0);
+      w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else {
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const uint32_t lo = (2 * p < (int)cnt) ? x[i0 + 2 * p] : 0u;
+        const uint32_t hi = (2 * p + 1 < (int)cnt) ? x[i0 + 2 * p + 1] : 0u;
+        w[p] = lo | (hi << 16);
+      }
+    }
+    uint32_t e2[4], s2[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      e2[p] = (w[p] >> 7) & 0x00FF00FFu;
+      s2[p] = ((w[p] >> 8) & 0x00800080u) | (w[p] & 0x007F007Fu);
+    }
+    const uint32_t ex0 = __byte_perm(e2[0], e2[1], 0x6420), ex1 = __byte_perm(e2[2], e2[3], 0x6420);
+    const uint32_t sm0 = __byte_perm(s2[0], s2[1], 0x6420), sm1 = __byte_perm(s2[2], s2[3], 0x6420);
+    if (cnt == 8) {
+      *reinterpret_cast<uint2*>(img + kTileHdr + i0) = make_uint2(sm0, sm1);
+      *reinterpret_cast<uint2*>(exps + i0) = make_uint2(ex0, ex1);
+    } else {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        if (t < (int)cnt) {
+          img[kTileHdr + i0 + t] = (uint8_t)((t < 4 ? sm0 : sm1) >> (8 * (t & 3)));
+          exps[i0 + t] = (uint8_t)((t < 4 ? ex0 : ex1) >> (8 * (t & 3)));
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      if (t < (int)cnt) bits += tab[((t < 4 ? ex0 : ex1) >> (8 * (t & 3))) & 0xFFu] >> 24;
+  }
+  part[warp * 32 + lane] = bits;
+  __syncthreads();
+
+  // Phase B (warp 0): bit offset of each warp's part inside each segment,
+  // word-aligned segment starts, raw/coded choice, publish the aggregate.
+  uint64_t agg = 0;
+  if (warp == 0) {
+    uint32_t off = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const uint32_t v = part[w * 32 + lane];
+      part[w * 32 + lane] = off;
+      off += v;
+    }
+    const uint32_t words = (off + 31) >> 5;
+    uint32_t incl = words;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= (uint32_t)o) incl += y;
+    }
+    const uint32_t W = __shfl_sync(kFull, incl, 31);
+    s_wstart[lane] = incl - words;
+    const bool coded = kSegTab + 4ull * W < nt;
+    const uint32_t exp_bytes = coded ? kSegTab + 4 * W : nt;
+    if (coded) *reinterpret_cast<uint16_t*>(img + exp_off + 2 * lane) = (uint16_t)words;
+    const uint32_t size = nt ? (uint32_t)(kTileHdr + sm_pad + pad16(exp_bytes)) : 0u;
+    agg = size + (k == 0 ? chunk_hdr_bytes(ci.n_tiles) : 0);
+    if (lane == 0) {
+      s_mode = coded ? 0u : 1u;
+      s_size = size;
+      *reinterpret_cast<uint4*>(img) = make_uint4(coded ? 0u : 1u, nt, exp_bytes, 0u);
+      st_release_u64(a.item_state + item, (item == 0 ? kFlagInc : kFlagAgg) | agg);
+    }
+  }
+  __syncthreads();
+
+  // Phase C (warp 0 first): look-back for this tile's byte offset, chunk
+  // header / tile table / chunk offsets.
+  if (warp == 0) {
+    bool err = false;
+    uint64_t excl = item == 0 ? 0 : lookback(a.item_state, item, lane, err);
+    if (item != 0 && lane == 0) st_release_u64(a.item_state + item, err ? kFlagErr : (kFlagInc | (excl + agg)));
+    uint64_t cs = 0;
+    if (!err) {
+      if (k == 0) {
+        cs = excl;
+        if (lane == 0) {
+          st_release_u64(&a.chunks[c].start_slot, kSlotValid | cs);
+          a.offsets[c] = cs;
+        }
+      } else {
+        // lane 0 waits for the chunk's first tile to publish the chunk start
+        uint64_t v = 0;
+        uint32_t to = 0;
+        if (lane == 0) {
+          const uint64_t t0 = globaltimer_ns();
+          v = ld_acquire_u64(&a.chunks[c].start_slot);
+          while (!(v & kSlotValid)) {
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+              to = 1;
+              break;
+            }
+            __nanosleep(64);
+            v = ld_acquire_u64(&a.chunks[c].start_slot);
+          }
+        }
+        v = __shfl_sync(kFull, v, 0);
+        err = __shfl_sync(kFull, to, 0) != 0;
+        cs = v & ~kSlotValid;
+      }
+    }
+    const uint64_t hdr = chunk_hdr_bytes(ci.n_tiles);
+    const uint64_t goff = excl + (k == 0 ? hdr : 0);
+    if (!err && (goff + s_size > a.cap || cs + hdr > a.cap)) {
+      err = true;
+      if (lane == 0) set_status(a.hdr, kStCapacity);
+    } else if (err && lane == 0) {
+      set_status(a.hdr, kStTimeout);
+    }
+    if (!err) {
+      uint8_t* cp = a.out + cs;
+      if (k == 0) {
+        if (lane < 8) {
+          uint32_t v;
+          switch (lane) {
+            case 0: v = kMagic; break;
+            case 1: v = kVersion | (kTileLog2 << 16) | (kSegLog2 << 24); break;
+            case 2: v = (uint32_t)ci.n; break;
+            case 3: v = (uint32_t)(ci.n >> 32); break;
+            case 4: v = ci.n_tiles; break;
+            case 5: v = base | ((uint32_t)(uint16_t)(int16_t)ci.q << 16); break;
+            case 6: v = (uint32_t)ci.lens; break;
+            default: v = (uint32_t)(ci.lens >> 32); break;
+          }
+          reinterpret_cast<uint32_t*>(cp)[lane] = v;
+        }
+        // zero the tail of the tile table up to 16 bytes
+        const uint32_t tail0 = 4 * ci.n_tiles, tail1 = (uint32_t)pad16(4ull * ci.n_tiles);
+        if (tail0 + 4 * lane < tail1) reinterpret_cast<uint32_t*>(cp + kChunkHdr + tail0)[lane] = 0;
+      }
+      if (nt && lane == 0) reinterpret_cast<uint32_t*>(cp + kChunkHdr)[k] = (uint32_t)(goff - cs);
+      if (item == a.n_items - 1 && lane == 0) a.offsets[a.n_chunks] = excl + agg;
+    }
+    if (lane == 0) {
+      s_goff = goff;
+      s_err = err ? 1u : 0u;
+    }
+  }
+
+  // Phase D: pack codewords into the exponent region (coded tiles); raw
+  // tiles are stored straight from the staging area.
+  if (s_mode == 0) {
+    uint32_t* sw = reinterpret_cast<uint32_t*>(img + exp_off + kSegTab) + s_wstart[lane];
+    const uint32_t start = part[warp * 32 + lane];
+    uint32_t widx = start >> 5, nacc = start & 31;
+    uint64_t acc = 0;
+#pragma unroll 1
+    for (int r = 0; r < 16; ++r) {
+      const uint32_t i0 = (warp * 16 + r) * kRow + lane * kLaneElems;
+      const uint32_t cnt = nt > i0 ? min(8u, nt - i0) : 0u;
+      if (cnt == 0) break;
+      const uint2 e8 = *reinterpret_cast<const uint2*>(exps + i0);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        if (t < (int)cnt) {
+          const uint32_t en = tab[((t < 4 ? e8.x : e8.y) >> (8 * (t & 3))) & 0xFFu];
+          acc |= (uint64_t)(en & 0xFFFFFFu) << nacc;
+          nacc += en >> 24;
+          if (nacc >= 32) {
+            atomicOr(sw + widx, (uint32_t)acc);
+            ++widx;
+            acc >>= 32;
+            nacc -= 32;
+          }
+        }
+      }
+    }
+    if (nacc) atomicOr(sw + widx, (uint32_t)acc);
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  // Phase E: TMA bulk store of the finished tile: one copy for a coded tile,
+  // image head + staged exponents for a raw tile.
+  if (tid == 0 && !s_err && s_size) {
+    if (s_mode == 0) {
+      bulk_store_and_wait(a.out + s_goff, img, s_size);
+    } else {
+      bulk_store2_and_wait(a.out + s_goff, img, exp_off, a.out + s_goff + exp_off, exps, sm_pad);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_select(const SelectArgs& args, cudaStream_t s) {
+  if (args.count == 0) return cudaSuccess;
+  zc_select_kernel<<<args.count, 256, 0, s>>>(args);
+  return cudaGetLastError();
+}
+
+static int g_enc_attr_done[64];
+
+cudaError_t launch_encode(const EncodeArgs& args, uint32_t n_items, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && !g_enc_attr_done[dev]) {
+    e = cudaFuncSetAttribute(zc_encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEncSmem);
+    if (e != cudaSuccess) return e;
+    g_enc_attr_done[dev] = 1;
+  }
+  zc_encode_kernel<<<n_items, kEncThreads, kEncSmem, s>>>(args);
+  return cudaGetLastError();
+}
+
+}  // namespace zc

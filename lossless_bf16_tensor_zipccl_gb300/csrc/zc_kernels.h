@@ -1,0 +1,87 @@
+// zc_kernels.h -- launch records and launchers of the sm_103a kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zc_format.h"
+
+namespace zc {
+
+// Scale selection: chunk records travel as kernel parameters, kSelectBatch
+// chunks per launch.
+constexpr uint32_t kSelectBatch = 256;
+
+struct SelectChunkArg {
+  uint64_t elem_start;
+  uint64_t n;
+  uint32_t first_item;
+  uint32_t n_tiles;
+  int32_t q_hint;
+  int32_t has_hint;
+};
+
+struct SelectArgs {
+  const uint16_t* in;
+  EncChunk* chunks;
+  uint32_t* item_chunk;
+  uint64_t* item_state;
+  WsHeader* hdr;
+  uint32_t chunk0;
+  uint32_t count;
+  int32_t base_off[16];
+  uint64_t lens[16];
+  SelectChunkArg c[kSelectBatch];
+};
+
+struct EncodeArgs {
+  const uint16_t* in;
+  uint8_t* out;
+  uint64_t cap;
+  uint64_t* offsets;
+  EncChunk* chunks;
+  const uint32_t* item_chunk;
+  uint64_t* item_state;
+  WsHeader* hdr;
+  uint32_t n_chunks;
+  uint32_t n_items;
+};
+
+struct DprepArgs {
+  const uint8_t* stream;
+  const uint64_t* offsets;
+  DecChunk* chunks;
+  uint32_t* item_start;  // n_chunks + 1
+  uint2* luts;           // n_chunks x 1024
+  WsHeader* hdr;
+  uint32_t n_chunks;
+  uint32_t max_items;
+  uint64_t n;
+};
+
+struct DecodeArgs {
+  const uint8_t* stream;
+  const DecChunk* chunks;
+  const uint32_t* item_start;
+  const uint2* luts;
+  uint16_t* out;
+  WsHeader* hdr;
+  uint32_t n_chunks;
+};
+
+struct ReduceArgs {
+  const uint8_t* peers[kMaxPeers];
+  uint64_t bytes[kMaxPeers];
+  DecChunk* chunks;  // one per peer
+  uint2* luts;       // k x 1024
+  WsHeader* hdr;
+  uint16_t* out;
+  uint64_t n;
+  uint32_t k;
+};
+
+cudaError_t launch_select(const SelectArgs& args, cudaStream_t s);
+cudaError_t launch_encode(const EncodeArgs& args, uint32_t n_items, cudaStream_t s);
+cudaError_t launch_decode(const DprepArgs& prep, const DecodeArgs& args, uint32_t max_items, cudaStream_t s);
+cudaError_t launch_reduce(const ReduceArgs& args, cudaStream_t s);
+
+}  // namespace zc

@@ -1,0 +1,111 @@
+"""The C ABI without a GPU: the library builds and loads, exports every symbol
+include/zipccl.h declares, and its host-only calls behave -- argument and
+capacity errors come back before any CUDA call, the worst-case bound and the
+code tables agree with the oracle's."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import lossless_bf16_tensor_zipccl_gb300 as zc
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "zipccl.h")).read()
+    return sorted(set(re.findall(r"\b(zipccl_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = zc.load()
+    names = declared_symbols()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(zc.EXPORTED_SYMBOLS) == names
+
+
+def test_format_version_and_status_strings():
+    assert zc.zipccl_format_version() == 1 == oracle.format_version()
+    for s in range(7):
+        assert zc.zipccl_status_string(s)
+    assert zc.zipccl_status_string(99) == "unknown status"
+
+
+def test_codebook_tables_match_oracle():
+    offs, lens = oracle.phase_tables()
+    for r in range(16):
+        o, l = zc.zipccl_codebook_phase(r)
+        assert o == offs[r] and l == lens[r], r
+    with pytest.raises(zc.ZipcclError):
+        zc.zipccl_codebook_phase(16)
+
+
+@pytest.mark.parametrize("chunks", [[1], [0], [0, 5, 0], [32768], [32769, 1, 65536], [1 << 20] * 3,
+                                    [12345678, 7]])
+def test_max_bytes_matches_oracle(chunks):
+    assert zc.zipccl_max_compressed_bytes(chunks) == oracle.max_compressed_bytes(chunks)
+
+
+def test_workspace_sizes():
+    assert zc.zipccl_compress_workspace_bytes([10, 0, 70000]) > 256
+    assert zc.zipccl_decompress_workspace_bytes(70010, 3) >= 256 + 3 * 8192
+    assert zc.zipccl_reduce_workspace_bytes(8) >= 256 + 8 * 8192
+    with pytest.raises(zc.ZipcclError):
+        zc.zipccl_reduce_workspace_bytes(17)
+    with pytest.raises(zc.ZipcclError):
+        zc.zipccl_compress_workspace_bytes([1 << 31])
+
+
+FAKE = 1 << 20  # aligned non-null "device" addresses: never dereferenced, every call below fails validation first
+
+
+def test_compress_argument_errors_return_before_launch():
+    ok_ws = zc.zipccl_compress_workspace_bytes([100])
+    cap = zc.zipccl_max_compressed_bytes([100])
+    # sum of chunks != n
+    assert zc.zipccl_compress(FAKE, 101, [100], None, FAKE, cap, FAKE, FAKE, ok_ws, 0) == zc.ERR_INVALID_ARG
+    # misaligned input / output / workspace
+    assert zc.zipccl_compress(FAKE + 2, 100, [100], None, FAKE, cap, FAKE, FAKE, ok_ws, 0) == zc.ERR_INVALID_ARG
+    assert zc.zipccl_compress(FAKE, 100, [100], None, FAKE + 8, cap, FAKE, FAKE, ok_ws, 0) == zc.ERR_INVALID_ARG
+    assert zc.zipccl_compress(FAKE, 100, [100], None, FAKE, cap, FAKE, FAKE + 16, ok_ws, 0) == zc.ERR_INVALID_ARG
+    # null pointers, no chunks
+    assert zc.zipccl_compress(0, 100, [100], None, FAKE, cap, FAKE, FAKE, ok_ws, 0) == zc.ERR_INVALID_ARG
+    assert zc.zipccl_compress(FAKE, 0, [], None, FAKE, cap, FAKE, FAKE, ok_ws, 0) == zc.ERR_INVALID_ARG
+    # capacity and workspace too small
+    assert zc.zipccl_compress(FAKE, 100, [100], None, FAKE, cap - 1, FAKE, FAKE, ok_ws, 0) == zc.ERR_CAPACITY
+    assert zc.zipccl_compress(FAKE, 100, [100], None, FAKE, cap, FAKE, FAKE, ok_ws - 1, 0) == zc.ERR_CAPACITY
+    # chunk too large
+    assert zc.zipccl_compress(FAKE, 1 << 31, [1 << 31], None, FAKE, 1 << 40, FAKE, FAKE, 1 << 40, 0) == \
+        zc.ERR_INVALID_ARG
+
+
+def test_decompress_and_reduce_argument_errors():
+    ws = zc.zipccl_decompress_workspace_bytes(100, 1)
+    assert zc.zipccl_decompress(FAKE, FAKE, 0, FAKE, 100, FAKE, ws, 0) == zc.ERR_INVALID_ARG
+    assert zc.zipccl_decompress(FAKE + 4, FAKE, 1, FAKE, 100, FAKE, ws, 0) == zc.ERR_INVALID_ARG
+    assert zc.zipccl_decompress(FAKE, FAKE, 1, FAKE, 100, FAKE, ws - 1, 0) == zc.ERR_CAPACITY
+    rws = zc.zipccl_reduce_workspace_bytes(2)
+    assert zc.zipccl_decompress_reduce([FAKE, FAKE], [64, 64], 0, 10, FAKE, FAKE, rws, 0) == zc.ERR_INVALID_ARG
+    assert zc.zipccl_decompress_reduce([FAKE] * 17, [64] * 17, 17, 10, FAKE, FAKE, 1 << 30, 0) == \
+        zc.ERR_INVALID_ARG
+    assert zc.zipccl_decompress_reduce([FAKE, FAKE + 8], [64, 64], 2, 10, FAKE, FAKE, rws, 0) == \
+        zc.ERR_INVALID_ARG
+    assert zc.zipccl_decompress_reduce([FAKE, 0], [64, 64], 2, 10, FAKE, FAKE, rws, 0) == zc.ERR_INVALID_ARG
+    assert zc.zipccl_decompress_reduce([FAKE, FAKE], [64, 64], 2, 10, FAKE, FAKE, rws - 1, 0) == zc.ERR_CAPACITY
+    assert zc.zipccl_get_device_status(0, 0) == zc.ERR_INVALID_ARG
+
+
+def test_product_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "lossless_bf16_tensor_zipccl_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in src and "from oracle" not in src and "zipccl_oracle" not in src, f

@@ -1,0 +1,246 @@
+"""GPU path vs the CPU oracle, through the C ABI.
+
+Bar: compressed streams and chunk offsets byte-identical to the oracle's,
+decompression bit-identical to the input, decompress_reduce bit-identical to
+the oracle's fixed-order fp32 fold.  Small cases span several tiles and ragged
+tails; the full-size workloads are checked on sampled chunks against the
+oracle (each chunk is a self-contained stream, so the oracle can encode it
+alone) and through properties that hold at any size (exact round trip,
+worst-case bound).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import lossless_bf16_tensor_zipccl_gb300 as zc  # noqa: E402
+import oracle  # noqa: E402
+import workloads  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    zc.load()
+    yield
+
+
+def to_dev(x: np.ndarray):
+    return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda()
+
+
+def stream_bytes(c: zc.Compressed) -> tuple[bytes, np.ndarray]:
+    offs = c.offsets.cpu().numpy().view(np.uint64)
+    return c.data[: int(offs[-1])].cpu().numpy().tobytes(), offs
+
+
+def gpu_roundtrip(x: np.ndarray, chunk_elems=None, hint=None, check_oracle=True):
+    d = to_dev(x)
+    c = zc.compress(d, chunk_elems, hint)
+    y = zc.decompress(c)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), d), "decompressed words differ from the input"
+    s, offs = stream_bytes(c)
+    if check_oracle:
+        so, oo = oracle.compress(x, chunk_elems, hint)
+        assert np.array_equal(offs, oo), "chunk offsets differ from the oracle"
+        assert s == so, f"stream differs from the oracle at byte {next(i for i in range(min(len(s), len(so))) if s[i] != so[i]) if len(s) == len(so) else 'length'}"
+    return c, s, offs
+
+
+# ------------------------------------------------------------------ small parity
+def test_pr1_parity_and_ratio():
+    w = workloads.pr1()
+    c, s, _ = gpu_roundtrip(w.x)
+    bpv = 8.0 * len(s) / w.n
+    h = oracle.entropy_bits(oracle.exponent_pmf(0.02))
+    assert bpv <= 1.01 * (8 + h) and bpv < 11.0
+
+
+def test_all_patterns_parity():
+    gpu_roundtrip(workloads.all_patterns().x)
+
+
+def test_spliced_patterns_escape_parity():
+    g = workloads.gaussian_bf16(1 << 20, 0.02, 11)
+    pos = np.random.default_rng(3).choice(g.size, 65536, replace=False)
+    g[pos] = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    gpu_roundtrip(g)
+
+
+@pytest.mark.parametrize("n", [0, 1, 7, 8, 9, 255, 256, 257, 2047, 32767, 32768, 32769, 65536 + 300, 3 * 32768 + 4095])
+def test_edge_sizes_parity(n):
+    gpu_roundtrip(workloads.gaussian_bf16(n, 0.5, 21, n), [n])
+
+
+@pytest.mark.parametrize("fill", [0x0000, 0x8000, 0x7FC0, 0xFFFF, 0x7F80, 0x0001, 0x3F80])
+def test_constant_chunks_parity(fill):
+    gpu_roundtrip(np.full(40000, fill, np.uint16))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_ragged_chunk_mixes_parity(seed):
+    w = workloads.random_chunks(100 + seed, n_chunks=int(2 + 3 * seed), max_elems=90000)
+    hints = None
+    if seed % 2:
+        hints = [s if i % 3 else 0.0 for i, s in enumerate(w.sigma)]
+    gpu_roundtrip(w.x, w.chunk_elems, hints)
+
+
+def test_empty_and_tiny_chunks():
+    sizes = [0, 0, 1, 0, 9, 32768, 0, 3]
+    x = workloads.gaussian_bf16(sum(sizes), 1.0, 8)
+    gpu_roundtrip(x, sizes)
+
+
+def test_many_chunks_more_than_one_select_batch():
+    sizes = [int(v) for v in np.random.default_rng(5).integers(0, 3000, size=600)]
+    x = workloads.gaussian_bf16(sum(sizes), 0.01, 9)
+    gpu_roundtrip(x, sizes)
+
+
+def test_gpu_decodes_oracle_stream():
+    w = workloads.random_chunks(77, n_chunks=6, max_elems=120000)
+    s, offs = oracle.compress(w.x, w.chunk_elems)
+    buf = torch.from_numpy(np.frombuffer(s, dtype=np.uint8).copy()).cuda()
+    o = torch.from_numpy(offs.view(np.int64).copy()).cuda()
+    c = zc.Compressed(buf, o, w.n, w.chunk_elems)
+    y = zc.decompress(c)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), w.x)
+
+
+def test_repeated_calls_reuse_workspace():
+    x = workloads.gaussian_bf16(200000, 0.1, 4)
+    d = to_dev(x)
+    ws = torch.empty(zc.zipccl_compress_workspace_bytes([200000]), dtype=torch.uint8, device="cuda")
+    first = None
+    for _ in range(3):
+        c = zc.compress(d, ws=ws)
+        s, _ = stream_bytes(c)
+        first = first or s
+        assert s == first
+
+
+# ------------------------------------------------------------------ reduce
+def oracle_chunks(xs):
+    return [oracle.compress(x)[0] for x in xs]
+
+
+def dev_chunks(chunks):
+    return [torch.from_numpy(np.frombuffer(c, dtype=np.uint8).copy()).cuda() for c in chunks]
+
+
+@pytest.mark.parametrize("k,n", [(1, 1000), (2, 32768), (3, 70001), (5, 40000), (8, 100000), (16, 33000)])
+def test_reduce_parity(k, n):
+    rng = np.random.default_rng(k * 1000 + n)
+    xs = [workloads.gaussian_bf16(n, 10.0 ** rng.uniform(-3, 1), 55, k, p) for p in range(k)]
+    if n > 100:
+        xs[0][:5] = np.array([0x7F80, 0xFF80, 0x7FC1, 0x0001, 0x8001], np.uint16)
+    chunks = oracle_chunks(xs)
+    ref = oracle.decompress_reduce(chunks, n)
+    y = zc.decompress_reduce(dev_chunks(chunks), n)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), ref)
+
+
+def test_reduce_raw_and_coded_tiles_mixed():
+    n = 100000
+    a = workloads.gaussian_bf16(n, 0.3, 1)
+    b = np.random.default_rng(2).integers(0, 65536, size=n, dtype=np.uint16)  # raw tiles
+    chunks = oracle_chunks([a, b, a])
+    ref = oracle.decompress_reduce(chunks, n)
+    y = zc.decompress_reduce(dev_chunks(chunks), n)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), ref)
+
+
+# ------------------------------------------------------------------ robustness
+def corrupt_status(buf: bytes, offs, n):
+    d = torch.from_numpy(np.frombuffer(buf, dtype=np.uint8).copy()).cuda()
+    o = torch.from_numpy(np.asarray(offs, dtype=np.uint64).view(np.int64).copy()).cuda()
+    out = torch.empty(max(1, n), dtype=torch.int16, device="cuda")
+    wsb = zc.zipccl_decompress_workspace_bytes(n, len(offs) - 1)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    st = zc.zipccl_decompress(d.data_ptr(), o.data_ptr(), len(offs) - 1, out.data_ptr(), n, ws.data_ptr(), wsb, s)
+    assert st == zc.OK
+    return zc.zipccl_get_device_status(ws.data_ptr(), s)
+
+
+def test_corrupt_streams_report_status():
+    x = workloads.gaussian_bf16(70000, 0.05, 3)
+    s, offs = oracle.compress(x)
+    n = x.size
+    b = bytearray(s)
+    assert corrupt_status(bytes(b), offs, n) == zc.OK
+    bad = bytearray(s); bad[0] ^= 1
+    assert corrupt_status(bytes(bad), offs, n) == zc.ERR_CORRUPT          # magic
+    bad = bytearray(s); bad[4] = 2
+    assert corrupt_status(bytes(bad), offs, n) == zc.ERR_VERSION          # version
+    bad = bytearray(s); bad[24] = 0x11
+    assert corrupt_status(bytes(bad), offs, n) == zc.ERR_CORRUPT          # lengths break Kraft
+    bad = bytearray(s); bad[32:36] = (10 ** 7).to_bytes(4, "little")
+    assert corrupt_status(bytes(bad), offs, n) == zc.ERR_CORRUPT          # tile offset past the end
+    t0 = int.from_bytes(s[32:36], "little")
+    bad = bytearray(s); bad[t0 + 8:t0 + 12] = (60000).to_bytes(4, "little")
+    assert corrupt_status(bytes(bad), offs, n) == zc.ERR_CORRUPT          # exponent bytes inconsistent
+    assert corrupt_status(s, offs, n + 1) == zc.ERR_CORRUPT               # element count mismatch
+    short = np.array(offs, dtype=np.uint64); short[-1] -= 16
+    assert corrupt_status(s[: int(short[-1])], short, n) == zc.ERR_CORRUPT  # truncated
+
+
+# ------------------------------------------------------------------ full-size workloads
+def sampled_chunk_parity(w: workloads.Workload, c: zc.Compressed, chunks_to_check):
+    s, offs = stream_bytes(c)
+    starts = np.concatenate([[0], np.cumsum(w.chunk_elems)])
+    for ci in chunks_to_check:
+        xo = w.x[starts[ci]: starts[ci + 1]]
+        so, _ = oracle.compress(xo, [xo.size])
+        assert s[int(offs[ci]): int(offs[ci + 1])] == so, f"chunk {ci} differs from the oracle"
+    return s, offs
+
+
+def full_size(w: workloads.Workload, sample):
+    d = to_dev(w.x)
+    c = zc.compress(d, w.chunk_elems)
+    y = zc.decompress(c)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), d)
+    s, offs = sampled_chunk_parity(w, c, sample)
+    assert len(s) <= zc.zipccl_max_compressed_bytes(w.chunk_elems)
+    return s, offs
+
+
+def test_full_gradient_bucket_and_reduce():
+    w = workloads.gradient()
+    s, _ = full_size(w, range(8))
+    h = oracle.entropy_bits(oracle.exponent_pmf(1e-3))
+    assert 8.0 * len(s) / w.n <= 1.02 * (8 + h)
+    peers = workloads.gradient_peers()
+    chunks = oracle_chunks(peers)
+    ref = oracle.decompress_reduce(chunks, peers[0].size)
+    y = zc.decompress_reduce(dev_chunks(chunks), peers[0].size)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), ref)
+
+
+def test_full_moe_dispatch():
+    w = workloads.moe()
+    full_size(w, [0, 17, 40, 63])
+
+
+def test_full_stress_escape_path():
+    w = workloads.stress()
+    s, offs = full_size(w, [0, 5, 15, 31, 100, 255])
+    for c in (15, 31):  # uniform random patterns: bounded expansion
+        assert int(offs[c + 1] - offs[c]) <= zc.zipccl_max_compressed_bytes([w.chunk_elems[c]])
+
+
+def test_full_fsdp_allgather():
+    w = workloads.fsdp()
+    full_size(w, [0, 9, 100, 223])
