@@ -211,6 +211,21 @@ def run_reference(args, rank: int, world: int):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The slowest rank's time (the job's time) on every rank; identity at world 1."""
+    if world <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank compresses its own bucket (weak scaling)."""
+    return 100 + 10007 * rank
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, rank: int, world: int):
     import torch
@@ -221,7 +236,7 @@ def run_ours(args, rank: int, world: int):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     zc.load()
-    seed = 100 + 10007 * rank
+    seed = rank_seed(rank)
     wl = workloads.gradient(seed=seed)
     peers = workloads.gradient_peers(seed=seed)
     chunk_elems = wl.chunk_elems
@@ -292,11 +307,7 @@ def run_ours(args, rank: int, world: int):
     stage_ms = {name: [ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)]
                 for j, (name, _) in enumerate(stages)}
     step_ms = [sum(stage_ms[n][i] for n, _ in stages) for i in range(args.steps)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
 
     unc = {"compress": 2 * N_BUCKET, "decompress": 2 * N_BUCKET, "decompress_reduce": 2 * K_PEERS * PEER_N}
     algo = {"compress": 2 * N_BUCKET + comp_bytes, "decompress": comp_bytes + 2 * N_BUCKET,

@@ -8,7 +8,7 @@
 
 #include <memory>
 
-#include "../../include/zipccl.h"
+#include "zipccl.h"
 #include "zc_codebook.h"
 #include "zc_device.cuh"
 #include "zc_format.h"
@@ -49,12 +49,12 @@ DecLayout dec_layout(uint32_t nc) {
   L.off_chunks = sizeof(WsHeader);
   L.off_item_start = L.off_chunks + pad256(sizeof(DecChunk) * (uint64_t)nc);
   L.off_luts = L.off_item_start + pad256(4 * ((uint64_t)nc + 1));
-  L.total = L.off_luts + (uint64_t)nc * kLutEntries * sizeof(uint2);
+  L.total = L.off_luts + (uint64_t)nc * kLutEntries * sizeof(uint32_t);
   return L;
 }
 
 uint64_t red_ws(uint32_t k) {
-  return sizeof(WsHeader) + pad256(sizeof(DecChunk) * (uint64_t)k) + (uint64_t)k * kLutEntries * sizeof(uint2);
+  return sizeof(WsHeader) + pad256(sizeof(DecChunk) * (uint64_t)k) + (uint64_t)k * kLutEntries * sizeof(uint32_t);
 }
 
 zipccl_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ZIPCCL_OK : ZIPCCL_ERR_CUDA; }
@@ -219,7 +219,7 @@ zipccl_status zipccl_decompress(const void* d_stream, const uint64_t* d_chunk_of
   pa.offsets = d_chunk_offsets;
   pa.chunks = reinterpret_cast<DecChunk*>(ws + L.off_chunks);
   pa.item_start = reinterpret_cast<uint32_t*>(ws + L.off_item_start);
-  pa.luts = reinterpret_cast<uint2*>(ws + L.off_luts);
+  pa.luts = reinterpret_cast<uint32_t*>(ws + L.off_luts);
   pa.hdr = reinterpret_cast<WsHeader*>(ws);
   pa.n_chunks = n_chunks;
   pa.max_items = (uint32_t)max_items;
@@ -254,7 +254,7 @@ zipccl_status zipccl_decompress_reduce(const void* const* d_peer_chunks, const u
   if (e != cudaSuccess) return ZIPCCL_ERR_CUDA;
   ra.hdr = reinterpret_cast<WsHeader*>(ws);
   ra.chunks = reinterpret_cast<DecChunk*>(ws + sizeof(WsHeader));
-  ra.luts = reinterpret_cast<uint2*>(ws + sizeof(WsHeader) + pad256(sizeof(DecChunk) * (uint64_t)k));
+  ra.luts = reinterpret_cast<uint32_t*>(ws + sizeof(WsHeader) + pad256(sizeof(DecChunk) * (uint64_t)k));
   ra.out = d_out;
   ra.n = n;
   ra.k = k;

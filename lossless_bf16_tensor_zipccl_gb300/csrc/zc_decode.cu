@@ -62,6 +62,9 @@ struct TileView {
 
 __device__ bool open_tile(const uint8_t* ch, uint64_t bytes, uint32_t n_tiles, uint32_t k, uint32_t nt,
                           uint32_t lane, TileView& tv) {
+  tv.tile = ch;
+  tv.mode = 1;
+  tv.exp_off = tv.exp_bytes = tv.wstart = tv.words = 0;
   const uint64_t toff = ld_u32(ch + kChunkHdr + 4ull * k);
   if ((toff & 15) || toff < chunk_hdr_bytes(n_tiles) || toff + kTileHdr > bytes) return false;
   const uint8_t* t = ch + toff;
@@ -100,16 +103,20 @@ __device__ __forceinline__ uint2 load_bytes8(const uint8_t* p, uint32_t cnt) {
   return make_uint2(lo, hi);
 }
 
+constexpr uint32_t kSmBlkRows = 8;                    // rows per staged sign/mantissa block
+constexpr uint32_t kSmBlkBytes = kSmBlkRows * kRow;    // 2 KB
+
 // Decode one 8-element lane group of row r into 4 words (8 BF16).
 struct RowSource {
   TileView tv;
   LaneDecoder dec;
   uint32_t nt, lane;
 
-  __device__ __forceinline__ void start(const uint2* lut, uint32_t base) {
-    if (lane == 0) bulk_prefetch_l2(tv.tile, (uint32_t)(tv.exp_off + pad16(tv.exp_bytes)));
+  // exp: the tile's exponent region, staged in shared memory or in place in
+  // global memory.
+  __device__ __forceinline__ void start(const uint32_t* lut, uint32_t base, const uint8_t* exp) {
     if (tv.mode == 0)
-      dec.init(reinterpret_cast<const uint32_t*>(tv.tile + tv.exp_off + kSegTab) + tv.wstart, tv.words, lut, base);
+      dec.init(reinterpret_cast<const uint32_t*>(exp + kSegTab) + tv.wstart, tv.words, lut, base);
   }
 
   __device__ __forceinline__ uint32_t count(uint32_t r) const {
@@ -133,10 +140,89 @@ struct RowSource {
     return make_uint4(a.x, a.y, b.x, b.y);
   }
 
-  __device__ __forceinline__ uint2 sm(uint32_t r) const {
-    return load_bytes8(tv.tile + kTileHdr + r * kRow + lane * kLaneElems, count(r));
+  // sign/mantissa bytes of row r from its staged block (shared memory)
+  __device__ __forceinline__ uint2 sm_staged(const uint8_t* blk, uint32_t r) const {
+    const uint32_t cnt = count(r);
+    const uint8_t* p = blk + (r % kSmBlkRows) * kRow + lane * kLaneElems;
+    if (cnt == 8) return *reinterpret_cast<const uint2*>(p);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      if (t < (int)cnt) {
+        const uint32_t b = p[t];
+        if (t < 4) lo |= b << (8 * t);
+        else hi |= b << (8 * (t - 4));
+      }
+    }
+    return make_uint2(lo, hi);
   }
 };
+
+// Double-buffered TMA staging of a tile's sign/mantissa plane, kSmBlkRows
+// rows (2 KB) per block, one warp.  Block b lives in stage b & 1; its barrier
+// completes phase b >> 1.
+struct SmStager {
+  uint8_t* buf;       // 2 x kSmBlkBytes, 16-B aligned
+  uint64_t* bars;     // 2 barriers
+  const uint8_t* g;   // the plane in global memory (tile + 16)
+  uint32_t plane;     // padded plane bytes (multiple of 16)
+  uint32_t nblk;
+
+  __device__ __forceinline__ void issue(uint32_t b) {
+    const uint32_t off = b * kSmBlkBytes;
+    const uint32_t bytes = min(kSmBlkBytes, plane - off);
+    bulk_load_async(buf + (b & 1) * kSmBlkBytes, g + off, bytes, bars + (b & 1));
+  }
+  __device__ __forceinline__ void start(uint32_t lane) {
+    if (lane == 0) {
+      mbar_init(bars, 1);
+      mbar_init(bars + 1, 1);
+      if (nblk > 0) issue(0);
+      if (nblk > 1) issue(1);
+    }
+    __syncwarp();
+  }
+  // Wait for block b; false when the bounded wait gave up (warp-uniform).
+  __device__ __forceinline__ bool acquire(uint32_t b) {
+    const bool ok = mbar_wait(bars + (b & 1), (b >> 1) & 1);
+    return !__any_sync(kFull, !ok);
+  }
+  __device__ __forceinline__ const uint8_t* block(uint32_t b) const { return buf + (b & 1) * kSmBlkBytes; }
+  // Every lane is done with block b: refill its stage with block b + 2.
+  __device__ __forceinline__ void release(uint32_t b, uint32_t lane) {
+    __syncwarp();
+    if (lane == 0 && b + 2 < nblk) issue(b + 2);
+  }
+};
+
+// Stage a coded tile's exponent region in shared memory with one TMA bulk
+// load when it fits `slot` bytes (lane 0 issues, every lane waits).  Returns
+// the region to decode from (shared or global) and sets `timeout` when the
+// bounded wait gave up (warp-uniform).
+__device__ __forceinline__ const uint8_t* stage_exponents(const TileView& tv, uint8_t* slot, uint32_t slot_bytes,
+                                                         uint64_t* bar, uint32_t lane, bool& timeout) {
+  timeout = false;
+  const uint8_t* g = tv.tile + tv.exp_off;
+  const uint32_t bytes = (uint32_t)pad16(tv.exp_bytes);
+  if (tv.mode != 0 || bytes > slot_bytes) return g;
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    bulk_load_async(slot, g, bytes, bar);
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(bar, 0);
+  timeout = __any_sync(kFull, !ok);
+  return slot;
+}
+
+// Copy one chunk's 4-KB decode table into shared memory (one warp).
+__device__ __forceinline__ void load_lut_warp(uint32_t* dst, const uint32_t* src, uint32_t lane) {
+  const uint4* g = reinterpret_cast<const uint4*>(src);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (uint32_t i = lane; i < kLutEntries / 4; i += 32) d[i] = __ldg(g + i);
+  __syncwarp();
+}
 
 __device__ __forceinline__ void store_row(uint16_t* y, uint32_t cnt, bool vec, uint4 v) {
   if (cnt == 8 && vec) {
@@ -239,12 +325,15 @@ __global__ void __launch_bounds__(256) zc_dprep_kernel(DprepArgs a) {
   }
 }
 
-constexpr int kDecWarps = 4;
-
-// One warp per tile.
-__global__ void __launch_bounds__(kDecWarps * 32) zc_decode_kernel(DecodeArgs a) {
-  const uint32_t lane = threadIdx.x & 31;
-  const uint32_t item = blockIdx.x * kDecWarps + (threadIdx.x >> 5);
+// One warp (one CTA) per tile.
+constexpr uint32_t kExpSlot = 12288;  // staged exponent region; larger regions are read in place
+__global__ void __launch_bounds__(32) zc_decode_kernel(DecodeArgs a) {
+  __shared__ __align__(128) uint8_t s_exp[kExpSlot];
+  __shared__ __align__(128) uint8_t s_sm[2 * kSmBlkBytes];
+  __shared__ __align__(16) uint32_t s_lut[kLutEntries];
+  __shared__ __align__(8) uint64_t s_bar[3];
+  const uint32_t lane = threadIdx.x;
+  const uint32_t item = blockIdx.x;
   // lane 0 reads the status once and the warp follows it together
   uint32_t bad = lane == 0 ? *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) : 0u;
   bad = __shfl_sync(kFull, bad, 0);
@@ -272,30 +361,36 @@ __global__ void __launch_bounds__(kDecWarps * 32) zc_decode_kernel(DecodeArgs a)
     if (lane == 0) set_status(a.hdr, kStCorrupt);
     return;
   }
-  src.start(a.luts + (size_t)c * kLutEntries, d.base);
+  SmStager stg;
+  stg.buf = s_sm;
+  stg.bars = s_bar + 1;
+  stg.g = src.tv.tile + kTileHdr;
+  stg.plane = (uint32_t)pad16(nt);
+  stg.nblk = (nt + kSmBlkBytes - 1) / kSmBlkBytes;
+  stg.start(lane);
+  bool timeout;
+  const uint8_t* exp = stage_exponents(src.tv, s_exp, kExpSlot, s_bar, lane, timeout);
+  load_lut_warp(s_lut, a.luts + (size_t)c * kLutEntries, lane);
+  src.start(s_lut, d.base, exp);
   const uint64_t e0 = d.elem_start + (uint64_t)k * kTile;
   uint16_t* y = a.out + e0;
   const bool vec = (e0 & 7) == 0;
   const uint32_t rows = (nt + kRow - 1) / kRow;
-  // sign/mantissa bytes run 4 rows ahead of the decoder
-  uint2 q0 = src.sm(0), q1 = src.sm(1), q2 = src.sm(2), q3 = src.sm(3);
-  for (uint32_t r = 0; r < rows; r += 4) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t rr = r + j;
-      if (rr < rows) {
-        uint2 cur = j == 0 ? q0 : (j == 1 ? q1 : (j == 2 ? q2 : q3));
-        const uint2 nxt = src.sm(rr + 4);
-        if (j == 0) q0 = nxt;
-        else if (j == 1) q1 = nxt;
-        else if (j == 2) q2 = nxt;
-        else q3 = nxt;
-        const uint32_t cnt = src.count(rr);
-        const uint4 v = src.row(rr, cur);
-        if (cnt) store_row(y + rr * kRow + lane * kLaneElems, cnt, vec, v);
-      }
+  for (uint32_t b = 0; b < stg.nblk && !timeout; ++b) {
+    if (!stg.acquire(b)) {
+      timeout = true;
+      break;
     }
+    const uint8_t* blk = stg.block(b);
+    const uint32_t rend = min(rows, (b + 1) * kSmBlkRows);
+    for (uint32_t r = b * kSmBlkRows; r < rend; ++r) {
+      const uint32_t cnt = src.count(r);
+      const uint4 v = src.row(r, src.sm_staged(blk, r));
+      if (cnt) store_row(y + r * kRow + lane * kLaneElems, cnt, vec, v);
+    }
+    stg.release(b, lane);
   }
+  if (timeout && lane == 0) set_status(a.hdr, kStTimeout);
 }
 
 // ---------------------------------------------------------------- reduce
@@ -336,16 +431,30 @@ __device__ __forceinline__ void add_bf16x2(float& a0, float& a1, uint32_t w) {
   a1 = __fadd_rn(a1, __uint_as_float(w & 0xFFFF0000u));
 }
 
-// One block per tile, one warp per peer.  Rows are decoded 16 at a time into
-// shared memory (peer-major), then every thread folds 8 elements across the
-// peers in rank order.
-constexpr uint32_t kRedRows = 16;
+// One block per tile, one warp per peer.  Each warp stages its peer's
+// exponent region and decode table in shared memory, then rows are decoded 8
+// at a time into shared memory (peer-major) and every thread folds 8 values
+// across the peers in rank order.
+constexpr uint32_t kRedRows = kSmBlkRows;
+constexpr uint32_t kRedStageBytes = kRedRows * kRow * 2;  // decoded BF16 rows per peer
+constexpr uint32_t kRedMaxStagedPeers = 9;                 // exponent slots fit in shared memory up to here
+
+__host__ __device__ constexpr size_t reduce_smem_bytes(uint32_t k) {
+  return (size_t)k * (kRedStageBytes + 2 * kSmBlkBytes + kLutEntries * 4 +
+                      (k <= kRedMaxStagedPeers ? kExpSlot : 0) + 32);
+}
 
 __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
-  extern __shared__ __align__(16) uint16_t sbuf[];  // k x kRedRows x kRow
+  extern __shared__ __align__(128) uint8_t rsm[];
   const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5, tid = threadIdx.x;
   const uint32_t t = blockIdx.x;
   const uint32_t nthreads = 32 * a.k;
+  const bool staged = a.k <= kRedMaxStagedPeers;
+  uint16_t* sbuf = reinterpret_cast<uint16_t*>(rsm);                           // k x kRedRows x kRow values
+  uint8_t* smst = rsm + (size_t)a.k * kRedStageBytes;                         // k x 2 staged s/m blocks
+  uint32_t* luts = reinterpret_cast<uint32_t*>(smst + (size_t)a.k * 2 * kSmBlkBytes);  // k x 1024
+  uint8_t* slots = reinterpret_cast<uint8_t*>(luts + (size_t)a.k * kLutEntries);       // k x kExpSlot
+  uint64_t* bars = reinterpret_cast<uint64_t*>(slots + (staged ? (size_t)a.k * kExpSlot : 0));  // k x 3
   __shared__ int s_bad;
   // one read of the status word per block, so every thread takes the same path
   if (tid == 0) s_bad = *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0;
@@ -356,26 +465,38 @@ __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
   RowSource src;
   src.nt = nt;
   src.lane = lane;
-  bool ok = d.ok && open_tile(a.peers[p], d.bytes, d.n_tiles, t, nt, lane, src.tv);
-  if (!ok && lane == 0) {
+  const bool ok = d.ok && open_tile(a.peers[p], d.bytes, d.n_tiles, t, nt, lane, src.tv);
+  bool timeout = false;
+  const uint8_t* exp = src.tv.tile;
+  SmStager stg;
+  stg.buf = smst + (size_t)p * 2 * kSmBlkBytes;
+  stg.bars = bars + 3 * p + 1;
+  stg.g = src.tv.tile + kTileHdr;
+  stg.plane = (uint32_t)pad16(nt);
+  stg.nblk = (nt + kSmBlkBytes - 1) / kSmBlkBytes;
+  if (ok) {
+    stg.start(lane);
+    exp = stage_exponents(src.tv, slots + (size_t)p * kExpSlot, staged ? kExpSlot : 0u, bars + 3 * p, lane, timeout);
+    load_lut_warp(luts + (size_t)p * kLutEntries, a.luts + (size_t)p * kLutEntries, lane);
+  }
+  if (lane == 0 && (!ok || timeout)) {
     s_bad = 1;
-    set_status(a.hdr, kStCorrupt);
+    set_status(a.hdr, ok ? kStTimeout : kStCorrupt);
   }
   __syncthreads();
   if (s_bad) return;  // uniform
-  src.start(a.luts + (size_t)p * kLutEntries, d.base);
+  src.start(luts + (size_t)p * kLutEntries, d.base, exp);
   uint16_t* mine = sbuf + (size_t)p * kRedRows * kRow;
   const uint32_t rows = (nt + kRow - 1) / kRow;
   uint16_t* y = a.out + (uint64_t)t * kTile;
-  for (uint32_t r0 = 0; r0 < rows; r0 += kRedRows) {
-    const uint32_t rend = min(rows, r0 + kRedRows);
-    uint2 q = src.sm(r0);
-    for (uint32_t r = r0; r < rend; ++r) {
-      const uint2 cur = q;
-      q = src.sm(r + 1 < rend ? r + 1 : rend);
-      const uint4 v = src.row(r, cur);
-      *reinterpret_cast<uint4*>(mine + (r - r0) * kRow + lane * kLaneElems) = v;
-    }
+  bool late = false;  // a bounded wait gave up: finish the loop, report it
+  for (uint32_t b = 0; b < stg.nblk; ++b) {
+    if (!late && !stg.acquire(b)) late = true;
+    const uint8_t* blk = stg.block(b);
+    const uint32_t r0 = b * kRedRows, rend = min(rows, r0 + kRedRows);
+    for (uint32_t r = r0; r < rend; ++r)
+      *reinterpret_cast<uint4*>(mine + (r - r0) * kRow + lane * kLaneElems) = src.row(r, src.sm_staged(blk, r));
+    if (!late) stg.release(b, lane);
     __syncthreads();
     const uint32_t m = min(kRedRows * kRow, nt - r0 * kRow);
     for (uint32_t e = tid * 8; e < m; e += nthreads * 8) {
@@ -405,6 +526,7 @@ __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
     }
     __syncthreads();
   }
+  if (late && lane == 0) set_status(a.hdr, kStTimeout);
 }
 
 // ---------------------------------------------------------------- launchers
@@ -414,7 +536,7 @@ cudaError_t launch_decode(const DprepArgs& prep, const DecodeArgs& args, uint32_
   zc_dprep_kernel<<<prep.n_chunks + 1, 256, 0, s>>>(prep);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || max_items == 0) return e;
-  zc_decode_kernel<<<(max_items + kDecWarps - 1) / kDecWarps, kDecWarps * 32, 0, s>>>(args);
+  zc_decode_kernel<<<max_items, 32, 0, s>>>(args);
   return cudaGetLastError();
 }
 
@@ -422,9 +544,10 @@ cudaError_t launch_reduce(const ReduceArgs& args, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int smem_max = (int)(kMaxPeers * kRedRows * kRow * sizeof(uint16_t));
+  size_t smem_max = 0;
+  for (uint32_t k = 1; k <= kMaxPeers; ++k) smem_max = reduce_smem_bytes(k) > smem_max ? reduce_smem_bytes(k) : smem_max;
   if (dev >= 0 && dev < 64 && !g_red_attr_done[dev]) {
-    e = cudaFuncSetAttribute(zc_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    e = cudaFuncSetAttribute(zc_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
     if (e != cudaSuccess) return e;
     g_red_attr_done[dev] = 1;
   }
@@ -432,8 +555,7 @@ cudaError_t launch_reduce(const ReduceArgs& args, cudaStream_t s) {
   e = cudaGetLastError();
   if (e != cudaSuccess || args.n == 0) return e;
   const uint32_t tiles = (uint32_t)tiles_of(args.n);
-  const size_t smem = (size_t)args.k * kRedRows * kRow * sizeof(uint16_t);
-  zc_reduce_kernel<<<tiles, 32 * args.k, smem, s>>>(args);
+  zc_reduce_kernel<<<tiles, 32 * args.k, reduce_smem_bytes(args.k), s>>>(args);
   return cudaGetLastError();
 }
 

@@ -62,41 +62,64 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// TMA bulk copy shared -> global (no multicast), then wait until it is done.
-__device__ __forceinline__ void bulk_store_and_wait(void* gdst, const void* ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
-               "r"(smem_addr(ssrc)), "r"(bytes)
+// TMA bulk store shared -> global (no multicast); several may be issued
+// before one commit.  bulk_commit_and_wait_read waits until shared memory has
+// been read; the global writes complete on their own before the grid ends.
+__device__ __forceinline__ void bulk_store_issue(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_addr(ssrc)),
+               "r"(bytes)
                : "memory");
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// Two TMA bulk copies shared -> global in one group, then wait.
-__device__ __forceinline__ void bulk_store2_and_wait(void* g0, const void* s0, uint32_t b0, void* g1, const void* s1,
-                                                     uint32_t b1) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(g0), "r"(smem_addr(s0)), "r"(b0)
-               : "memory");
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(g1), "r"(smem_addr(s1)), "r"(b1)
-               : "memory");
+__device__ __forceinline__ void bulk_commit_and_wait_read() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// ---- mbarrier-tracked TMA bulk load global -> shared (single use, phase 0)
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_load_async(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(sdst)),
+               "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
+// Wait for phase `parity` of the barrier, giving up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_addr(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
 }
 
 // ---------------------------------------------------------------- code tables
-// Canonical codeword (MSB-first value) of symbol `sym` for packed lengths.
+// Canonical codeword (MSB-first value) of symbol `sym` for packed lengths:
+// codes are handed out in (length, symbol) order, so the code of s counts, at
+// length L(s), every code value taken by a symbol that precedes it:
+//   code(s) = sum_{t before s} 2^(L(s) - L(t)).
 __device__ __forceinline__ uint32_t canonical_code(uint64_t lens, int sym) {
-  int count[kLmax + 1];
+  const uint32_t L = (uint32_t)((lens >> (4 * sym)) & 15);
+  uint32_t code = 0;
 #pragma unroll
-  for (int l = 0; l <= kLmax; ++l) count[l] = 0;
-#pragma unroll
-  for (int s = 0; s < kNsym; ++s) count[(lens >> (4 * s)) & 15]++;
-  const int L = (int)((lens >> (4 * sym)) & 15);
-  uint32_t first = 0;
-  for (int l = 1; l < L; ++l) first = (first + count[l]) << 1;
-  uint32_t rank = 0;
-  for (int s = 0; s < sym; ++s)
-    if ((int)((lens >> (4 * s)) & 15) == L) ++rank;
-  return first + rank;
+  for (int t = 0; t < kNsym; ++t) {
+    const uint32_t lt = (uint32_t)((lens >> (4 * t)) & 15);
+    if (lt < L || (lt == L && t < sym)) code += 1u << (L - lt);
+  }
+  return code;
 }
 
 __device__ __forceinline__ uint32_t bit_reverse(uint32_t v, int len) {
@@ -115,18 +138,24 @@ __host__ __device__ __forceinline__ bool lens_complete(uint64_t lens) {
 }
 
 // Multi-symbol decode table: entry i describes the symbols that the 10-bit
-// window i (next bits of the stream, LSB first) starts with.
-//   .x = up to 5 symbols, 4 bits each (first symbol lowest)
-//   .y = bits consumed | symbols << 8 | escape-last << 16
+// window i (next bits of the stream, LSB first) starts with, packed in 32 bits:
+//   bits 0-19  up to 5 symbols, 4 bits each (first symbol lowest)
+//   bits 20-23 bits consumed (<= 10)
+//   bits 24-26 symbols decoded (1..5)
+//   bit  27    the last symbol is the escape
 // Decoding stops after an escape; its 8 raw bits are not in the window count.
-__device__ __forceinline__ uint2 lut_entry(uint32_t idx, const uint8_t* L, const uint32_t* rev) {
+constexpr uint32_t kLutEsc = 1u << 27;
+
+__device__ __forceinline__ uint32_t lut_entry(uint32_t idx, uint64_t lens, const uint32_t (&rev)[kNsym]) {
   uint32_t pos = 0, ns = 0, nib = 0, esc = 0;
-  while (ns < 5) {
+#pragma unroll 1
+  while (ns < 5 && !esc) {
     int found = -1;
     uint32_t flen = 0;
+#pragma unroll
     for (int s = 0; s < kNsym; ++s) {
-      const uint32_t l = L[s];
-      if (l <= (uint32_t)kLmax - pos && ((idx >> pos) & ((1u << l) - 1u)) == rev[s]) {
+      const uint32_t l = (uint32_t)((lens >> (4 * s)) & 15);
+      if (l + pos <= (uint32_t)kLmax && ((idx >> pos) & ((1u << l) - 1u)) == rev[s]) {
         found = s;
         flen = l;
       }
@@ -135,23 +164,17 @@ __device__ __forceinline__ uint2 lut_entry(uint32_t idx, const uint8_t* L, const
     nib |= (uint32_t)found << (4 * ns);
     ++ns;
     pos += flen;
-    if (found == kEsc) {
-      esc = 1;
-      break;
-    }
+    esc = found == kEsc;
   }
-  return make_uint2(nib, pos | (ns << 8) | (esc << 16));
+  return nib | (pos << 20) | (ns << 24) | (esc << 27);
 }
 
 // Fill a 1024-entry table cooperatively (all threads of the block).
-__device__ __forceinline__ void build_lut(uint64_t lens, uint2* lut) {
-  uint8_t L[kNsym];
+__device__ __forceinline__ void build_lut(uint64_t lens, uint32_t* lut) {
   uint32_t rev[kNsym];
-  for (int s = 0; s < kNsym; ++s) {
-    L[s] = (uint8_t)((lens >> (4 * s)) & 15);
-    rev[s] = bit_reverse(canonical_code(lens, s), L[s]);
-  }
-  for (uint32_t i = threadIdx.x; i < kLutEntries; i += blockDim.x) lut[i] = lut_entry(i, L, rev);
+#pragma unroll
+  for (int s = 0; s < kNsym; ++s) rev[s] = bit_reverse(canonical_code(lens, s), (int)((lens >> (4 * s)) & 15));
+  for (uint32_t i = threadIdx.x; i < kLutEntries; i += blockDim.x) lut[i] = lut_entry(i, lens, rev);
 }
 
 // ---------------------------------------------------------------- merge
@@ -167,23 +190,23 @@ __device__ __forceinline__ uint2 merge4(uint32_t e4, uint32_t sm4) {
 
 // ---------------------------------------------------------------- lane decoder
 // Decodes one segment of a coded tile: symbols are taken 1-5 at a time from a
-// 1024-entry table indexed by the next 10 stream bits; the window is a funnel
+// 1024-entry table (in shared memory) indexed by the next 10 stream bits; the window is a funnel
 // shift over two words with a third prefetched.  Pending symbols wait as
 // nibbles in `acc`; escape exponents wait as bytes in escv (positions 0-7)
 // and esch (8-11).
 struct LaneDecoder {
   const uint32_t* seg;
-  const uint2* lut;
+  const uint32_t* lut;  // shared-memory copy of the chunk's table
   uint64_t acc, escv;
   uint32_t nw, wi, cur, nxt, nx2, boff, cnt, esch, base4;
 
-  __device__ __forceinline__ uint32_t word(uint32_t i) const { return i < nw ? __ldg(seg + i) : 0u; }
+  // seg points into shared memory (staged exponent region) or global memory
+  __device__ __forceinline__ uint32_t word(uint32_t i) const { return i < nw ? seg[i] : 0u; }
 
-  __device__ __forceinline__ void init(const uint32_t* s, uint32_t n_words, const uint2* table, uint32_t base) {
+  __device__ __forceinline__ void init(const uint32_t* s, uint32_t n_words, const uint32_t* table, uint32_t base) {
     seg = s;
     nw = n_words;
     lut = table;
-    for (uint32_t o = 32; o < nw; o += 32) prefetch_l1(seg + o);
     cur = word(0);
     nxt = word(1);
     nx2 = word(2);
@@ -200,11 +223,11 @@ struct LaneDecoder {
   __device__ __forceinline__ void fill(uint32_t target) {
     while (cnt < target) {
       const uint32_t win = __funnelshift_r(cur, nxt, boff);
-      const uint2 en = __ldg(lut + (win & (kLutEntries - 1)));
-      uint32_t nb = en.y & 0xFFu;
-      acc |= (uint64_t)en.x << (4 * cnt);
-      cnt += (en.y >> 8) & 0xFFu;
-      if (en.y & 0x10000u) {
+      const uint32_t en = lut[win & (kLutEntries - 1)];
+      uint32_t nb = (en >> 20) & 15u;
+      acc |= (uint64_t)(en & 0xFFFFFu) << (4 * cnt);
+      cnt += (en >> 24) & 7u;
+      if (en & kLutEsc) {
         const uint32_t e = (win >> nb) & 0xFFu;
         const uint32_t p = cnt - 1;
         nb += 8;

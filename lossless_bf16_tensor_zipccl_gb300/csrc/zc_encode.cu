@@ -104,10 +104,12 @@ __global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ 
 
 // ---------------------------------------------------------------- encode
 // Shared memory: tile image (header | sign/mantissa plane | exponent region)
-// | staged exponent bytes | encode table (256 x u32) | partial bit counts.
+// | staged exponent bytes | per-exponent table | pair table | part offsets.
 constexpr uint32_t kImgBytes = kTileHdr + kTile + kTile;
-constexpr uint32_t kEncSmem = kImgBytes + kTile + 256 * 4 + 256 * 4;
-constexpr int kEncThreads = 256;  // 8 warps; warp w owns rows 16w..16w+15
+constexpr int kEncThreads = 512;  // 16 warps; warp w owns rows 8w..8w+7
+constexpr int kEncWarps = kEncThreads / 32;
+constexpr int kRowsPerWarp = kRows / kEncWarps;
+constexpr uint32_t kEncSmem = kImgBytes + kTile + 256 * 4 + 256 * 4 + kEncWarps * 32 * 4;
 
 // Decoupled look-back over the flat tile list (warp-wide).  Each tile
 // publishes its byte count (aggregate), then its inclusive prefix.  Returns
@@ -152,12 +154,52 @@ __device__ uint64_t lookback(uint64_t* state, uint32_t item, uint32_t lane, bool
   }
 }
 
+// 4 exponent bytes -> 4 symbol bytes (x = e - base inside the window, else
+// 15 = escape); esc gets 0xFF in each escaped byte.
+__device__ __forceinline__ uint32_t symbols4(uint32_t e4, uint32_t base4, uint32_t& esc) {
+  const uint32_t x = __vsub4(e4, base4);          // per byte, mod 256
+  esc = __vcmpgeu4(x, 0x0F0F0F0Fu);               // x >= 15 (or wrapped below base)
+  return (x & ~esc) | (0x0F0F0F0Fu & esc);
+}
+
+// Pair indices of 4 symbol bytes: byte 0 = x0 | x1 << 4, byte 2 = x2 | x3 << 4.
+__device__ __forceinline__ uint32_t pairs4(uint32_t x4) { return x4 | (x4 >> 4); }
+
+// Bit sink for one lane's part of a segment in shared memory: the first word
+// and the last word may be shared with the neighbouring parts (OR-ed in); the
+// words in between belong to this part alone (stored).
+struct BitSink {
+  uint32_t* sw;
+  uint64_t acc;
+  uint32_t widx, nacc;
+  bool first;
+  __device__ __forceinline__ void put(uint32_t code, uint32_t len) {
+    acc |= (uint64_t)code << nacc;
+    nacc += len;
+    if (nacc >= 32) {
+      if (first) {
+        atomicOr(sw + widx, (uint32_t)acc);
+        first = false;
+      } else {
+        sw[widx] = (uint32_t)acc;
+      }
+      ++widx;
+      acc >>= 32;
+      nacc -= 32;
+    }
+  }
+  __device__ __forceinline__ void finish() {
+    if (nacc) atomicOr(sw + widx, (uint32_t)acc);
+  }
+};
+
 __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* img = smem;
   uint8_t* exps = smem + kImgBytes;  // exponent bytes in element order
-  uint32_t* tab = reinterpret_cast<uint32_t*>(smem + kImgBytes + kTile);
-  uint32_t* part = tab + 256;
+  uint32_t* tab = reinterpret_cast<uint32_t*>(smem + kImgBytes + kTile);  // per exponent: code | len << 24
+  uint32_t* pair = tab + 256;          // per symbol pair: codes (<= 20 bits) | len << 20, escape without raw bits
+  uint32_t* part = pair + 256;         // [warp][segment] bits, then bit offsets
   __shared__ uint32_t s_item, s_mode, s_err, s_size;
   __shared__ uint32_t s_wstart[32];
   __shared__ unsigned long long s_goff;
@@ -176,21 +218,28 @@ __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a)
   const uint64_t elem0 = ci.elem_start + (uint64_t)k * kTile;
   const uint16_t* x = a.in + elem0;
   const bool vec = (elem0 & 7) == 0;
-  const uint32_t base = ci.base;
+  const uint32_t base = ci.base, base4 = base * 0x01010101u;
   const uint32_t sm_pad = (uint32_t)pad16(nt);
   const uint32_t exp_off = kTileHdr + sm_pad;
 
-  // Encode table: entry for exponent value tid = reversed codeword | length << 24;
-  // an escape entry carries the 8 raw exponent bits after the codeword.
-  {
+  // Code tables.  tab[e]: reversed codeword | length << 24 (an escape entry
+  // carries the 8 raw exponent bits after the codeword).  pair[x0 | x1 << 4]:
+  // both reversed codewords, first one lowest | total length << 20.
+  if (tid < 256) {
     const int xs = (int)tid - (int)base;
     const int sym = (xs >= 0 && xs < kWindow) ? xs : kEsc;
     const int L = (int)((ci.lens >> (4 * sym)) & 15);
     const uint32_t rev = bit_reverse(canonical_code(ci.lens, sym), L);
     tab[tid] = sym == kEsc ? ((rev | (tid << L)) | ((uint32_t)(L + 8) << 24)) : (rev | ((uint32_t)L << 24));
+  } else {
+    const uint32_t pi = tid - 256, s0 = pi & 15, s1 = pi >> 4;
+    const uint32_t l0 = (uint32_t)((ci.lens >> (4 * s0)) & 15), l1 = (uint32_t)((ci.lens >> (4 * s1)) & 15);
+    const uint32_t c0 = bit_reverse(canonical_code(ci.lens, (int)s0), (int)l0);
+    const uint32_t c1 = bit_reverse(canonical_code(ci.lens, (int)s1), (int)l1);
+    pair[pi] = (c0 | (c1 << l0)) | ((l0 + l1) << 20);
   }
-  // Zero the padding of the sign/mantissa plane and the whole exponent area
-  // (coded words are OR-ed in).
+  // Zero the padding of the sign/mantissa plane and staging, and the
+  // exponent area (the boundary words of coded parts are OR-ed in).
   if (tid < 16 && nt + tid < sm_pad) {
     img[kTileHdr + nt + tid] = 0;
     exps[nt + tid] = 0;
@@ -199,48 +248,60 @@ __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a)
     *reinterpret_cast<uint4*>(img + exp_off + o) = make_uint4(0, 0, 0, 0);
   __syncthreads();
 
-  // Phase A: 16-B loads, split into sign/mantissa bytes (image) and exponent
-  // bytes (staging); sum the code lengths.
+  // Phase A: 16-B loads; sign/mantissa bytes to the image, exponent bytes to
+  // the staging area; sum the code lengths (pair table + 8 per escape).
   uint32_t bits = 0;
+  {
+    uint4 v[kRowsPerWarp];
 #pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    const uint32_t i0 = (warp * 16 + r) * kRow + lane * kLaneElems;
-    const uint32_t cnt = nt > i0 ? min(8u, nt - i0) : 0u;
-    uint32_t w[4];
-    if (cnt == 8 && vec) {
-      const uint4 v = ld_stream_v4(x + i0);
-      w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-    } else {
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const uint32_t i0 = (warp * kRowsPerWarp + r) * kRow + lane * kLaneElems;
+      const uint32_t cnt = nt > i0 ? min(8u, nt - i0) : 0u;
+      if (cnt == 8 && vec) {
+        v[r] = ld_stream_v4(x + i0);
+      } else {
+        uint32_t w[4];
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const uint32_t lo = (2 * p < (int)cnt) ? x[i0 + 2 * p] : 0u;
-        const uint32_t hi = (2 * p + 1 < (int)cnt) ? x[i0 + 2 * p + 1] : 0u;
-        w[p] = lo | (hi << 16);
+        for (int p = 0; p < 4; ++p) {
+          const uint32_t lo = (2 * p < (int)cnt) ? x[i0 + 2 * p] : 0u;
+          const uint32_t hi = (2 * p + 1 < (int)cnt) ? x[i0 + 2 * p + 1] : 0u;
+          w[p] = lo | (hi << 16);
+        }
+        v[r] = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
-    uint32_t e2[4], s2[4];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      e2[p] = (w[p] >> 7) & 0x00FF00FFu;
-      s2[p] = ((w[p] >> 8) & 0x00800080u) | (w[p] & 0x007F007Fu);
-    }
-    const uint32_t ex0 = __byte_perm(e2[0], e2[1], 0x6420), ex1 = __byte_perm(e2[2], e2[3], 0x6420);
-    const uint32_t sm0 = __byte_perm(s2[0], s2[1], 0x6420), sm1 = __byte_perm(s2[2], s2[3], 0x6420);
-    if (cnt == 8) {
-      *reinterpret_cast<uint2*>(img + kTileHdr + i0) = make_uint2(sm0, sm1);
-      *reinterpret_cast<uint2*>(exps + i0) = make_uint2(ex0, ex1);
-    } else {
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const uint32_t i0 = (warp * kRowsPerWarp + r) * kRow + lane * kLaneElems;
+      const uint32_t cnt = nt > i0 ? min(8u, nt - i0) : 0u;
+      const uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+      uint32_t e2[4], s2[4];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        if (t < (int)cnt) {
-          img[kTileHdr + i0 + t] = (uint8_t)((t < 4 ? sm0 : sm1) >> (8 * (t & 3)));
-          exps[i0 + t] = (uint8_t)((t < 4 ? ex0 : ex1) >> (8 * (t & 3)));
+      for (int p = 0; p < 4; ++p) {
+        e2[p] = (w[p] >> 7) & 0x00FF00FFu;
+        s2[p] = ((w[p] >> 8) & 0x00800080u) | (w[p] & 0x007F007Fu);
+      }
+      const uint32_t ex0 = __byte_perm(e2[0], e2[1], 0x6420), ex1 = __byte_perm(e2[2], e2[3], 0x6420);
+      const uint32_t sm0 = __byte_perm(s2[0], s2[1], 0x6420), sm1 = __byte_perm(s2[2], s2[3], 0x6420);
+      if (cnt == 8) {
+        *reinterpret_cast<uint2*>(img + kTileHdr + i0) = make_uint2(sm0, sm1);
+        *reinterpret_cast<uint2*>(exps + i0) = make_uint2(ex0, ex1);
+        uint32_t m0, m1;
+        const uint32_t t0 = pairs4(symbols4(ex0, base4, m0)), t1 = pairs4(symbols4(ex1, base4, m1));
+        bits += (pair[t0 & 0xFF] >> 20) + (pair[(t0 >> 16) & 0xFF] >> 20) + (pair[t1 & 0xFF] >> 20) +
+                (pair[(t1 >> 16) & 0xFF] >> 20) + __popc(m0) + __popc(m1);
+      } else if (cnt) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          if (t < (int)cnt) {
+            const uint32_t e = ((t < 4 ? ex0 : ex1) >> (8 * (t & 3))) & 0xFFu;
+            img[kTileHdr + i0 + t] = (uint8_t)((t < 4 ? sm0 : sm1) >> (8 * (t & 3)));
+            exps[i0 + t] = (uint8_t)e;
+            bits += tab[e] >> 24;
+          }
         }
       }
     }
-#pragma unroll
-    for (int t = 0; t < 8; ++t)
-      if (t < (int)cnt) bits += tab[((t < 4 ? ex0 : ex1) >> (8 * (t & 3))) & 0xFFu] >> 24;
   }
   part[warp * 32 + lane] = bits;
   __syncthreads();
@@ -251,7 +312,7 @@ __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a)
   if (warp == 0) {
     uint32_t off = 0;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
+    for (int w = 0; w < kEncWarps; ++w) {
       const uint32_t v = part[w * 32 + lane];
       part[w * 32 + lane] = off;
       off += v;
@@ -355,44 +416,57 @@ __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a)
   // Phase D: pack codewords into the exponent region (coded tiles); raw
   // tiles are stored straight from the staging area.
   if (s_mode == 0) {
-    uint32_t* sw = reinterpret_cast<uint32_t*>(img + exp_off + kSegTab) + s_wstart[lane];
     const uint32_t start = part[warp * 32 + lane];
-    uint32_t widx = start >> 5, nacc = start & 31;
-    uint64_t acc = 0;
-#pragma unroll 1
-    for (int r = 0; r < 16; ++r) {
-      const uint32_t i0 = (warp * 16 + r) * kRow + lane * kLaneElems;
+    BitSink sink;
+    sink.sw = reinterpret_cast<uint32_t*>(img + exp_off + kSegTab) + s_wstart[lane];
+    sink.acc = 0;
+    sink.widx = start >> 5;
+    sink.nacc = start & 31;
+    sink.first = true;
+#pragma unroll 2
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const uint32_t i0 = (warp * kRowsPerWarp + r) * kRow + lane * kLaneElems;
       const uint32_t cnt = nt > i0 ? min(8u, nt - i0) : 0u;
       if (cnt == 0) break;
       const uint2 e8 = *reinterpret_cast<const uint2*>(exps + i0);
+      uint32_t m0 = 0, m1 = 0, t0 = 0, t1 = 0;
+      if (cnt == 8) {
+        t0 = pairs4(symbols4(e8.x, base4, m0));
+        t1 = pairs4(symbols4(e8.y, base4, m1));
+      }
+      if (cnt == 8 && (m0 | m1) == 0) {
+        const uint32_t p0 = pair[t0 & 0xFF], p1 = pair[(t0 >> 16) & 0xFF];
+        const uint32_t p2 = pair[t1 & 0xFF], p3 = pair[(t1 >> 16) & 0xFF];
+        sink.put(p0 & 0xFFFFFu, p0 >> 20);
+        sink.put(p1 & 0xFFFFFu, p1 >> 20);
+        sink.put(p2 & 0xFFFFFu, p2 >> 20);
+        sink.put(p3 & 0xFFFFFu, p3 >> 20);
+      } else {
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        if (t < (int)cnt) {
-          const uint32_t en = tab[((t < 4 ? e8.x : e8.y) >> (8 * (t & 3))) & 0xFFu];
-          acc |= (uint64_t)(en & 0xFFFFFFu) << nacc;
-          nacc += en >> 24;
-          if (nacc >= 32) {
-            atomicOr(sw + widx, (uint32_t)acc);
-            ++widx;
-            acc >>= 32;
-            nacc -= 32;
+        for (int t = 0; t < 8; ++t) {
+          if (t < (int)cnt) {
+            const uint32_t en = tab[((t < 4 ? e8.x : e8.y) >> (8 * (t & 3))) & 0xFFu];
+            sink.put(en & 0xFFFFFFu, en >> 24);
           }
         }
       }
     }
-    if (nacc) atomicOr(sw + widx, (uint32_t)acc);
+    sink.finish();
   }
   fence_proxy_async_smem();
   __syncthreads();
 
   // Phase E: TMA bulk store of the finished tile: one copy for a coded tile,
-  // image head + staged exponents for a raw tile.
+  // image head + staged exponents for a raw tile.  The CTA leaves once shared
+  // memory has been read.
   if (tid == 0 && !s_err && s_size) {
     if (s_mode == 0) {
-      bulk_store_and_wait(a.out + s_goff, img, s_size);
+      bulk_store_issue(a.out + s_goff, img, s_size);
     } else {
-      bulk_store2_and_wait(a.out + s_goff, img, exp_off, a.out + s_goff + exp_off, exps, sm_pad);
+      bulk_store_issue(a.out + s_goff, img, exp_off);
+      bulk_store_issue(a.out + s_goff + exp_off, exps, sm_pad);
     }
+    bulk_commit_and_wait_read();
   }
 }
 

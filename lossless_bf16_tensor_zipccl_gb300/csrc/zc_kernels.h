@@ -51,7 +51,7 @@ struct DprepArgs {
   const uint64_t* offsets;
   DecChunk* chunks;
   uint32_t* item_start;  // n_chunks + 1
-  uint2* luts;           // n_chunks x 1024
+  uint32_t* luts;        // n_chunks x 1024
   WsHeader* hdr;
   uint32_t n_chunks;
   uint32_t max_items;
@@ -62,7 +62,7 @@ struct DecodeArgs {
   const uint8_t* stream;
   const DecChunk* chunks;
   const uint32_t* item_start;
-  const uint2* luts;
+  const uint32_t* luts;
   uint16_t* out;
   WsHeader* hdr;
   uint32_t n_chunks;
@@ -72,7 +72,7 @@ struct ReduceArgs {
   const uint8_t* peers[kMaxPeers];
   uint64_t bytes[kMaxPeers];
   DecChunk* chunks;  // one per peer
-  uint2* luts;       // k x 1024
+  uint32_t* luts;    // k x 1024
   WsHeader* hdr;
   uint16_t* out;
   uint64_t n;
