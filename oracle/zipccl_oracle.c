@@ -23,18 +23,19 @@
  * Stream format v1 (little-endian), as written by zo_compress:
  *   chunk  = header(32) | u32 tile_off[n_tiles] zero-padded to 16 | tiles
  *   header = u32 magic 0x4C43435A | u16 version 1 | u8 tile_log2 15 |
- *            u8 seg_log2 10 | u64 n_elems | u32 n_tiles | u8 base |
+ *            u8 seg_log2 9 | u64 n_elems | u32 n_tiles | u8 base |
  *            u8 flags 0 | i16 q | u8 lens[8] (symbol 2i low nibble, 2i+1 high)
  *   tile   = u32 mode (0 coded, 1 raw) | u32 n_t | u32 exp_bytes | u32 0 |
  *            s/m plane: n_t bytes, byte i = sign<<7 | mantissa, padded to 16 |
  *            exponent region padded to 16:
  *              raw:   n_t exponent bytes in element order
- *              coded: u16 seg_words[32] | 32 segments of u32 words
- *   element i of a tile belongs to segment ((i mod 256) / 8); a segment lists
+ *              coded: u16 seg_bits[64] | the 64 segment bitstreams back to
+ *                     back at bit granularity, zero-padded to a u32 word
+ *   element i of a tile belongs to segment ((i mod 512) / 8); a segment lists
  *   its elements in increasing i.  Symbol x = e - base for 0 <= x <= 14, else
  *   ESC (15) followed by the 8 raw bits of e.  Bits are packed LSB-first into
  *   little-endian u32 words; a canonical codeword is emitted MSB-first, i.e.
- *   stored bit-reversed.  Segments are zero-padded to a word.
+ *   stored bit-reversed.  Coded only when 128 + 4 ceil(bits / 32) < n_t.
  */
 #include <math.h>
 #include <stdint.h>
@@ -44,16 +45,16 @@
 #define ZO_MAGIC 0x4C43435Au
 #define ZO_VERSION 1
 #define ZO_TILE 32768u
-#define ZO_ROW 256u
+#define ZO_ROW 512u
 #define ZO_LANE_ELEMS 8u
-#define ZO_SEGS 32u
+#define ZO_SEGS 64u
 #define ZO_NSYM 16
 #define ZO_WINDOW 15
 #define ZO_ESC 15
 #define ZO_LMAX 10
 #define ZO_CHUNK_HDR 32u
 #define ZO_TILE_HDR 16u
-#define ZO_SEGTAB 64u
+#define ZO_SEGTAB 128u
 
 enum { ZO_OK = 0, ZO_ERR_INVALID_ARG = 1, ZO_ERR_CAPACITY = 2, ZO_ERR_CORRUPT = 3,
        ZO_ERR_VERSION = 4 };
@@ -384,12 +385,12 @@ uint64_t zo_max_compressed_bytes(const uint64_t *chunk_elems, uint32_t n_chunks)
 static uint64_t encode_tile(const uint16_t *x, uint64_t nt, int base, const int *lens,
                             const uint32_t *codes, uint8_t *out)
 {
-    uint64_t i, j, r0, t8, seg_bits_total = 0, exp_bytes, off;
-    uint32_t seg_words[ZO_SEGS];
+    uint64_t i, j, r0, t8, exp_bytes, off, nwords;
+    uint32_t seg_bits[ZO_SEGS];
     uint64_t sm_off = ZO_TILE_HDR, ex_off = ZO_TILE_HDR + pad16(nt);
-    uint32_t *words = (uint32_t *)calloc(ZO_TILE, sizeof(uint32_t)); /* >= worst case / 4 */
-    uint32_t *segbuf = (uint32_t *)calloc(ZO_TILE, sizeof(uint32_t));
-    uint64_t nwords = 0;
+    /* worst case 18 bits per value */
+    uint32_t *words = (uint32_t *)calloc((18 * ZO_TILE) / 32 + 2, sizeof(uint32_t));
+    zo_bitw bw;
     int mode;
 
     /* sign/mantissa plane */
@@ -398,13 +399,12 @@ static uint64_t encode_tile(const uint16_t *x, uint64_t nt, int base, const int 
     for (i = nt; i < pad16(nt); i++)
         out[sm_off + i] = 0;
 
-    /* exponent segments */
+    /* exponent segments, one after another in a single bitstream */
+    bw.words = words;
+    bw.nbits = 0;
     for (j = 0; j < ZO_SEGS; j++) {
-        zo_bitw bw;
-        uint64_t w;
-        bw.words = segbuf;
-        bw.nbits = 0;
-        /* segment j: positions row * 256 + 8 j + t, t = 0..7, in row order */
+        uint64_t start = bw.nbits;
+        /* segment j: positions row * 512 + 8 j + t, t = 0..7, in row order */
         for (r0 = 0; r0 < nt; r0 += ZO_ROW) {
           for (t8 = 0; t8 < ZO_LANE_ELEMS; t8++) {
             int e, sym, L, b;
@@ -421,20 +421,16 @@ static uint64_t encode_tile(const uint16_t *x, uint64_t nt, int base, const int 
                     bw_put(&bw, ((uint32_t)e >> b) & 1u);
           }
         }
-        seg_bits_total += bw.nbits;
-        seg_words[j] = (uint32_t)((bw.nbits + 31) / 32);
-        for (w = 0; w < seg_words[j]; w++)
-            words[nwords + w] = segbuf[w];
-        nwords += seg_words[j];
+        seg_bits[j] = (uint32_t)(bw.nbits - start);
     }
-    (void)seg_bits_total;
+    nwords = (bw.nbits + 31) / 32;
 
     /* coded only when strictly smaller than raw exponent bytes */
     mode = (ZO_SEGTAB + 4 * nwords < nt) ? 0 : 1;
     if (mode == 0) {
         exp_bytes = ZO_SEGTAB + 4 * nwords;
         for (j = 0; j < ZO_SEGS; j++)
-            put_u16(out + ex_off + 2 * j, seg_words[j]);
+            put_u16(out + ex_off + 2 * j, seg_bits[j]);
         for (i = 0; i < nwords; i++)
             put_u32(out + ex_off + ZO_SEGTAB + 4 * i, words[i]);
     } else {
@@ -449,7 +445,6 @@ static uint64_t encode_tile(const uint16_t *x, uint64_t nt, int base, const int 
     put_u32(out + 8, (uint32_t)exp_bytes);
     put_u32(out + 12, 0);
     free(words);
-    free(segbuf);
     return ex_off + pad16(exp_bytes);
 }
 
@@ -495,7 +490,7 @@ int zo_compress(const uint16_t *in, uint64_t n, const uint64_t *chunk_elems, uin
         put_u32(ch + 0, ZO_MAGIC);
         put_u16(ch + 4, ZO_VERSION);
         ch[6] = 15;
-        ch[7] = 10;
+        ch[7] = 9;
         put_u64(ch + 8, nc);
         put_u32(ch + 16, (uint32_t)T);
         ch[20] = (uint8_t)base;
@@ -586,7 +581,7 @@ static int decode_chunk(const uint8_t *ch, uint64_t chunk_bytes, uint16_t *out, 
     zo_decoder dec;
     if (chunk_bytes < ZO_CHUNK_HDR || get_u32(ch) != ZO_MAGIC)
         return ZO_ERR_CORRUPT;
-    if (get_u16(ch + 4) != ZO_VERSION || ch[6] != 15 || ch[7] != 10)
+    if (get_u16(ch + 4) != ZO_VERSION || ch[6] != 15 || ch[7] != 9)
         return ZO_ERR_VERSION;
     nc = get_u64(ch + 8);
     T = get_u32(ch + 16);
@@ -628,17 +623,17 @@ static int decode_chunk(const uint8_t *ch, uint64_t chunk_bytes, uint16_t *out, 
             for (k = 0; k < nt; k++)
                 y[k] |= (uint16_t)((uint32_t)tile[ex_off + k] << 7);
         } else if (mode == 0) {
-            uint64_t wsum = 0, wpos = 0;
+            uint64_t bsum = 0, bpos = 0;
             for (j = 0; j < ZO_SEGS; j++)
-                wsum += get_u16(tile + ex_off + 2 * j);
-            if (exp_bytes != ZO_SEGTAB + 4 * wsum)
+                bsum += get_u16(tile + ex_off + 2 * j);
+            if (exp_bytes != ZO_SEGTAB + 4 * ((bsum + 31) / 32))
                 return ZO_ERR_CORRUPT;
             for (j = 0; j < ZO_SEGS; j++) {
                 zo_bitr br;
-                uint64_t nw = get_u16(tile + ex_off + 2 * j);
-                br.bytes = tile + ex_off + ZO_SEGTAB + 4 * wpos;
-                br.nbits_total = 32 * nw;
-                br.pos = 0;
+                uint64_t nb = get_u16(tile + ex_off + 2 * j);
+                br.bytes = tile + ex_off + ZO_SEGTAB;
+                br.pos = bpos;
+                br.nbits_total = bpos + nb;
                 for (r0 = 0; r0 < nt; r0 += ZO_ROW)
                 for (t8 = 0; t8 < ZO_LANE_ELEMS; t8++) {
                     int sym;
@@ -663,7 +658,9 @@ static int decode_chunk(const uint8_t *ch, uint64_t chunk_bytes, uint16_t *out, 
                     }
                     y[k] |= (uint16_t)(e << 7);
                 }
-                wpos += nw;
+                if (br.pos != bpos + nb)
+                    return ZO_ERR_CORRUPT;
+                bpos += nb;
             }
         } else {
             return ZO_ERR_CORRUPT;

@@ -286,23 +286,19 @@ def test_size_identity_pr1():
     sym = e.astype(np.int64) - ch.base
     sym[(sym < 0) | (sym > 14)] = 15
     Lx = np.array(lens)[sym] + np.where(sym == 15, 8, 0)
-    total_payload = 0
     for t, tile in enumerate(ch.tiles):
         assert tile.mode == 0
-        seg = ((np.arange(tile.n) % 256) // 8)
+        seg = ((np.arange(tile.n) % zstream.ROW) // zstream.LANE)
         tl = Lx[t * 32768: t * 32768 + tile.n]
-        for j in range(32):
-            bits = int(tl[seg == j].sum())
-            assert tile.seg_bits_used[j] == bits
-            assert tile.seg_words[j] == (bits + 31) // 32
-            total_payload += bits
-    # total = payload (word-rounded per segment) + s/m plane + documented metadata
+        for j in range(zstream.SEGS):
+            # payload bits of a segment = sum of its code lengths + 8 per escape
+            assert tile.seg_bits[j] == int(tl[seg == j].sum())
+        assert tile.payload_words == (sum(tile.seg_bits) + 31) // 32
+    # total = s/m plane + payload words + documented metadata
     expect = 32 + zstream.pad16(4 * len(ch.tiles))
     for tile in ch.tiles:
-        expect += 16 + zstream.pad16(tile.n) + zstream.pad16(64 + 4 * sum(tile.seg_words))
+        expect += 16 + zstream.pad16(tile.n) + zstream.pad16(zstream.SEGTAB + 4 * tile.payload_words)
     assert len(s) == expect
-    word_bits = sum(32 * sum(t.seg_words) for t in ch.tiles)
-    assert 0 <= word_bits - total_payload < 32 * 32 * len(ch.tiles)
 
 
 def test_pr1_entropy_and_bits_per_value():

@@ -15,9 +15,10 @@ import numpy as np
 
 MAGIC = 0x4C43435A
 TILE = 32768
-ROW = 256
+ROW = 512
 LANE = 8
-SEGS = 32
+SEGS = 64
+SEGTAB = 2 * SEGS
 
 
 def pad16(x: int) -> int:
@@ -43,8 +44,8 @@ class Tile:
     exp_bytes: int
     offset: int
     size: int
-    seg_words: list[int] = field(default_factory=list)
-    seg_bits_used: list[int] = field(default_factory=list)
+    seg_bits: list[int] = field(default_factory=list)
+    payload_words: int = 0
     escapes: int = 0
 
 
@@ -66,7 +67,7 @@ def _bits_lsb_first(words: bytes) -> str:
 
 def parse_chunk(buf: bytes) -> Chunk:
     magic, version, tile_log2, seg_log2, n, n_tiles, base, flags, q = struct.unpack_from("<IHBBQIBBh", buf, 0)
-    assert magic == MAGIC and version == 1 and tile_log2 == 15 and seg_log2 == 10 and flags == 0
+    assert magic == MAGIC and version == 1 and tile_log2 == 15 and seg_log2 == 9 and flags == 0
     lens = []
     for i in range(8):
         b = buf[24 + i]
@@ -93,15 +94,17 @@ def parse_chunk(buf: bytes) -> Chunk:
             assert exp_bytes == nt
             e = np.frombuffer(buf, dtype=np.uint8, count=nt, offset=ex).astype(np.uint16)
         else:
-            segw = list(struct.unpack_from("<32H", buf, ex))
-            assert exp_bytes == 64 + 4 * sum(segw)
-            tile.seg_words = segw
+            segb = list(struct.unpack_from(f"<{SEGS}H", buf, ex))
+            total = sum(segb)
+            nwords = (total + 31) // 32
+            assert exp_bytes == SEGTAB + 4 * nwords
+            tile.seg_bits = segb
+            tile.payload_words = nwords
             e = np.zeros(nt, dtype=np.uint16)
-            wpos = ex + 64
+            bits = _bits_lsb_first(buf[ex + SEGTAB: ex + SEGTAB + 4 * nwords])
+            k = 0
             for j in range(SEGS):
-                bits = _bits_lsb_first(buf[wpos: wpos + 4 * segw[j]])
-                wpos += 4 * segw[j]
-                k = 0
+                end = k + segb[j]
                 idx = [r + LANE * j + t8 for r in range(0, nt, ROW) for t8 in range(LANE) if r + LANE * j + t8 < nt]
                 for i in idx:
                     cw = ""
@@ -115,9 +118,9 @@ def parse_chunk(buf: bytes) -> Chunk:
                         tile.escapes += 1
                     else:
                         e[i] = base + s
-                assert set(bits[k:]) <= {"0"}, "segment padding must be zero bits"
-                assert (len(bits) - k) < 32
-                tile.seg_bits_used.append(k)
+                assert k == end, "segment bit length must match its symbols"
+            assert set(bits[k:]) <= {"0"}, "payload padding must be zero bits"
+            assert len(bits) - k < 32
         assert all(v == 0 for v in buf[ex + exp_bytes: ex + pad16(exp_bytes)])
         out[t * TILE: t * TILE + nt] = vals | (e << 7)
         tiles.append(tile)
