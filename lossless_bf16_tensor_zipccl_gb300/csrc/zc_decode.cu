@@ -7,15 +7,16 @@
 //     every byte restored;
 //   - Fig. 3 / Fig. 5 captions: zipcclReduceScatter receives the peers'
 //     compressed chunks, then decompresses and reduces them ->
-//     zc_reduce_kernel decodes the same tile of k peer chunks and sums in fp32
-//     in rank order, with no bf16 round trip through global memory.
+//     zc_reduce_kernel decodes the same half tile of k peer chunks and sums in
+//     fp32 in rank order, with no bf16 round trip through global memory.
 //
 // Decoding is table-driven: one 1024-entry table per chunk (built from the
 // code lengths in the chunk header) returns up to five symbols per lookup.
-// Each lane of a warp decodes one segment; the 32 segments of a tile are
-// interleaved 8 elements at a time, so a warp's loads of sign/mantissa bytes
-// and stores of BF16 words stay coalesced while each lane runs its own
-// bitstream.
+// A tile's 64 segments are decoded by two warps, one lane per segment; the
+// segments interleave 8 values at a time along each 512-value row, so a
+// warp's stores of BF16 words stay coalesced while every lane runs its own
+// bitstream.  The exponent bitstream and the sign/mantissa bytes arrive in
+// shared memory by TMA bulk copies.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,10 +27,6 @@ namespace zc {
 
 __device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 __device__ __forceinline__ uint64_t ld_u64(const uint8_t* p) { return *reinterpret_cast<const uint64_t*>(p); }
-
-__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
 // Header checks shared by both prep kernels; returns 0 or a status code.
 struct HeaderInfo {
@@ -53,18 +50,21 @@ __device__ uint32_t check_header(const uint8_t* ch, uint64_t bytes, HeaderInfo& 
   return 0;
 }
 
-// Location of tile k of a chunk, validated against the chunk's extent.
+// Tile k of a chunk, validated against the chunk's extent, as seen by the
+// warp decoding half `half` (segments 32 half .. 32 half + 31).
 struct TileView {
   const uint8_t* tile;
   uint32_t mode, exp_off, exp_bytes;
-  uint32_t wstart, words;  // this lane's segment (coded tiles)
+  uint32_t start;           // this lane's segment: first bit in the payload (coded tiles)
+  uint32_t hbit0, hbit1;    // bit range of this half's segments in the payload
+  uint32_t bits;            // payload bits of the whole tile
 };
 
 __device__ bool open_tile(const uint8_t* ch, uint64_t bytes, uint32_t n_tiles, uint32_t k, uint32_t nt,
-                          uint32_t lane, TileView& tv) {
+                          uint32_t half, uint32_t lane, TileView& tv) {
   tv.tile = ch;
   tv.mode = 1;
-  tv.exp_off = tv.exp_bytes = tv.wstart = tv.words = 0;
+  tv.exp_off = tv.exp_bytes = tv.start = tv.hbit0 = tv.hbit1 = tv.bits = 0;
   const uint64_t toff = ld_u32(ch + kChunkHdr + 4ull * k);
   if ((toff & 15) || toff < chunk_hdr_bytes(n_tiles) || toff + kTileHdr > bytes) return false;
   const uint8_t* t = ch + toff;
@@ -74,19 +74,25 @@ __device__ bool open_tile(const uint8_t* ch, uint64_t bytes, uint32_t n_tiles, u
   tv.exp_bytes = h.z;
   tv.exp_off = kTileHdr + (uint32_t)pad16(nt);
   if (h.y != nt || h.x > 1 || toff + tv.exp_off + pad16(h.z) > bytes) return false;
-  tv.wstart = tv.words = 0;
   if (tv.mode == 1) return h.z == nt;
   if (h.z < kSegTab || ((h.z - kSegTab) & 3)) return false;
-  const uint32_t w = reinterpret_cast<const uint16_t*>(t + tv.exp_off)[lane];
-  uint32_t incl = w;
+  const uint16_t* segbits = reinterpret_cast<const uint16_t*>(t + tv.exp_off);
+  const uint32_t b0 = segbits[lane], b1 = segbits[32 + lane];
+  uint32_t i0 = b0, i1 = b1;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= (uint32_t)o) incl += y;
+    const uint32_t y0 = __shfl_up_sync(kFull, i0, o), y1 = __shfl_up_sync(kFull, i1, o);
+    if (lane >= (uint32_t)o) {
+      i0 += y0;
+      i1 += y1;
+    }
   }
-  tv.wstart = incl - w;
-  tv.words = w;
-  return __shfl_sync(kFull, incl, 31) == (h.z - kSegTab) / 4;
+  const uint32_t t0 = __shfl_sync(kFull, i0, 31), t1 = __shfl_sync(kFull, i1, 31);
+  tv.start = half == 0 ? i0 - b0 : t0 + i1 - b1;
+  tv.hbit0 = half == 0 ? 0u : t0;
+  tv.hbit1 = half == 0 ? t0 : t0 + t1;
+  tv.bits = t0 + t1;
+  return (t0 + t1 + 31) / 32 == (h.z - kSegTab) / 4;
 }
 
 __device__ __forceinline__ uint2 load_bytes8(const uint8_t* p, uint32_t cnt) {
@@ -103,36 +109,40 @@ __device__ __forceinline__ uint2 load_bytes8(const uint8_t* p, uint32_t cnt) {
   return make_uint2(lo, hi);
 }
 
-constexpr uint32_t kSmBlkRows = 8;                    // rows per staged sign/mantissa block
-constexpr uint32_t kSmBlkBytes = kSmBlkRows * kRow;    // 2 KB
+constexpr uint32_t kSmBlkRows = 4;                     // rows per staged sign/mantissa block
+constexpr uint32_t kSmBlkBytes = kSmBlkRows * kHalf;   // one warp's half rows: 1 KB
 
-// Decode one 8-element lane group of row r into 4 words (8 BF16).
+// A copy of payload bytes [lo, lo + bytes) staged in shared memory (or the
+// payload in place in global memory when lo == 0 and `global` is set).
+struct ExpSource {
+  const uint32_t* words;  // word holding payload bit 8 * lo
+  uint32_t bit_base;      // 8 * lo
+  const uint32_t* end;    // one past the last readable word
+};
+
+// Decode one warp's 8-value lane group of row r into 4 words (8 BF16).
 struct RowSource {
   TileView tv;
   LaneDecoder dec;
-  uint32_t nt, lane;
+  uint32_t nt, col;  // col: first value of this lane in a row
 
-  // exp: the tile's exponent region, staged in shared memory or in place in
-  // global memory.
-  __device__ __forceinline__ void start(const uint32_t* lut, uint32_t base, const uint8_t* exp) {
-    if (tv.mode == 0)
-      dec.init(reinterpret_cast<const uint32_t*>(exp + kSegTab) + tv.wstart, tv.words, lut, base);
+  __device__ __forceinline__ void start(const uint32_t* lut, uint32_t base, const ExpSource& xs) {
+    if (tv.mode == 0) dec.init(xs.words, tv.start - xs.bit_base, xs.end, lut, base);
   }
 
   __device__ __forceinline__ uint32_t count(uint32_t r) const {
-    const uint32_t i0 = r * kRow + lane * kLaneElems;
+    const uint32_t i0 = r * kRow + col;
     return nt > i0 ? min(8u, nt - i0) : 0u;
   }
 
   __device__ __forceinline__ uint4 row(uint32_t r, uint2 sm) {
-    const uint32_t i0 = r * kRow + lane * kLaneElems;
     const uint32_t cnt = count(r);
     uint32_t lo = 0, hi = 0;
     if (tv.mode == 0) {
-      dec.fill(cnt);
+      dec.fill_warp(cnt);
       dec.take8(lo, hi);
     } else {
-      const uint2 e = load_bytes8(tv.tile + tv.exp_off + i0, cnt);
+      const uint2 e = load_bytes8(tv.tile + tv.exp_off + r * kRow + col, cnt);
       lo = e.x;
       hi = e.y;
     }
@@ -143,7 +153,7 @@ struct RowSource {
   // sign/mantissa bytes of row r from its staged block (shared memory)
   __device__ __forceinline__ uint2 sm_staged(const uint8_t* blk, uint32_t r) const {
     const uint32_t cnt = count(r);
-    const uint8_t* p = blk + (r % kSmBlkRows) * kRow + lane * kLaneElems;
+    const uint8_t* p = blk + (r % kSmBlkRows) * kHalf + (col % kHalf);
     if (cnt == 8) return *reinterpret_cast<const uint2*>(p);
     uint32_t lo = 0, hi = 0;
 #pragma unroll
@@ -158,20 +168,32 @@ struct RowSource {
   }
 };
 
-// Double-buffered TMA staging of a tile's sign/mantissa plane, kSmBlkRows
-// rows (2 KB) per block, one warp.  Block b lives in stage b & 1; its barrier
-// completes phase b >> 1.
+// Double-buffered TMA staging of one warp's half of the sign/mantissa plane,
+// kSmBlkRows rows per block (one bulk copy per row piece).  Block b lives in
+// stage b & 1; its barrier completes phase b >> 1.
 struct SmStager {
   uint8_t* buf;       // 2 x kSmBlkBytes, 16-B aligned
   uint64_t* bars;     // 2 barriers
   const uint8_t* g;   // the plane in global memory (tile + 16)
   uint32_t plane;     // padded plane bytes (multiple of 16)
+  uint32_t half_off;  // 0 or kHalf
   uint32_t nblk;
 
-  __device__ __forceinline__ void issue(uint32_t b) {
-    const uint32_t off = b * kSmBlkBytes;
-    const uint32_t bytes = min(kSmBlkBytes, plane - off);
-    bulk_load_async(buf + (b & 1) * kSmBlkBytes, g + off, bytes, bars + (b & 1));
+  __device__ __forceinline__ uint32_t piece(uint32_t r) const {
+    const uint32_t off = r * kRow + half_off;
+    return off < plane ? min(kHalf, plane - off) : 0u;
+  }
+  __device__ __forceinline__ void issue(uint32_t b) {  // lane 0
+    uint32_t tx = 0;
+#pragma unroll
+    for (uint32_t j = 0; j < kSmBlkRows; ++j) tx += piece(b * kSmBlkRows + j);
+    mbar_arrive_expect_tx(bars + (b & 1), tx);
+    uint8_t* dst = buf + (b & 1) * kSmBlkBytes;
+#pragma unroll
+    for (uint32_t j = 0; j < kSmBlkRows; ++j) {
+      const uint32_t r = b * kSmBlkRows + j, sz = piece(r);
+      if (sz) bulk_copy_g2s(dst + j * kHalf, g + r * kRow + half_off, sz, bars + (b & 1));
+    }
   }
   __device__ __forceinline__ void start(uint32_t lane) {
     if (lane == 0) {
@@ -193,35 +215,30 @@ struct SmStager {
     __syncwarp();
     if (lane == 0 && b + 2 < nblk) issue(b + 2);
   }
+  // Before leaving early: wait (bounded) for the copies of blocks b and b + 1,
+  // the ones that may still be in flight when block b was not acquired.
+  __device__ __forceinline__ void drain(uint32_t b) {
+    for (uint32_t j = b; j < nblk && j < b + 2; ++j) (void)mbar_wait(bars + (j & 1), (j >> 1) & 1);
+  }
 };
 
-// Stage a coded tile's exponent region in shared memory with one TMA bulk
-// load when it fits `slot` bytes (lane 0 issues, every lane waits).  Returns
-// the region to decode from (shared or global) and sets `timeout` when the
-// bounded wait gave up (warp-uniform).
-__device__ __forceinline__ const uint8_t* stage_exponents(const TileView& tv, uint8_t* slot, uint32_t slot_bytes,
-                                                         uint64_t* bar, uint32_t lane, bool& timeout) {
-  timeout = false;
-  const uint8_t* g = tv.tile + tv.exp_off;
-  const uint32_t bytes = (uint32_t)pad16(tv.exp_bytes);
-  if (tv.mode != 0 || bytes > slot_bytes) return g;
-  if (lane == 0) {
-    mbar_init(bar, 1);
-    bulk_load_async(slot, g, bytes, bar);
-  }
-  __syncwarp();
-  const bool ok = mbar_wait(bar, 0);
-  timeout = __any_sync(kFull, !ok);
-  return slot;
+// Bytes of the payload to stage for payload bits [bit0, bit1): from the
+// 16-byte boundary below bit0 up to the words the decoders may read, within
+// the exponent region; 0 when that does not fit `slot`.
+__device__ __forceinline__ uint32_t stage_span(const TileView& tv, uint32_t bit0, uint32_t bit1, uint32_t slot,
+                                               uint32_t& lo) {
+  const uint32_t pay = (uint32_t)pad16(tv.exp_bytes) - kSegTab;  // payload bytes readable in the region
+  lo = (bit0 >> 7) << 4;
+  const uint32_t hi = min(pay, (uint32_t)pad16(((bit1 + 31) >> 5) * 4 + 12));
+  const uint32_t bytes = hi > lo ? hi - lo : 0u;
+  return bytes <= slot ? bytes : 0u;
 }
 
-// Copy one chunk's 4-KB decode table into shared memory (one warp).
-__device__ __forceinline__ void load_lut_warp(uint32_t* dst, const uint32_t* src, uint32_t lane) {
+// Copy one chunk's 4-KB decode table into shared memory (nthreads threads).
+__device__ __forceinline__ void load_lut(uint32_t* dst, const uint32_t* src, uint32_t tid, uint32_t nthreads) {
   const uint4* g = reinterpret_cast<const uint4*>(src);
   uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (uint32_t i = lane; i < kLutEntries / 4; i += 32) d[i] = __ldg(g + i);
-  __syncwarp();
+  for (uint32_t i = tid; i < kLutEntries / 4; i += nthreads) d[i] = __ldg(g + i);
 }
 
 __device__ __forceinline__ void store_row(uint16_t* y, uint32_t cnt, bool vec, uint4 v) {
@@ -325,20 +342,22 @@ __global__ void __launch_bounds__(256) zc_dprep_kernel(DprepArgs a) {
   }
 }
 
-// One warp (one CTA) per tile.
-constexpr uint32_t kExpSlot = 12288;  // staged exponent region; larger regions are read in place
-__global__ void __launch_bounds__(32) zc_decode_kernel(DecodeArgs a) {
+// One CTA per tile: warp h decodes the tile's half h (segments 32h..32h+31).
+constexpr uint32_t kExpSlot = 12288;  // staged payload; larger ones are read in place
+
+__global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
   __shared__ __align__(128) uint8_t s_exp[kExpSlot];
-  __shared__ __align__(128) uint8_t s_sm[2 * kSmBlkBytes];
+  __shared__ __align__(128) uint8_t s_sm[2][2 * kSmBlkBytes];
   __shared__ __align__(16) uint32_t s_lut[kLutEntries];
-  __shared__ __align__(8) uint64_t s_bar[3];
-  const uint32_t lane = threadIdx.x;
+  __shared__ __align__(8) uint64_t s_bar[2][2];
+  __shared__ __align__(8) uint64_t s_xbar;
+  __shared__ uint32_t s_flag[3];
+  const uint32_t tid = threadIdx.x, lane = tid & 31, half = tid >> 5;
   const uint32_t item = blockIdx.x;
-  // lane 0 reads the status once and the warp follows it together
-  uint32_t bad = lane == 0 ? *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) : 0u;
-  bad = __shfl_sync(kFull, bad, 0);
-  if (bad) return;
-  if (item >= a.hdr->total_items) return;
+  // one read of the status word per block, so both warps take the same path
+  if (tid == 0) s_flag[0] = *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0 || item >= a.hdr->total_items;
+  __syncthreads();
+  if (s_flag[0]) return;
   uint32_t lo = 0, hi = a.n_chunks;  // largest c with item_start[c] <= item
   while (hi - lo > 1) {
     const uint32_t mid = (lo + hi) >> 1;
@@ -348,49 +367,98 @@ __global__ void __launch_bounds__(32) zc_decode_kernel(DecodeArgs a) {
   const uint32_t c = lo;
   const DecChunk d = a.chunks[c];
   const uint32_t k = item - a.item_start[c];
-  if (!d.ok || k >= d.n_tiles) {
-    if (lane == 0) set_status(a.hdr, kStCorrupt);
-    return;
-  }
-  const uint32_t nt = (uint32_t)min((uint64_t)kTile, d.n - (uint64_t)k * kTile);
+  const bool chunk_ok = d.ok && k < d.n_tiles;
+  const uint32_t nt = chunk_ok ? (uint32_t)min((uint64_t)kTile, d.n - (uint64_t)k * kTile) : 0u;
   const uint8_t* ch = a.stream + d.stream_off;
   RowSource src;
   src.nt = nt;
-  src.lane = lane;
-  if (!open_tile(ch, d.bytes, d.n_tiles, k, nt, lane, src.tv)) {
-    if (lane == 0) set_status(a.hdr, kStCorrupt);
+  src.col = half * kHalf + lane * kLaneElems;
+  const bool ok = chunk_ok && open_tile(ch, d.bytes, d.n_tiles, k, nt, half, lane, src.tv);
+  if (lane == 0) s_flag[1 + half] = ok ? 0u : 1u;
+  load_lut(s_lut, a.luts + (size_t)(chunk_ok ? c : 0) * kLutEntries, tid, 64);
+  __syncthreads();
+  if (s_flag[1] | s_flag[2]) {
+    if (tid == 0) set_status(a.hdr, kStCorrupt);
     return;
   }
+  // The whole coded payload comes into shared memory with one TMA copy.
+  const uint8_t* payload = src.tv.tile + src.tv.exp_off + kSegTab;
+  uint32_t slo = 0;
+  const uint32_t sbytes = src.tv.mode == 0 ? stage_span(src.tv, 0, src.tv.bits, kExpSlot, slo) : 0u;
+  if (tid == 0 && sbytes) {
+    mbar_init(&s_xbar, 1);
+    mbar_arrive_expect_tx(&s_xbar, sbytes);
+    bulk_copy_g2s(s_exp, payload, sbytes, &s_xbar);
+  }
   SmStager stg;
-  stg.buf = s_sm;
-  stg.bars = s_bar + 1;
+  stg.buf = s_sm[half];
+  stg.bars = s_bar[half];
   stg.g = src.tv.tile + kTileHdr;
   stg.plane = (uint32_t)pad16(nt);
-  stg.nblk = (nt + kSmBlkBytes - 1) / kSmBlkBytes;
-  stg.start(lane);
-  bool timeout;
-  const uint8_t* exp = stage_exponents(src.tv, s_exp, kExpSlot, s_bar, lane, timeout);
-  load_lut_warp(s_lut, a.luts + (size_t)c * kLutEntries, lane);
-  src.start(s_lut, d.base, exp);
-  const uint64_t e0 = d.elem_start + (uint64_t)k * kTile;
-  uint16_t* y = a.out + e0;
-  const bool vec = (e0 & 7) == 0;
+  stg.half_off = half * kHalf;
   const uint32_t rows = (nt + kRow - 1) / kRow;
-  for (uint32_t b = 0; b < stg.nblk && !timeout; ++b) {
-    if (!stg.acquire(b)) {
-      timeout = true;
-      break;
-    }
-    const uint8_t* blk = stg.block(b);
-    const uint32_t rend = min(rows, (b + 1) * kSmBlkRows);
-    for (uint32_t r = b * kSmBlkRows; r < rend; ++r) {
-      const uint32_t cnt = src.count(r);
-      const uint4 v = src.row(r, src.sm_staged(blk, r));
-      if (cnt) store_row(y + r * kRow + lane * kLaneElems, cnt, vec, v);
-    }
-    stg.release(b, lane);
+  stg.nblk = (rows + kSmBlkRows - 1) / kSmBlkRows;
+  stg.start(lane);
+  __syncthreads();  // the payload barrier is initialised
+  bool timeout = sbytes && !mbar_wait(&s_xbar, 0);
+  timeout = __any_sync(kFull, timeout);
+  ExpSource xs;
+  if (sbytes) {
+    xs.words = reinterpret_cast<const uint32_t*>(s_exp);
+    xs.bit_base = 0;
+    xs.end = reinterpret_cast<const uint32_t*>(s_exp + sbytes);
+  } else {
+    xs.words = reinterpret_cast<const uint32_t*>(payload);
+    xs.bit_base = 0;
+    xs.end = reinterpret_cast<const uint32_t*>(src.tv.tile + src.tv.exp_off + pad16(src.tv.exp_bytes));
   }
-  if (timeout && lane == 0) set_status(a.hdr, kStTimeout);
+  src.start(s_lut, d.base, xs);
+  const uint64_t e0 = d.elem_start + (uint64_t)k * kTile;
+  uint16_t* y = a.out + e0 + src.col;
+  const bool vec = (e0 & 7) == 0;
+  uint32_t b = 0;  // first block not yet acquired
+  if (timeout) {
+    // skip the rows; the status tells the caller
+  } else if (nt == kTile && vec && src.tv.mode == 0) {
+    // full coded tile: every lane has 8 values in every row
+    for (; b < stg.nblk; ++b) {
+      if (!stg.acquire(b)) {
+        timeout = true;
+        break;
+      }
+      const uint8_t* blk = stg.block(b) + lane * kLaneElems;
+      uint16_t* yb = y + b * kSmBlkRows * kRow;
+#pragma unroll
+      for (uint32_t j = 0; j < kSmBlkRows; ++j) {
+        const uint2 sm = *reinterpret_cast<const uint2*>(blk + j * kHalf);
+        uint32_t elo, ehi;
+        src.dec.fill_warp(8);
+        src.dec.take8(elo, ehi);
+        const uint2 u = merge4(elo, sm.x), v = merge4(ehi, sm.y);
+        *reinterpret_cast<uint4*>(yb + j * kRow) = make_uint4(u.x, u.y, v.x, v.y);
+      }
+      stg.release(b, lane);
+    }
+  } else {
+    for (; b < stg.nblk; ++b) {
+      if (!stg.acquire(b)) {
+        timeout = true;
+        break;
+      }
+      const uint8_t* blk = stg.block(b);
+      const uint32_t rend = min(rows, (b + 1) * kSmBlkRows);
+      for (uint32_t r = b * kSmBlkRows; r < rend; ++r) {
+        const uint32_t cnt = src.count(r);
+        const uint4 v = src.row(r, src.sm_staged(blk, r));
+        if (cnt) store_row(y + r * kRow, cnt, vec, v);
+      }
+      stg.release(b, lane);
+    }
+  }
+  if (timeout) {
+    stg.drain(b);
+    if (lane == 0) set_status(a.hdr, kStTimeout);
+  }
 }
 
 // ---------------------------------------------------------------- reduce
@@ -431,30 +499,29 @@ __device__ __forceinline__ void add_bf16x2(float& a0, float& a1, uint32_t w) {
   a1 = __fadd_rn(a1, __uint_as_float(w & 0xFFFF0000u));
 }
 
-// One block per tile, one warp per peer.  Each warp stages its peer's
-// exponent region and decode table in shared memory, then rows are decoded 8
-// at a time into shared memory (peer-major) and every thread folds 8 values
-// across the peers in rank order.
+// One block per half tile, one warp per peer.  Each warp stages its peer's
+// decode table, the payload bits of its half and the sign/mantissa blocks in
+// shared memory, decodes kRedRows half rows at a time into shared memory
+// (peer-major), then every thread folds 8 values across the peers in rank
+// order.
 constexpr uint32_t kRedRows = kSmBlkRows;
-constexpr uint32_t kRedStageBytes = kRedRows * kRow * 2;  // decoded BF16 rows per peer
-constexpr uint32_t kRedMaxStagedPeers = 9;                 // exponent slots fit in shared memory up to here
+constexpr uint32_t kRedStageBytes = kRedRows * kHalf * 2;  // decoded BF16 half rows per peer
+constexpr uint32_t kRedSlot = 6144;                        // staged half payload per peer
 
 __host__ __device__ constexpr size_t reduce_smem_bytes(uint32_t k) {
-  return (size_t)k * (kRedStageBytes + 2 * kSmBlkBytes + kLutEntries * 4 +
-                      (k <= kRedMaxStagedPeers ? kExpSlot : 0) + 32);
+  return (size_t)k * (kRedStageBytes + 2 * kSmBlkBytes + kLutEntries * 4 + kRedSlot + 32);
 }
 
 __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
   extern __shared__ __align__(128) uint8_t rsm[];
   const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5, tid = threadIdx.x;
-  const uint32_t t = blockIdx.x;
+  const uint32_t t = blockIdx.x >> 1, half = blockIdx.x & 1;
   const uint32_t nthreads = 32 * a.k;
-  const bool staged = a.k <= kRedMaxStagedPeers;
-  uint16_t* sbuf = reinterpret_cast<uint16_t*>(rsm);                           // k x kRedRows x kRow values
-  uint8_t* smst = rsm + (size_t)a.k * kRedStageBytes;                         // k x 2 staged s/m blocks
+  uint16_t* sbuf = reinterpret_cast<uint16_t*>(rsm);                                   // k x kRedRows half rows
+  uint8_t* smst = rsm + (size_t)a.k * kRedStageBytes;                                 // k x 2 s/m blocks
   uint32_t* luts = reinterpret_cast<uint32_t*>(smst + (size_t)a.k * 2 * kSmBlkBytes);  // k x 1024
-  uint8_t* slots = reinterpret_cast<uint8_t*>(luts + (size_t)a.k * kLutEntries);       // k x kExpSlot
-  uint64_t* bars = reinterpret_cast<uint64_t*>(slots + (staged ? (size_t)a.k * kExpSlot : 0));  // k x 3
+  uint8_t* slots = reinterpret_cast<uint8_t*>(luts + (size_t)a.k * kLutEntries);       // k x kRedSlot
+  uint64_t* bars = reinterpret_cast<uint64_t*>(slots + (size_t)a.k * kRedSlot);       // k x 3
   __shared__ int s_bad;
   // one read of the status word per block, so every thread takes the same path
   if (tid == 0) s_bad = *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0;
@@ -464,42 +531,71 @@ __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
   const DecChunk d = a.chunks[p];
   RowSource src;
   src.nt = nt;
-  src.lane = lane;
-  const bool ok = d.ok && open_tile(a.peers[p], d.bytes, d.n_tiles, t, nt, lane, src.tv);
-  bool timeout = false;
-  const uint8_t* exp = src.tv.tile;
+  src.col = half * kHalf + lane * kLaneElems;
+  const bool ok = d.ok && open_tile(a.peers[p], d.bytes, d.n_tiles, t, nt, half, lane, src.tv);
   SmStager stg;
   stg.buf = smst + (size_t)p * 2 * kSmBlkBytes;
-  stg.bars = bars + 3 * p + 1;
+  stg.bars = bars + 3 * p;
   stg.g = src.tv.tile + kTileHdr;
   stg.plane = (uint32_t)pad16(nt);
-  stg.nblk = (nt + kSmBlkBytes - 1) / kSmBlkBytes;
+  stg.half_off = half * kHalf;
+  const uint32_t rows = (nt + kRow - 1) / kRow;
+  stg.nblk = (rows + kSmBlkRows - 1) / kSmBlkRows;
+  const uint8_t* payload = src.tv.tile + src.tv.exp_off + kSegTab;
+  uint8_t* slot = slots + (size_t)p * kRedSlot;
+  uint32_t slo = 0, sbytes = 0;
+  bool timeout = false;
   if (ok) {
+    if (src.tv.mode == 0) sbytes = stage_span(src.tv, src.tv.hbit0, src.tv.hbit1, kRedSlot, slo);
+    if (lane == 0 && sbytes) {
+      mbar_init(bars + 3 * p + 2, 1);
+      mbar_arrive_expect_tx(bars + 3 * p + 2, sbytes);
+      bulk_copy_g2s(slot, payload + slo, sbytes, bars + 3 * p + 2);
+    }
     stg.start(lane);
-    exp = stage_exponents(src.tv, slots + (size_t)p * kExpSlot, staged ? kExpSlot : 0u, bars + 3 * p, lane, timeout);
-    load_lut_warp(luts + (size_t)p * kLutEntries, a.luts + (size_t)p * kLutEntries, lane);
+    load_lut(luts + (size_t)p * kLutEntries, a.luts + (size_t)p * kLutEntries, lane, 32);
+    __syncwarp();
+    timeout = sbytes && !mbar_wait(bars + 3 * p + 2, 0);
+    timeout = __any_sync(kFull, timeout);
   }
   if (lane == 0 && (!ok || timeout)) {
     s_bad = 1;
     set_status(a.hdr, ok ? kStTimeout : kStCorrupt);
   }
   __syncthreads();
-  if (s_bad) return;  // uniform
-  src.start(luts + (size_t)p * kLutEntries, d.base, exp);
-  uint16_t* mine = sbuf + (size_t)p * kRedRows * kRow;
-  const uint32_t rows = (nt + kRow - 1) / kRow;
+  if (s_bad) {  // uniform
+    if (ok) stg.drain(0);
+    return;
+  }
+  ExpSource xs;
+  if (sbytes) {
+    xs.words = reinterpret_cast<const uint32_t*>(slot);
+    xs.bit_base = 8 * slo;
+    xs.end = reinterpret_cast<const uint32_t*>(slot + sbytes);
+  } else {
+    xs.words = reinterpret_cast<const uint32_t*>(payload);
+    xs.bit_base = 0;
+    xs.end = reinterpret_cast<const uint32_t*>(src.tv.tile + src.tv.exp_off + pad16(src.tv.exp_bytes));
+  }
+  src.start(luts + (size_t)p * kLutEntries, d.base, xs);
+  uint16_t* mine = sbuf + (size_t)p * kRedRows * kHalf;
   uint16_t* y = a.out + (uint64_t)t * kTile;
   bool late = false;  // a bounded wait gave up: finish the loop, report it
+  uint32_t late_b = 0;
   for (uint32_t b = 0; b < stg.nblk; ++b) {
-    if (!late && !stg.acquire(b)) late = true;
+    if (!late && !stg.acquire(b)) {
+      late = true;
+      late_b = b;
+    }
     const uint8_t* blk = stg.block(b);
     const uint32_t r0 = b * kRedRows, rend = min(rows, r0 + kRedRows);
     for (uint32_t r = r0; r < rend; ++r)
-      *reinterpret_cast<uint4*>(mine + (r - r0) * kRow + lane * kLaneElems) = src.row(r, src.sm_staged(blk, r));
+      *reinterpret_cast<uint4*>(mine + (r - r0) * kHalf + lane * kLaneElems) = src.row(r, src.sm_staged(blk, r));
     if (!late) stg.release(b, lane);
     __syncthreads();
-    const uint32_t m = min(kRedRows * kRow, nt - r0 * kRow);
-    for (uint32_t e = tid * 8; e < m; e += nthreads * 8) {
+    for (uint32_t e = tid * 8; e < kRedRows * kHalf; e += nthreads * 8) {
+      const uint32_t gi = (r0 + e / kHalf) * kRow + half * kHalf + (e % kHalf);
+      if (gi >= nt) continue;
       float acc[8];
       {
         const uint4 v = *reinterpret_cast<const uint4*>(sbuf + e);
@@ -511,7 +607,7 @@ __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
         }
       }
       for (uint32_t pp = 1; pp < a.k; ++pp) {
-        const uint4 v = *reinterpret_cast<const uint4*>(sbuf + (size_t)pp * kRedRows * kRow + e);
+        const uint4 v = *reinterpret_cast<const uint4*>(sbuf + (size_t)pp * kRedRows * kHalf + e);
         add_bf16x2(acc[0], acc[1], v.x);
         add_bf16x2(acc[2], acc[3], v.y);
         add_bf16x2(acc[4], acc[5], v.z);
@@ -522,11 +618,14 @@ __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
       o.y = f32_to_bf16_rne(acc[2]) | (f32_to_bf16_rne(acc[3]) << 16);
       o.z = f32_to_bf16_rne(acc[4]) | (f32_to_bf16_rne(acc[5]) << 16);
       o.w = f32_to_bf16_rne(acc[6]) | (f32_to_bf16_rne(acc[7]) << 16);
-      store_row(y + r0 * kRow + e, min(8u, m - e), true, o);
+      store_row(y + gi, min(8u, nt - gi), true, o);
     }
     __syncthreads();
   }
-  if (late && lane == 0) set_status(a.hdr, kStTimeout);
+  if (late) {
+    stg.drain(late_b);
+    if (lane == 0) set_status(a.hdr, kStTimeout);
+  }
 }
 
 // ---------------------------------------------------------------- launchers
@@ -536,7 +635,7 @@ cudaError_t launch_decode(const DprepArgs& prep, const DecodeArgs& args, uint32_
   zc_dprep_kernel<<<prep.n_chunks + 1, 256, 0, s>>>(prep);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || max_items == 0) return e;
-  zc_decode_kernel<<<max_items, 32, 0, s>>>(args);
+  zc_decode_kernel<<<max_items, 64, 0, s>>>(args);
   return cudaGetLastError();
 }
 
@@ -544,10 +643,9 @@ cudaError_t launch_reduce(const ReduceArgs& args, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  size_t smem_max = 0;
-  for (uint32_t k = 1; k <= kMaxPeers; ++k) smem_max = reduce_smem_bytes(k) > smem_max ? reduce_smem_bytes(k) : smem_max;
   if (dev >= 0 && dev < 64 && !g_red_attr_done[dev]) {
-    e = cudaFuncSetAttribute(zc_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
+    e = cudaFuncSetAttribute(zc_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)reduce_smem_bytes(kMaxPeers));
     if (e != cudaSuccess) return e;
     g_red_attr_done[dev] = 1;
   }
@@ -555,7 +653,7 @@ cudaError_t launch_reduce(const ReduceArgs& args, cudaStream_t s) {
   e = cudaGetLastError();
   if (e != cudaSuccess || args.n == 0) return e;
   const uint32_t tiles = (uint32_t)tiles_of(args.n);
-  zc_reduce_kernel<<<tiles, 32 * args.k, reduce_smem_bytes(args.k), s>>>(args);
+  zc_reduce_kernel<<<2 * tiles, 32 * args.k, reduce_smem_bytes(args.k), s>>>(args);
   return cudaGetLastError();
 }
 

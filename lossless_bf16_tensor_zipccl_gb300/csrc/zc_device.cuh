@@ -48,10 +48,6 @@ __device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
   return v;
 }
 
-__device__ __forceinline__ void prefetch_l1(const void* p) {
-  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
-}
-
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -76,14 +72,19 @@ __device__ __forceinline__ void bulk_commit_and_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-// ---- mbarrier-tracked TMA bulk load global -> shared (single use, phase 0)
+// ---- mbarrier-tracked TMA bulk loads global -> shared
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void bulk_load_async(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+// Arrive once on the barrier and announce `bytes` of TMA traffic for its phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+// TMA bulk copy global -> shared (no multicast), completing `bytes` on the barrier.
+__device__ __forceinline__ void bulk_copy_g2s(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                    smem_addr(sdst)),
                "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
@@ -189,78 +190,109 @@ __device__ __forceinline__ uint2 merge4(uint32_t e4, uint32_t sm4) {
 }
 
 // ---------------------------------------------------------------- lane decoder
-// Decodes one segment of a coded tile: symbols are taken 1-5 at a time from a
-// 1024-entry table (in shared memory) indexed by the next 10 stream bits; the window is a funnel
-// shift over two words with a third prefetched.  Pending symbols wait as
-// nibbles in `acc`; escape exponents wait as bytes in escv (positions 0-7)
-// and esch (8-11).
+// Decodes one segment of a coded tile.  Symbols come 1-5 at a time from a
+// 1024-entry table (shared memory) indexed by the next 10 stream bits; the
+// window is a funnel shift over two words (boff < 32) and a third word is
+// loaded one step ahead.  Words are read through a plain pointer: a copy of
+// the exponent region staged in shared memory, or the region in place in
+// global memory, never past its last word.  Up to 16 decoded symbols wait as
+// nibbles in a 64-bit accumulator, so a lane can decode ahead of the row its
+// warp emits; escape exponents wait as bytes in esc0..esc3 with a mask.
 struct LaneDecoder {
-  const uint32_t* seg;
-  const uint32_t* lut;  // shared-memory copy of the chunk's table
-  uint64_t acc, escv;
-  uint32_t nw, wi, cur, nxt, nx2, boff, cnt, esch, base4;
+  const uint32_t* wp;    // next word to load
+  const uint32_t* wend;  // one past the last readable word
+  const uint32_t* lut;
+  uint64_t acc;
+  uint32_t w0, w1, w2, boff, cnt;
+  uint32_t escm, esc0, esc1, esc2, esc3;
+  uint32_t base4;
 
-  // seg points into shared memory (staged exponent region) or global memory
-  __device__ __forceinline__ uint32_t word(uint32_t i) const { return i < nw ? seg[i] : 0u; }
+  __device__ __forceinline__ uint32_t next_word() {
+    const uint32_t w = wp < wend ? *wp : 0u;
+    ++wp;
+    return w;
+  }
 
-  __device__ __forceinline__ void init(const uint32_t* s, uint32_t n_words, const uint32_t* table, uint32_t base) {
-    seg = s;
-    nw = n_words;
+  // payload: first word of the tile's coded bitstream; start: this segment's
+  // first bit in it; end: one past the last readable word.
+  __device__ __forceinline__ void init(const uint32_t* payload, uint32_t start, const uint32_t* end,
+                                       const uint32_t* table, uint32_t base) {
+    wp = payload + (start >> 5);
+    wend = end;
     lut = table;
-    cur = word(0);
-    nxt = word(1);
-    nx2 = word(2);
-    wi = 3;
-    boff = 0;
+    w0 = next_word();
+    w1 = next_word();
+    w2 = next_word();
+    boff = start & 31;
     acc = 0;
     cnt = 0;
-    escv = 0;
-    esch = 0;
+    escm = esc0 = esc1 = esc2 = esc3 = 0;
     base4 = base * 0x01010101u;
   }
 
-  // Decode until at least `target` symbols are pending (target <= 8).
-  __device__ __forceinline__ void fill(uint32_t target) {
-    while (cnt < target) {
-      const uint32_t win = __funnelshift_r(cur, nxt, boff);
-      const uint32_t en = lut[win & (kLutEntries - 1)];
-      uint32_t nb = (en >> 20) & 15u;
-      acc |= (uint64_t)(en & 0xFFFFFu) << (4 * cnt);
-      cnt += (en >> 24) & 7u;
-      if (en & kLutEsc) {
-        const uint32_t e = (win >> nb) & 0xFFu;
-        const uint32_t p = cnt - 1;
-        nb += 8;
-        if (p < 8) {
-          escv = (escv & ~(0xFFull << (8 * p))) | ((uint64_t)e << (8 * p));
-        } else {
-          const uint32_t q = 8 * (p - 8);
-          esch = (esch & ~(0xFFu << q)) | (e << q);
-        }
-      }
-      boff += nb;
-      if (boff >= 32) {
-        boff -= 32;
-        cur = nxt;
-        nxt = nx2;
-        nx2 = word(wi);
-        ++wi;
-      }
+  __device__ __forceinline__ void place_escape(uint32_t p, uint32_t e) {
+    const uint32_t sh = 8 * (p & 3), m = ~(0xFFu << sh), v = e << sh;
+    switch (p >> 2) {
+      case 0: esc0 = (esc0 & m) | v; break;
+      case 1: esc1 = (esc1 & m) | v; break;
+      case 2: esc2 = (esc2 & m) | v; break;
+      default: esc3 = (esc3 & m) | v; break;
+    }
+    escm |= 1u << p;
+  }
+
+  // One table step.  Requires cnt <= 11 (room for 5 more symbols).
+  __device__ __forceinline__ void step() {
+    const uint32_t win = __funnelshift_r(w0, w1, boff);
+    const uint32_t en = lut[win & (kLutEntries - 1)];
+    acc |= (uint64_t)(en & 0xFFFFFu) << (4 * cnt);
+    uint32_t nb = (en >> 20) & 15u;
+    cnt += (en >> 24) & 7u;
+    if (__builtin_expect((en & kLutEsc) != 0, 0)) {
+      place_escape(cnt - 1, (win >> nb) & 0xFFu);
+      nb += 8;
+    }
+    boff += nb;
+    if (boff >= 32) {  // the window passed a word: slide by one
+      boff -= 32;
+      w0 = w1;
+      w1 = w2;
+      w2 = next_word();
+    }
+  }
+
+  // Warp-wide: decode until every lane holds at least `need` symbols (need
+  // <= 8); lanes that are there already keep decoding while they have room,
+  // so the next row starts ahead.  All 32 lanes must call this together.
+  __device__ __forceinline__ void fill_warp(uint32_t need) {
+    if (cnt <= 11) step();
+    if (cnt <= 11) step();
+    while (__any_sync(kFull, cnt < need)) {
+      if (cnt <= 11) step();
     }
   }
 
   // Pop 8 pending symbols as exponent bytes (e0..e3, e4..e7).
-  __device__ __forceinline__ void take8(uint32_t& lo, uint32_t& hi) {
-    const uint32_t nib = (uint32_t)acc;
-    const uint32_t ev = nib & 0x0F0F0F0Fu, od = (nib >> 4) & 0x0F0F0F0Fu;
-    const uint32_t x0 = __byte_perm(ev, od, 0x5140), x1 = __byte_perm(ev, od, 0x7362);
-    const uint32_t m0 = __vcmpeq4(x0, 0x0F0F0F0Fu), m1 = __vcmpeq4(x1, 0x0F0F0F0Fu);
-    lo = ((x0 + base4) & ~m0) | ((uint32_t)escv & m0);
-    hi = ((x1 + base4) & ~m1) | ((uint32_t)(escv >> 32) & m1);
+  __device__ __forceinline__ void take8(uint32_t& e_lo, uint32_t& e_hi) {
+    const uint32_t lo = (uint32_t)acc;
+    const uint32_t ev = lo & 0x0F0F0F0Fu, od = (lo >> 4) & 0x0F0F0F0Fu;
+    e_lo = __byte_perm(ev, od, 0x5140) + base4;
+    e_hi = __byte_perm(ev, od, 0x7362) + base4;
+    if (__builtin_expect((escm & 0xFFu) != 0, 0)) {  // substitute the raw exponents of escapes
+      const uint32_t m = escm;
+      const uint32_t m0 = (m & 1 ? 0xFFu : 0u) | (m & 2 ? 0xFF00u : 0u) | (m & 4 ? 0xFF0000u : 0u) |
+                          (m & 8 ? 0xFF000000u : 0u);
+      const uint32_t m1 = (m & 16 ? 0xFFu : 0u) | (m & 32 ? 0xFF00u : 0u) | (m & 64 ? 0xFF0000u : 0u) |
+                          (m & 128 ? 0xFF000000u : 0u);
+      e_lo = (e_lo & ~m0) | (esc0 & m0);
+      e_hi = (e_hi & ~m1) | (esc1 & m1);
+    }
     acc >>= 32;
     cnt = cnt > 8 ? cnt - 8 : 0;  // fewer than 8 only on a segment's last row
-    escv = esch;
-    esch = 0;
+    esc0 = esc2;
+    esc1 = esc3;
+    esc2 = esc3 = 0;
+    escm >>= 8;
   }
 };
 

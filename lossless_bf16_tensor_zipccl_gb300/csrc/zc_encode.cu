@@ -10,8 +10,8 @@
 //     traffic, few launches, communication-aware layout -> one fused kernel
 //     per tile computes lengths, packs bits in shared memory, finds its
 //     output offset by decoupled look-back over the flat tile list of all
-//     per-destination chunks, and writes the tile image with one TMA bulk
-//     store;
+//     per-destination chunks, and writes the tile image with TMA bulk
+//     stores;
 //   - Fig. 7 caption (shared-memory data layout): the tile image is staged in
 //     shared memory as header | sign/mantissa plane | exponent region.
 #include <cuda_runtime.h>
@@ -33,7 +33,8 @@ __device__ __forceinline__ int64_t floor_div_pos(int64_t a, int64_t b) {  // b >
 // floor(b n / 64)), skipping e = 0 and e = 255, gives
 //   q = round-half-up(16 (mean - 127 + 1.4164)),
 // 1.4164 being 1/2 + (gamma + ln 2)/(2 ln 2): the mean of floor(log2 |Z|)
-// below log2(sigma) for a centred Gaussian.
+// below log2(sigma) for a centred Gaussian.  The block also writes the
+// chunk's code tables for the encoder.
 __global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ SelectArgs a) {
   const SelectChunkArg ca = a.c[blockIdx.x];
   const uint32_t ci = a.chunk0 + blockIdx.x;
@@ -82,6 +83,7 @@ __global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ 
   const int r = q - 16 * kq;
   int base = kq + 127 + a.base_off[r];
   base = base < 0 ? 0 : (base > 240 ? 240 : base);
+  const uint64_t lens = a.lens[r];
   if (threadIdx.x == 0) {
     EncChunk ec;
     ec.elem_start = ca.elem_start;
@@ -90,10 +92,30 @@ __global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ 
     ec.n_tiles = ca.n_tiles;
     ec.q = q;
     ec.base = (uint32_t)base;
-    ec.lens = a.lens[r];
+    ec.lens = lens;
     ec.start_slot = 0;
     ec.pad[0] = ec.pad[1] = 0;
     a.chunks[ci] = ec;
+  }
+  // Code tables of the chunk.  tab[e]: reversed codeword | length << 24 (an
+  // escape entry carries the 8 raw exponent bits after the codeword).
+  // pair[x0 | x1 << 4]: both reversed codewords, first lowest (bits 0-19) |
+  // an escape flag (bit 20) | total length including 8 raw bits per escape
+  // (bits 26-31); a pair with an escape is packed symbol by symbol.
+  {
+    uint32_t* tab = a.tables + (size_t)ci * kEncTableWords;
+    const uint32_t e = threadIdx.x;
+    const int xs = (int)e - base;
+    const int sym = (xs >= 0 && xs < kWindow) ? xs : kEsc;
+    const int L = (int)((lens >> (4 * sym)) & 15);
+    const uint32_t rev = bit_reverse(canonical_code(lens, sym), L);
+    tab[e] = sym == kEsc ? ((rev | (e << L)) | ((uint32_t)(L + 8) << 24)) : (rev | ((uint32_t)L << 24));
+    const uint32_t s0 = e & 15, s1 = e >> 4;
+    const uint32_t l0 = (uint32_t)((lens >> (4 * s0)) & 15), l1 = (uint32_t)((lens >> (4 * s1)) & 15);
+    const uint32_t c0 = bit_reverse(canonical_code(lens, (int)s0), (int)l0);
+    const uint32_t c1 = bit_reverse(canonical_code(lens, (int)s1), (int)l1);
+    const uint32_t raw = (s0 == (uint32_t)kEsc ? 8u : 0u) + (s1 == (uint32_t)kEsc ? 8u : 0u);
+    tab[256 + e] = (c0 | (c1 << l0)) | (raw ? kPairEsc : 0u) | ((l0 + l1 + raw) << 26);
   }
   const uint32_t items = ca.n_tiles ? ca.n_tiles : 1u;
   for (uint32_t i = threadIdx.x; i < items; i += blockDim.x) {
@@ -103,13 +125,28 @@ __global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ 
 }
 
 // ---------------------------------------------------------------- encode
+// One CTA per tile.  Row warps 0..6 own the left half of every row
+// (segments 0..31), row warps 7..13 the right half (segments 32..63), each a
+// run of 9 or 10 rows; lane l of a row warp in half h works on segment
+// 32 h + l.  Warp 14 is the control warp: it lays out the segments,
+// publishes the tile's size, runs the look-back and writes the chunk header
+// while the row warps pack codewords.
 // Shared memory: tile image (header | sign/mantissa plane | exponent region)
-// | staged exponent bytes | per-exponent table | pair table | part offsets.
+// | staged exponent bytes | code tables | per-(row warp, lane) bit counts.
 constexpr uint32_t kImgBytes = kTileHdr + kTile + kTile;
-constexpr int kEncThreads = 512;  // 16 warps; warp w owns rows 8w..8w+7
-constexpr int kEncWarps = kEncThreads / 32;
-constexpr int kRowsPerWarp = kRows / kEncWarps;
-constexpr uint32_t kEncSmem = kImgBytes + kTile + 256 * 4 + 256 * 4 + kEncWarps * 32 * 4;
+constexpr int kRowWarpsPerHalf = 7;
+constexpr int kRowWarps = 2 * kRowWarpsPerHalf;
+constexpr int kCtlWarp = kRowWarps;
+constexpr int kEncThreads = 32 * (kRowWarps + 1);
+constexpr int kMaxRowsPerWarp = (kRows + kRowWarpsPerHalf - 1) / kRowWarpsPerHalf;
+constexpr uint32_t kEncSmem = kImgBytes + kTile + kEncTableWords * 4 + kRowWarps * 32 * 4;
+
+__device__ __forceinline__ uint32_t warp_row_begin(uint32_t w) {
+  return (kRows * (w % kRowWarpsPerHalf)) / kRowWarpsPerHalf;
+}
+__device__ __forceinline__ uint32_t warp_row_end(uint32_t w) {
+  return (kRows * (w % kRowWarpsPerHalf + 1)) / kRowWarpsPerHalf;
+}
 
 // Decoupled look-back over the flat tile list (warp-wide).  Each tile
 // publishes its byte count (aggregate), then its inclusive prefix.  Returns
@@ -154,54 +191,79 @@ __device__ uint64_t lookback(uint64_t* state, uint32_t item, uint32_t lane, bool
   }
 }
 
-// 4 exponent bytes -> 4 symbol bytes (x = e - base inside the window, else
-// 15 = escape); esc gets 0xFF in each escaped byte.
-__device__ __forceinline__ uint32_t symbols4(uint32_t e4, uint32_t base4, uint32_t& esc) {
-  const uint32_t x = __vsub4(e4, base4);          // per byte, mod 256
-  esc = __vcmpgeu4(x, 0x0F0F0F0Fu);               // x >= 15 (or wrapped below base)
-  return (x & ~esc) | (0x0F0F0F0Fu & esc);
+// Pair index x0 | x1 << 4 of the two BF16 values in word w, with
+// x = e - base inside the window and 15 (escape) outside it.
+__device__ __forceinline__ uint32_t pair_index(uint32_t w, uint32_t base) {
+  const uint32_t x0 = min(((w >> 7) & 0xFFu) - base, 15u);  // wraps below base -> escape
+  const uint32_t x1 = min(((w >> 23) & 0xFFu) - base, 15u);
+  return x0 | (x1 << 4);
 }
 
-// Pair indices of 4 symbol bytes: byte 0 = x0 | x1 << 4, byte 2 = x2 | x3 << 4.
-__device__ __forceinline__ uint32_t pairs4(uint32_t x4) { return x4 | (x4 >> 4); }
+// The same from two exponent bytes at positions b and b + 1 of e4.
+__device__ __forceinline__ uint32_t pair_index_bytes(uint32_t e4, uint32_t b, uint32_t base) {
+  const uint32_t x0 = min(((e4 >> (8 * b)) & 0xFFu) - base, 15u);
+  const uint32_t x1 = min(((e4 >> (8 * b + 8)) & 0xFFu) - base, 15u);
+  return x0 | (x1 << 4);
+}
 
-// Bit sink for one lane's part of a segment in shared memory: the first word
-// and the last word may be shared with the neighbouring parts (OR-ed in); the
-// words in between belong to this part alone (stored).
+// Bit sink for one lane's part of a segment in shared memory (32-bit,
+// branch-free).  The part's first word may be shared with the previous part
+// and its last word with the next one: both are OR-ed in at the end; the
+// words in between belong to this part alone and are stored as they fill.
+// code < 2^24, len <= 24, nacc < 32.
 struct BitSink {
   uint32_t* sw;
-  uint64_t acc;
-  uint32_t widx, nacc;
-  bool first;
+  uint32_t acc, widx, nacc, first_idx, first_word, nfl;
+  __device__ __forceinline__ void begin(uint32_t* words, uint32_t start_bit) {
+    sw = words;
+    acc = 0;
+    widx = first_idx = start_bit >> 5;
+    nacc = start_bit & 31;
+    first_word = 0;
+    nfl = 0;
+  }
   __device__ __forceinline__ void put(uint32_t code, uint32_t len) {
-    acc |= (uint64_t)code << nacc;
+    const uint32_t spill = __funnelshift_l(code, 0u, nacc);  // bits of code << nacc above bit 31
+    acc |= code << nacc;
     nacc += len;
-    if (nacc >= 32) {
-      if (first) {
-        atomicOr(sw + widx, (uint32_t)acc);
-        first = false;
-      } else {
-        sw[widx] = (uint32_t)acc;
-      }
-      ++widx;
-      acc >>= 32;
-      nacc -= 32;
-    }
+    const bool flush = nacc >= 32;
+    if (flush && nfl) sw[widx] = acc;
+    first_word = (flush && !nfl) ? acc : first_word;
+    nfl |= flush ? 1u : 0u;
+    widx += flush ? 1u : 0u;
+    acc = flush ? spill : acc;
+    nacc -= flush ? 32u : 0u;
   }
   __device__ __forceinline__ void finish() {
-    if (nacc) atomicOr(sw + widx, (uint32_t)acc);
+    if (nfl) atomicOr(sw + first_idx, first_word);
+    if (nacc) atomicOr(sw + widx, acc);
   }
 };
+
+// Sign/mantissa bytes and exponent bytes of the 8 values in 4 words.
+__device__ __forceinline__ void split8(const uint32_t (&w)[4], uint32_t& sm0, uint32_t& sm1, uint32_t& ex0,
+                                       uint32_t& ex1) {
+  uint32_t e2[4], s2[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    e2[p] = (w[p] >> 7) & 0x00FF00FFu;
+    s2[p] = ((w[p] >> 8) & 0x00800080u) | (w[p] & 0x007F007Fu);
+  }
+  ex0 = __byte_perm(e2[0], e2[1], 0x6420);
+  ex1 = __byte_perm(e2[2], e2[3], 0x6420);
+  sm0 = __byte_perm(s2[0], s2[1], 0x6420);
+  sm1 = __byte_perm(s2[2], s2[3], 0x6420);
+}
 
 __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* img = smem;
   uint8_t* exps = smem + kImgBytes;  // exponent bytes in element order
   uint32_t* tab = reinterpret_cast<uint32_t*>(smem + kImgBytes + kTile);  // per exponent: code | len << 24
-  uint32_t* pair = tab + 256;          // per symbol pair: codes (<= 20 bits) | len << 20, escape without raw bits
-  uint32_t* part = pair + 256;         // [warp][segment] bits, then bit offsets
+  uint32_t* pair = tab + 256;                                             // per symbol pair
+  uint32_t* part = tab + kEncTableWords;  // [row warp][lane] bits, then bit offsets
   __shared__ uint32_t s_item, s_mode, s_err, s_size;
-  __shared__ uint32_t s_wstart[32];
+  __shared__ uint32_t s_segstart[kSegs];
   __shared__ unsigned long long s_goff;
 
   const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -218,28 +280,13 @@ __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a)
   const uint64_t elem0 = ci.elem_start + (uint64_t)k * kTile;
   const uint16_t* x = a.in + elem0;
   const bool vec = (elem0 & 7) == 0;
-  const uint32_t base = ci.base, base4 = base * 0x01010101u;
+  const uint32_t base = ci.base;
   const uint32_t sm_pad = (uint32_t)pad16(nt);
   const uint32_t exp_off = kTileHdr + sm_pad;
 
-  // Code tables.  tab[e]: reversed codeword | length << 24 (an escape entry
-  // carries the 8 raw exponent bits after the codeword).  pair[x0 | x1 << 4]:
-  // both reversed codewords, first one lowest | total length << 20.
-  if (tid < 256) {
-    const int xs = (int)tid - (int)base;
-    const int sym = (xs >= 0 && xs < kWindow) ? xs : kEsc;
-    const int L = (int)((ci.lens >> (4 * sym)) & 15);
-    const uint32_t rev = bit_reverse(canonical_code(ci.lens, sym), L);
-    tab[tid] = sym == kEsc ? ((rev | (tid << L)) | ((uint32_t)(L + 8) << 24)) : (rev | ((uint32_t)L << 24));
-  } else {
-    const uint32_t pi = tid - 256, s0 = pi & 15, s1 = pi >> 4;
-    const uint32_t l0 = (uint32_t)((ci.lens >> (4 * s0)) & 15), l1 = (uint32_t)((ci.lens >> (4 * s1)) & 15);
-    const uint32_t c0 = bit_reverse(canonical_code(ci.lens, (int)s0), (int)l0);
-    const uint32_t c1 = bit_reverse(canonical_code(ci.lens, (int)s1), (int)l1);
-    pair[pi] = (c0 | (c1 << l0)) | ((l0 + l1) << 20);
-  }
-  // Zero the padding of the sign/mantissa plane and staging, and the
-  // exponent area (the boundary words of coded parts are OR-ed in).
+  // Tables from the select kernel; zero the padding of the sign/mantissa
+  // plane and staging, and the exponent area (boundary words are OR-ed in).
+  for (uint32_t i = tid; i < kEncTableWords; i += kEncThreads) tab[i] = __ldg(a.tables + (size_t)c * kEncTableWords + i);
   if (tid < 16 && nt + tid < sm_pad) {
     img[kTileHdr + nt + tid] = 0;
     exps[nt + tid] = 0;
@@ -248,18 +295,38 @@ __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a)
     *reinterpret_cast<uint4*>(img + exp_off + o) = make_uint4(0, 0, 0, 0);
   __syncthreads();
 
-  // Phase A: 16-B loads; sign/mantissa bytes to the image, exponent bytes to
-  // the staging area; sum the code lengths (pair table + 8 per escape).
-  uint32_t bits = 0;
-  {
-    uint4 v[kRowsPerWarp];
+  const uint32_t rb = warp < kRowWarps ? warp_row_begin(warp) : kRows;
+  const uint32_t re = warp < kRowWarps ? warp_row_end(warp) : kRows;
+  const uint32_t col = (warp < kRowWarps ? (warp / kRowWarpsPerHalf) * kHalf : 0u) + lane * kLaneElems;
+
+  // Phase A (row warps): 16-B loads; sign/mantissa bytes to the image,
+  // exponent bytes to the staging area; sum the code lengths (pair table,
+  // which counts the 8 raw bits of an escape).
+  const bool full = nt == kTile && vec;
+  if (warp < kRowWarps) {
+    uint32_t bits = 0;
+    if (full) {
+      uint4 v[kMaxRowsPerWarp];
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      const uint32_t i0 = (warp * kRowsPerWarp + r) * kRow + lane * kLaneElems;
-      const uint32_t cnt = nt > i0 ? min(8u, nt - i0) : 0u;
-      if (cnt == 8 && vec) {
-        v[r] = ld_stream_v4(x + i0);
-      } else {
+      for (int r = 0; r < kMaxRowsPerWarp; ++r)
+        if (rb + r < re) v[r] = ld_stream_v4(x + (rb + r) * kRow + col);
+#pragma unroll
+      for (int r = 0; r < kMaxRowsPerWarp; ++r) {
+        if (rb + r < re) {
+          const uint32_t i0 = (rb + r) * kRow + col;
+          const uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+          uint32_t sm0, sm1, ex0, ex1;
+          split8(w, sm0, sm1, ex0, ex1);
+          *reinterpret_cast<uint2*>(img + kTileHdr + i0) = make_uint2(sm0, sm1);
+          *reinterpret_cast<uint2*>(exps + i0) = make_uint2(ex0, ex1);
+          bits += (pair[pair_index(w[0], base)] >> 26) + (pair[pair_index(w[1], base)] >> 26) +
+                  (pair[pair_index(w[2], base)] >> 26) + (pair[pair_index(w[3], base)] >> 26);
+        }
+      }
+    } else {
+      for (uint32_t row = rb; row < re; ++row) {
+        const uint32_t i0 = row * kRow + col;
+        const uint32_t cnt = nt > i0 ? min(8u, nt - i0) : 0u;
         uint32_t w[4];
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
@@ -267,30 +334,8 @@ __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a)
           const uint32_t hi = (2 * p + 1 < (int)cnt) ? x[i0 + 2 * p + 1] : 0u;
           w[p] = lo | (hi << 16);
         }
-        v[r] = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      const uint32_t i0 = (warp * kRowsPerWarp + r) * kRow + lane * kLaneElems;
-      const uint32_t cnt = nt > i0 ? min(8u, nt - i0) : 0u;
-      const uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
-      uint32_t e2[4], s2[4];
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        e2[p] = (w[p] >> 7) & 0x00FF00FFu;
-        s2[p] = ((w[p] >> 8) & 0x00800080u) | (w[p] & 0x007F007Fu);
-      }
-      const uint32_t ex0 = __byte_perm(e2[0], e2[1], 0x6420), ex1 = __byte_perm(e2[2], e2[3], 0x6420);
-      const uint32_t sm0 = __byte_perm(s2[0], s2[1], 0x6420), sm1 = __byte_perm(s2[2], s2[3], 0x6420);
-      if (cnt == 8) {
-        *reinterpret_cast<uint2*>(img + kTileHdr + i0) = make_uint2(sm0, sm1);
-        *reinterpret_cast<uint2*>(exps + i0) = make_uint2(ex0, ex1);
-        uint32_t m0, m1;
-        const uint32_t t0 = pairs4(symbols4(ex0, base4, m0)), t1 = pairs4(symbols4(ex1, base4, m1));
-        bits += (pair[t0 & 0xFF] >> 20) + (pair[(t0 >> 16) & 0xFF] >> 20) + (pair[t1 & 0xFF] >> 20) +
-                (pair[(t1 >> 16) & 0xFF] >> 20) + __popc(m0) + __popc(m1);
-      } else if (cnt) {
+        uint32_t sm0, sm1, ex0, ex1;
+        split8(w, sm0, sm1, ex0, ex1);
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           if (t < (int)cnt) {
@@ -302,33 +347,47 @@ __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a)
         }
       }
     }
+    part[warp * 32 + lane] = bits;
   }
-  part[warp * 32 + lane] = bits;
   __syncthreads();
 
-  // Phase B (warp 0): bit offset of each warp's part inside each segment,
-  // word-aligned segment starts, raw/coded choice, publish the aggregate.
+  // Phase B (control warp): bit offset of each row warp's part inside its
+  // segment, bit-granular segment starts, raw/coded choice, publish the
+  // aggregate.  Lane l handles segments l and 32 + l.
   uint64_t agg = 0;
-  if (warp == 0) {
-    uint32_t off = 0;
+  if (warp == kCtlWarp) {
+    uint32_t seg[2];
 #pragma unroll
-    for (int w = 0; w < kEncWarps; ++w) {
-      const uint32_t v = part[w * 32 + lane];
-      part[w * 32 + lane] = off;
-      off += v;
+    for (int h = 0; h < 2; ++h) {
+      uint32_t off = 0;
+#pragma unroll
+      for (int w = 0; w < kRowWarpsPerHalf; ++w) {
+        const uint32_t i = (h * kRowWarpsPerHalf + w) * 32 + lane;
+        const uint32_t v = part[i];
+        part[i] = off;
+        off += v;
+      }
+      seg[h] = off;
     }
-    const uint32_t words = (off + 31) >> 5;
-    uint32_t incl = words;
+    uint32_t start0 = seg[0], start1 = seg[1];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(kFull, incl, o);
-      if (lane >= (uint32_t)o) incl += y;
+      const uint32_t y0 = __shfl_up_sync(kFull, start0, o), y1 = __shfl_up_sync(kFull, start1, o);
+      if (lane >= (uint32_t)o) {
+        start0 += y0;
+        start1 += y1;
+      }
     }
-    const uint32_t W = __shfl_sync(kFull, incl, 31);
-    s_wstart[lane] = incl - words;
-    const bool coded = kSegTab + 4ull * W < nt;
-    const uint32_t exp_bytes = coded ? kSegTab + 4 * W : nt;
-    if (coded) *reinterpret_cast<uint16_t*>(img + exp_off + 2 * lane) = (uint16_t)words;
+    const uint32_t total0 = __shfl_sync(kFull, start0, 31), total1 = __shfl_sync(kFull, start1, 31);
+    s_segstart[lane] = start0 - seg[0];
+    s_segstart[32 + lane] = total0 + start1 - seg[1];
+    const uint32_t words = (total0 + total1 + 31) >> 5;
+    const bool coded = kSegTab + 4ull * words < nt;
+    const uint32_t exp_bytes = coded ? kSegTab + 4 * words : nt;
+    if (coded) {
+      reinterpret_cast<uint16_t*>(img + exp_off)[lane] = (uint16_t)seg[0];
+      reinterpret_cast<uint16_t*>(img + exp_off)[32 + lane] = (uint16_t)seg[1];
+    }
     const uint32_t size = nt ? (uint32_t)(kTileHdr + sm_pad + pad16(exp_bytes)) : 0u;
     agg = size + (k == 0 ? chunk_hdr_bytes(ci.n_tiles) : 0);
     if (lane == 0) {
@@ -340,9 +399,9 @@ __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a)
   }
   __syncthreads();
 
-  // Phase C (warp 0 first): look-back for this tile's byte offset, chunk
-  // header / tile table / chunk offsets.
-  if (warp == 0) {
+  if (warp == kCtlWarp) {
+    // Phase C (control warp): look-back for this tile's byte offset, chunk
+    // header / tile table / chunk offsets.
     bool err = false;
     uint64_t excl = item == 0 ? 0 : lookback(a.item_state, item, lane, err);
     if (item != 0 && lane == 0) st_release_u64(a.item_state + item, err ? kFlagErr : (kFlagInc | (excl + agg)));
@@ -411,36 +470,30 @@ __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a)
       s_goff = goff;
       s_err = err ? 1u : 0u;
     }
-  }
-
-  // Phase D: pack codewords into the exponent region (coded tiles); raw
-  // tiles are stored straight from the staging area.
-  if (s_mode == 0) {
-    const uint32_t start = part[warp * 32 + lane];
+  } else if (s_mode == 0) {
+    // Phase D (row warps): pack codewords into the exponent region; raw tiles
+    // are stored straight from the staging area.
     BitSink sink;
-    sink.sw = reinterpret_cast<uint32_t*>(img + exp_off + kSegTab) + s_wstart[lane];
-    sink.acc = 0;
-    sink.widx = start >> 5;
-    sink.nacc = start & 31;
-    sink.first = true;
-#pragma unroll 2
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      const uint32_t i0 = (warp * kRowsPerWarp + r) * kRow + lane * kLaneElems;
-      const uint32_t cnt = nt > i0 ? min(8u, nt - i0) : 0u;
+    sink.begin(reinterpret_cast<uint32_t*>(img + exp_off + kSegTab),
+               s_segstart[(warp / kRowWarpsPerHalf) * 32 + lane] + part[warp * 32 + lane]);
+#pragma unroll 1
+    for (uint32_t row = rb; row < re; ++row) {
+      const uint32_t i0 = row * kRow + col;
+      const uint32_t cnt = full ? 8u : (nt > i0 ? min(8u, nt - i0) : 0u);
       if (cnt == 0) break;
       const uint2 e8 = *reinterpret_cast<const uint2*>(exps + i0);
-      uint32_t m0 = 0, m1 = 0, t0 = 0, t1 = 0;
+      uint32_t p0 = 0, p1 = 0, p2 = 0, p3 = 0;
       if (cnt == 8) {
-        t0 = pairs4(symbols4(e8.x, base4, m0));
-        t1 = pairs4(symbols4(e8.y, base4, m1));
+        p0 = pair[pair_index_bytes(e8.x, 0, base)];
+        p1 = pair[pair_index_bytes(e8.x, 2, base)];
+        p2 = pair[pair_index_bytes(e8.y, 0, base)];
+        p3 = pair[pair_index_bytes(e8.y, 2, base)];
       }
-      if (cnt == 8 && (m0 | m1) == 0) {
-        const uint32_t p0 = pair[t0 & 0xFF], p1 = pair[(t0 >> 16) & 0xFF];
-        const uint32_t p2 = pair[t1 & 0xFF], p3 = pair[(t1 >> 16) & 0xFF];
-        sink.put(p0 & 0xFFFFFu, p0 >> 20);
-        sink.put(p1 & 0xFFFFFu, p1 >> 20);
-        sink.put(p2 & 0xFFFFFu, p2 >> 20);
-        sink.put(p3 & 0xFFFFFu, p3 >> 20);
+      if (__builtin_expect(cnt == 8 && !((p0 | p1 | p2 | p3) & kPairEsc), 1)) {
+        sink.put(p0 & 0xFFFFFu, p0 >> 26);
+        sink.put(p1 & 0xFFFFFu, p1 >> 26);
+        sink.put(p2 & 0xFFFFFu, p2 >> 26);
+        sink.put(p3 & 0xFFFFFu, p3 >> 26);
       } else {
 #pragma unroll
         for (int t = 0; t < 8; ++t) {

@@ -4,7 +4,7 @@
 // Stream format v1 (little-endian):
 //   chunk  = ChunkHeader (32 B) | u32 tile_off[n_tiles] (from chunk start),
 //            zero-padded to 16 B | tiles (each 16-B aligned, back to back)
-//   ChunkHeader: u32 magic | u16 version | u8 tile_log2 (15) | u8 seg_log2 (10)
+//   ChunkHeader: u32 magic | u16 version | u8 tile_log2 (15) | u8 seg_log2 (9)
 //            | u64 n_elems | u32 n_tiles | u8 base | u8 flags (0) | i16 q
 //            | u8 lens[8]  (4-bit code lengths; symbol 2i in the low nibble)
 //   tile   = TileHeader (16 B): u32 mode (0 coded, 1 raw) | u32 n_t
@@ -12,15 +12,15 @@
 //            | sign/mantissa plane: n_t bytes (s << 7 | m), zero-padded to 16
 //            | exponent region (exp_bytes, zero-padded to 16):
 //                raw:   n_t exponent bytes in element order
-//                coded: u16 seg_words[32] | segments 0..31 of u32 words
-//   Element i of a tile sits in row i / 256 and segment (i mod 256) / 8; a
+//                coded: u16 seg_bits[64] | the 64 segment bitstreams back to
+//                       back at bit granularity, zero-padded to a u32 word
+//   Element i of a tile sits in row i / 512 and segment (i mod 512) / 8; a
 //   segment holds its elements' exponent symbols in increasing i.  Symbol
 //   x = e - base when 0 <= x <= 14, otherwise ESC (15) followed by the 8 raw
 //   exponent bits.  Bits fill u32 words from the least significant bit; a
 //   canonical codeword (assigned in (length, symbol) order) goes out most
-//   significant bit first, i.e. it is stored bit-reversed.  Each segment is
-//   zero-padded to a whole word.  Coded mode is used only when
-//   64 + 4 * sum(seg_words) < n_t.
+//   significant bit first, i.e. it is stored bit-reversed.  Coded mode is used
+//   only when 128 + 4 * ceil(sum(seg_bits) / 32) < n_t.
 #pragma once
 #include <stdint.h>
 
@@ -39,18 +39,19 @@ constexpr uint32_t kMagic = 0x4C43435Au;  // bytes 'Z' 'C' 'C' 'L'
 constexpr uint32_t kVersion = 1;
 constexpr uint32_t kTileLog2 = 15;
 constexpr uint32_t kTile = 1u << kTileLog2;  // elements per tile
-constexpr uint32_t kSegLog2 = 10;            // symbols per full segment
-constexpr uint32_t kRow = 256;               // elements per tile row
-constexpr uint32_t kRows = kTile / kRow;     // 128
+constexpr uint32_t kSegLog2 = 9;             // symbols per full segment: 512
+constexpr uint32_t kRow = 512;               // elements per tile row
+constexpr uint32_t kRows = kTile / kRow;     // 64
+constexpr uint32_t kHalf = kRow / 2;         // one warp's 32 segments cover half a row
 constexpr uint32_t kLaneElems = 8;           // consecutive elements of one segment per row
-constexpr uint32_t kSegs = 32;
+constexpr uint32_t kSegs = 64;
 constexpr int kNsym = 16;
 constexpr int kWindow = 15;
 constexpr int kEsc = 15;
 constexpr int kLmax = 10;
 constexpr uint32_t kChunkHdr = 32;
 constexpr uint32_t kTileHdr = 16;
-constexpr uint32_t kSegTab = 64;
+constexpr uint32_t kSegTab = 2 * kSegs;  // u16 bit length per segment
 constexpr uint32_t kMaxPeers = 16;
 constexpr uint32_t kLutEntries = 1u << kLmax;
 

@@ -10,6 +10,8 @@ namespace zc {
 // Scale selection: chunk records travel as kernel parameters, kSelectBatch
 // chunks per launch.
 constexpr uint32_t kSelectBatch = 256;
+constexpr uint32_t kEncTableWords = 512;  // per chunk: 256 per-exponent + 256 symbol-pair code entries
+constexpr uint32_t kPairEsc = 1u << 20;   // symbol-pair entry holds an escape
 
 struct SelectChunkArg {
   uint64_t elem_start;
@@ -23,6 +25,7 @@ struct SelectChunkArg {
 struct SelectArgs {
   const uint16_t* in;
   EncChunk* chunks;
+  uint32_t* tables;  // per chunk: kEncTableWords code-table words
   uint32_t* item_chunk;
   uint64_t* item_state;
   WsHeader* hdr;
@@ -39,6 +42,7 @@ struct EncodeArgs {
   uint64_t cap;
   uint64_t* offsets;
   EncChunk* chunks;
+  const uint32_t* tables;
   const uint32_t* item_chunk;
   uint64_t* item_state;
   WsHeader* hdr;
