@@ -118,6 +118,41 @@ zipccl_status zipccl_decompress_reduce(const void *const *d_peer_chunks,
                                        void *stream);
 
 /*
+ * zipccl_decompress_reduce for callers that may not allocate device memory
+ * at the point of the call: code that runs inside a device allocator's own
+ * hook or callback (allocating there would re-enter the allocator), and
+ * processes whose device memory is all reserved up front by a caching
+ * allocator, where a new allocation would fail or force the cache to be
+ * emptied.  Same kernels, same results; the workspace is a scratch area
+ * compiled into this library (one per device) instead of a caller buffer, and
+ * no call allocates or frees anything.  The paper has no counterpart to this
+ * call: it serves only such callers.
+ *   - The scratch holds ZIPCCL_NOALLOC_SCRATCH_BYTES bytes per device, the
+ *     workspace of k = ZIPCCL_NOALLOC_MAX_PEERS (16) peers.  k == 0 or
+ *     k > 16 returns ZIPCCL_ERR_INVALID_ARG before anything is launched.
+ *   - The first call on a device, made with that device current, does a
+ *     one-time set-up: it looks up the scratch's device address, which may
+ *     load this library's kernels onto the device.  Make that first call
+ *     before any stream capture begins.  A failed lookup returns
+ *     ZIPCCL_ERR_CUDA.
+ *   - Each call first clears the scratch's 256-byte status header on
+ *     `stream` (cudaMemsetAsync); the rest of the scratch is written before
+ *     it is read, so nothing else must start at zero.
+ *   - One scratch per device is shared by every call on that device: calls
+ *     that may overlap (other streams, host threads, or processes sharing the
+ *     context) race on it and must be ordered by the caller, e.g. on one
+ *     stream.
+ *   - d_scratch (may be NULL) receives the scratch's device address; pass it
+ *     to zipccl_get_device_status to read the device status of the call.
+ */
+#define ZIPCCL_NOALLOC_MAX_PEERS 16
+#define ZIPCCL_NOALLOC_SCRATCH_BYTES (256u + 1024u + 16u * 4096u)
+zipccl_status zipccl_decompress_reduce_noalloc(const void *const *d_peer_chunks,
+                                               const uint64_t *peer_chunk_bytes, uint32_t k,
+                                               uint64_t n, uint16_t *d_out, void **d_scratch,
+                                               void *stream);
+
+/*
  * Synchronizes `stream`, then returns the status the kernels of the last call
  * on this workspace recorded (ZIPCCL_OK, ZIPCCL_ERR_CORRUPT,
  * ZIPCCL_ERR_VERSION, ZIPCCL_ERR_TIMEOUT), or ZIPCCL_ERR_CUDA.

@@ -27,8 +27,8 @@ __all__ = [
     "ZipcclError", "load", "library_path", "zipccl_format_version", "zipccl_status_string",
     "zipccl_max_compressed_bytes", "zipccl_compress_workspace_bytes", "zipccl_decompress_workspace_bytes",
     "zipccl_reduce_workspace_bytes", "zipccl_compress", "zipccl_decompress", "zipccl_decompress_reduce",
-    "zipccl_get_device_status", "zipccl_codebook_phase", "compress", "decompress", "decompress_reduce",
-    "Compressed", "EXPORTED_SYMBOLS",
+    "zipccl_get_device_status", "zipccl_codebook_phase", "zipccl_decompress_reduce_noalloc", "compress",
+    "decompress", "decompress_reduce", "Compressed", "EXPORTED_SYMBOLS",
 ]
 
 OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_CORRUPT, ERR_VERSION, ERR_TIMEOUT, ERR_CUDA = range(7)
@@ -36,7 +36,7 @@ EXPORTED_SYMBOLS = [
     "zipccl_format_version", "zipccl_status_string", "zipccl_max_compressed_bytes",
     "zipccl_compress_workspace_bytes", "zipccl_decompress_workspace_bytes", "zipccl_reduce_workspace_bytes",
     "zipccl_compress", "zipccl_decompress", "zipccl_decompress_reduce", "zipccl_get_device_status",
-    "zipccl_codebook_phase",
+    "zipccl_codebook_phase", "zipccl_decompress_reduce_noalloc",
 ]
 
 _lock = threading.Lock()
@@ -94,6 +94,9 @@ def load(build_if_missing: bool = True):
         L.zipccl_decompress_reduce.argtypes = [ctypes.POINTER(vp), u64p, u32, u64, vp, vp, u64, vp]
         L.zipccl_get_device_status.restype = ctypes.c_int
         L.zipccl_get_device_status.argtypes = [vp, vp]
+        L.zipccl_decompress_reduce_noalloc.restype = ctypes.c_int
+        L.zipccl_decompress_reduce_noalloc.argtypes = [ctypes.POINTER(vp), u64p, u32, u64, vp,
+                                                       ctypes.POINTER(vp), vp]
         L.zipccl_codebook_phase.restype = ctypes.c_int
         L.zipccl_codebook_phase.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_uint8)]
         _lib = L
@@ -169,6 +172,16 @@ def zipccl_decompress_reduce(d_peer_chunks, peer_chunk_bytes, k: int, n: int, d_
 
 def zipccl_get_device_status(d_ws: int, stream: int) -> int:
     return int(load().zipccl_get_device_status(d_ws, stream))
+
+
+def zipccl_decompress_reduce_noalloc(d_peer_chunks, peer_chunk_bytes, k: int, n: int, d_out: int,
+                                     stream: int) -> tuple[int, int]:
+    """The no-allocation reduce call; returns (status, device address of its scratch)."""
+    ptrs = (ctypes.c_void_p * max(1, len(d_peer_chunks)))(*[int(p) for p in d_peer_chunks])
+    scratch = ctypes.c_void_p()
+    st = load().zipccl_decompress_reduce_noalloc(ptrs, _u64_array(peer_chunk_bytes), k, n, d_out,
+                                                 ctypes.byref(scratch), stream)
+    return int(st), int(scratch.value or 0)
 
 
 def zipccl_codebook_phase(phase: int) -> tuple[int, list[int]]:

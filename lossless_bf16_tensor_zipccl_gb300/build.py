@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libzipccl.so")
-SOURCES = ["zc_api.cu", "zc_encode.cu", "zc_decode.cu", "zc_codebook.cpp"]
+SOURCES = ["zc_api.cu", "zc_encode.cu", "zc_decode.cu", "zc_noalloc.cu", "zc_codebook.cpp"]
 HEADERS = ["zc_format.h", "zc_device.cuh", "zc_kernels.h", "zc_codebook.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # No fast-math: the reduce folds in IEEE fp32 with subnormals kept.
