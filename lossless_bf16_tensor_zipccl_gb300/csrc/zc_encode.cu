@@ -49,17 +49,20 @@ __global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ 
   } else {
     const uint16_t* x = a.in + ca.elem_start;
     long long S = 0, K = 0;
-    if (ca.n <= 4096) {
-      for (uint64_t i = threadIdx.x; i < ca.n; i += blockDim.x) {
-        const uint32_t e = (x[i] >> 7) & 0xFFu;
-        if (e != 0 && e != 255) { S += e; ++K; }
-      }
-    } else {
-      for (uint32_t s = threadIdx.x; s < 4096; s += blockDim.x) {
-        const uint64_t b = s >> 6, off = s & 63;
-        const uint32_t e = (x[(b * ca.n) / 64 + off] >> 7) & 0xFFu;
-        if (e != 0 && e != 255) { S += e; ++K; }
-      }
+    // 16 samples per thread (256 threads), all loads issued before any is used
+    uint32_t ev[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t s = threadIdx.x + 256u * i;
+      uint64_t at;
+      if (ca.n <= 4096) at = s;                                         // every element
+      else at = ((uint64_t)(s >> 6) * ca.n) / 64 + (s & 63);            // block s/64, offset s%64
+      ev[i] = at < ca.n ? x[at] : 0xFFFFu;                              // exponent 255: not counted
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t e = (ev[i] >> 7) & 0xFFu;
+      if (e != 0 && e != 255) { S += e; ++K; }
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
@@ -125,28 +128,34 @@ __global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ 
 }
 
 // ---------------------------------------------------------------- encode
-// One CTA per tile.  Row warps 0..6 own the left half of every row
-// (segments 0..31), row warps 7..13 the right half (segments 32..63), each a
-// run of 9 or 10 rows; lane l of a row warp in half h works on segment
-// 32 h + l.  Warp 14 is the control warp: it lays out the segments,
-// publishes the tile's size, runs the look-back and writes the chunk header
-// while the row warps pack codewords.
+// One CTA per tile.  Row warps 0..7 own the left half of every row
+// (segments 0..31), row warps 8..15 the right half (segments 32..63), eight
+// rows each; lane l of a row warp in half h works on segment 32 h + l.
+// Warp 16 is the control warp: it lays out the segments, publishes the
+// tile's size, runs the look-back and writes the chunk header while the row
+// warps assemble the exponent region.
+//
+// Single pass over the input: a row warp reads its rows once, writes the
+// sign/mantissa bytes into the tile image and packs each lane's codewords
+// into a private word buffer in shared memory as it goes (bit 0 of the part
+// at bit 0 of word 0).  Once every part's length is known, each lane copies
+// its part to its bit position in the segment stream with funnel shifts:
+// words that only this part touches are stored, the two end words are OR-ed.
+// A part longer than its private buffer (a lane with many escapes) sends
+// the tile down a slower path that re-reads its input and packs in place; a
+// raw tile re-reads its input to store the exponent bytes.
+//
 // Shared memory: tile image (header | sign/mantissa plane | exponent region)
-// | staged exponent bytes | code tables | per-(row warp, lane) bit counts.
+// | private part buffers | code tables | per-(row warp, lane) bit counts.
 constexpr uint32_t kImgBytes = kTileHdr + kTile + kTile;
-constexpr int kRowWarpsPerHalf = 7;
+constexpr int kRowWarpsPerHalf = 8;
 constexpr int kRowWarps = 2 * kRowWarpsPerHalf;
 constexpr int kCtlWarp = kRowWarps;
 constexpr int kEncThreads = 32 * (kRowWarps + 1);
-constexpr int kMaxRowsPerWarp = (kRows + kRowWarpsPerHalf - 1) / kRowWarpsPerHalf;
-constexpr uint32_t kEncSmem = kImgBytes + kTile + kEncTableWords * 4 + kRowWarps * 32 * 4;
-
-__device__ __forceinline__ uint32_t warp_row_begin(uint32_t w) {
-  return (kRows * (w % kRowWarpsPerHalf)) / kRowWarpsPerHalf;
-}
-__device__ __forceinline__ uint32_t warp_row_end(uint32_t w) {
-  return (kRows * (w % kRowWarpsPerHalf + 1)) / kRowWarpsPerHalf;
-}
+constexpr int kRowsPerWarp = kRows / kRowWarpsPerHalf;   // 8
+constexpr uint32_t kPrivWords = 16;                       // 512 bits per lane part (8 bits per value)
+constexpr uint32_t kPrivBytes = kRowWarps * 32 * kPrivWords * 4;
+constexpr uint32_t kEncSmem = kImgBytes + kPrivBytes + kEncTableWords * 4 + kRowWarps * 32 * 4;
 
 // Decoupled look-back over the flat tile list (warp-wide).  Each tile
 // publishes its byte count (aggregate), then its inclusive prefix.  Returns
@@ -191,21 +200,6 @@ __device__ uint64_t lookback(uint64_t* state, uint32_t item, uint32_t lane, bool
   }
 }
 
-// Pair index x0 | x1 << 4 of the two BF16 values in word w, with
-// x = e - base inside the window and 15 (escape) outside it.
-__device__ __forceinline__ uint32_t pair_index(uint32_t w, uint32_t base) {
-  const uint32_t x0 = min(((w >> 7) & 0xFFu) - base, 15u);  // wraps below base -> escape
-  const uint32_t x1 = min(((w >> 23) & 0xFFu) - base, 15u);
-  return x0 | (x1 << 4);
-}
-
-// The same from two exponent bytes at positions b and b + 1 of e4.
-__device__ __forceinline__ uint32_t pair_index_bytes(uint32_t e4, uint32_t b, uint32_t base) {
-  const uint32_t x0 = min(((e4 >> (8 * b)) & 0xFFu) - base, 15u);
-  const uint32_t x1 = min(((e4 >> (8 * b + 8)) & 0xFFu) - base, 15u);
-  return x0 | (x1 << 4);
-}
-
 // Bit sink for one lane's part of a segment in shared memory (32-bit,
 // branch-free).  The part's first word may be shared with the previous part
 // and its last word with the next one: both are OR-ed in at the end; the
@@ -240,29 +234,103 @@ struct BitSink {
   }
 };
 
-// Sign/mantissa bytes and exponent bytes of the 8 values in 4 words.
-__device__ __forceinline__ void split8(const uint32_t (&w)[4], uint32_t& sm0, uint32_t& sm1, uint32_t& ex0,
-                                       uint32_t& ex1) {
-  uint32_t e2[4], s2[4];
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    e2[p] = (w[p] >> 7) & 0x00FF00FFu;
-    s2[p] = ((w[p] >> 8) & 0x00800080u) | (w[p] & 0x007F007Fu);
+// Bit packer into a lane's private buffer (word j at p[32 j]).  Counts every
+// bit; words past kPrivWords are dropped and the caller sees the overflow in
+// bits().  code < 2^len, len <= 32.
+struct PrivSink {
+  uint32_t* p;
+  uint32_t acc, nacc, widx;
+  __device__ __forceinline__ void begin(uint32_t* lane_words) {
+    p = lane_words;
+    acc = nacc = widx = 0;
   }
-  ex0 = __byte_perm(e2[0], e2[1], 0x6420);
-  ex1 = __byte_perm(e2[2], e2[3], 0x6420);
-  sm0 = __byte_perm(s2[0], s2[1], 0x6420);
-  sm1 = __byte_perm(s2[2], s2[3], 0x6420);
+  __device__ __forceinline__ void put(uint32_t code, uint32_t len) {
+    const uint32_t spill = __funnelshift_l(code, 0u, nacc);  // bits of code << nacc above bit 31
+    acc |= code << nacc;
+    nacc += len;
+    if (nacc >= 32) {
+      if (widx < kPrivWords) p[32 * widx] = acc;
+      ++widx;
+      nacc -= 32;
+      acc = spill;
+    }
+  }
+  __device__ __forceinline__ void finish() {
+    if (nacc && widx < kPrivWords) p[32 * widx] = acc;
+  }
+  __device__ __forceinline__ uint32_t bits() const { return 32 * widx + nacc; }
+};
+
+// x << s for s < 32, 0 for s >= 32.
+__device__ __forceinline__ uint32_t shl_clamped(uint32_t x, uint32_t s) { return __funnelshift_l(0u, x, s); }
+
+// Sign/mantissa bytes (s << 7 | m) and exponent bytes of 4 BF16 values held
+// in two words (value 2i in the low half of word i).
+__device__ __forceinline__ void split4(uint32_t w0, uint32_t w1, uint32_t& sm, uint32_t& ex) {
+  const uint32_t lo = __byte_perm(w0, w1, 0x6420);  // low byte of each value
+  const uint32_t hi = __byte_perm(w0, w1, 0x7531);  // high byte of each value
+  sm = (hi & 0x80808080u) | (lo & 0x7F7F7F7Fu);
+  ex = ((hi << 1) & 0xFEFEFEFEu) | ((lo >> 7) & 0x01010101u);
+}
+
+// Pack the 8 exponents of one lane row (bytes of ex0, ex1) into the sink.
+// Fast path: every x = e - base in 0..14, codes combined through the
+// symbol-pair table into one put when the row fits 32 bits.
+__device__ __forceinline__ void pack_row8(PrivSink& sink, uint32_t ex0, uint32_t ex1, uint32_t base4,
+                                          const uint32_t* pair, const uint32_t* tab) {
+  const uint32_t y0 = ex0 - base4, y1 = ex1 - base4;  // bytes x (borrows only when some x < 0)
+  const bool in_window = ((y0 | y1) & 0xF0F0F0F0u) == 0;
+  const uint32_t z0 = y0 | (y0 >> 4), z1 = y1 | (y1 >> 4);
+  const uint32_t p0 = pair[z0 & 0xFFu], p1 = pair[(z0 >> 16) & 0xFFu];
+  const uint32_t p2 = pair[z1 & 0xFFu], p3 = pair[(z1 >> 16) & 0xFFu];
+  const bool fast = in_window && !((p0 | p1 | p2 | p3) & kPairEsc);
+  const uint32_t l0 = p0 >> 26, l1 = p1 >> 26, l2 = p2 >> 26, l3 = p3 >> 26;
+  const uint32_t s2 = l0 + l1, s3 = s2 + l2, tot = s3 + l3;
+  if (fast && tot <= 32) {
+    const uint32_t rc = (p0 & 0xFFFFFu) | shl_clamped(p1 & 0xFFFFFu, l0) | shl_clamped(p2 & 0xFFFFFu, s2) |
+                        shl_clamped(p3 & 0xFFFFFu, s3);
+    sink.put(rc, tot);
+  } else if (fast) {
+    sink.put(p0 & 0xFFFFFu, l0);
+    sink.put(p1 & 0xFFFFFu, l1);
+    sink.put(p2 & 0xFFFFFu, l2);
+    sink.put(p3 & 0xFFFFFu, l3);
+  } else {
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const uint32_t en = tab[((t < 4 ? ex0 : ex1) >> (8 * (t & 3))) & 0xFFu];
+      sink.put(en & 0xFFFFFFu, en >> 24);
+    }
+  }
+}
+
+// The 8 (or fewer, cnt) values of one lane row as 4 words, from a 16-B
+// aligned full group or element by element.
+__device__ __forceinline__ void load_group(const uint16_t* x, uint32_t cnt, bool vec, uint32_t (&w)[4]) {
+  if (vec && cnt == 8) {
+    const uint4 v = ld_stream_v4(x);
+    w[0] = v.x;
+    w[1] = v.y;
+    w[2] = v.z;
+    w[3] = v.w;
+  } else {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const uint32_t lo = (2 * p < (int)cnt) ? x[2 * p] : 0u;
+      const uint32_t hi = (2 * p + 1 < (int)cnt) ? x[2 * p + 1] : 0u;
+      w[p] = lo | (hi << 16);
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* img = smem;
-  uint8_t* exps = smem + kImgBytes;  // exponent bytes in element order
-  uint32_t* tab = reinterpret_cast<uint32_t*>(smem + kImgBytes + kTile);  // per exponent: code | len << 24
-  uint32_t* pair = tab + 256;                                             // per symbol pair
+  uint32_t* priv = reinterpret_cast<uint32_t*>(smem + kImgBytes);                    // [warp][word][lane]
+  uint32_t* tab = reinterpret_cast<uint32_t*>(smem + kImgBytes + kPrivBytes);       // per exponent
+  uint32_t* pair = tab + 256;                                                        // per symbol pair
   uint32_t* part = tab + kEncTableWords;  // [row warp][lane] bits, then bit offsets
-  __shared__ uint32_t s_item, s_mode, s_err, s_size;
+  __shared__ uint32_t s_item, s_mode, s_err, s_size, s_over;
   __shared__ uint32_t s_segstart[kSegs];
   __shared__ unsigned long long s_goff;
 
@@ -270,6 +338,7 @@ __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a)
   if (tid == 0) {
     s_item = atomicAdd(&a.hdr->counter, 1u);  // tiles start in claim order
     s_err = 0;
+    s_over = 0;
   }
   __syncthreads();
   const uint32_t item = s_item;
@@ -281,73 +350,71 @@ __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a)
   const uint16_t* x = a.in + elem0;
   const bool vec = (elem0 & 7) == 0;
   const uint32_t base = ci.base;
+  const uint32_t base4 = base * 0x01010101u;
   const uint32_t sm_pad = (uint32_t)pad16(nt);
   const uint32_t exp_off = kTileHdr + sm_pad;
+  uint32_t* region = reinterpret_cast<uint32_t*>(img + exp_off + kSegTab);  // coded payload words
 
   // Tables from the select kernel; zero the padding of the sign/mantissa
-  // plane and staging, and the exponent area (boundary words are OR-ed in).
+  // plane and the exponent area (the end words of each part are OR-ed in).
   for (uint32_t i = tid; i < kEncTableWords; i += kEncThreads) tab[i] = __ldg(a.tables + (size_t)c * kEncTableWords + i);
-  if (tid < 16 && nt + tid < sm_pad) {
-    img[kTileHdr + nt + tid] = 0;
-    exps[nt + tid] = 0;
-  }
+  if (tid < 16 && nt + tid < sm_pad) img[kTileHdr + nt + tid] = 0;
   for (uint32_t o = tid * 16; o < sm_pad; o += kEncThreads * 16)
     *reinterpret_cast<uint4*>(img + exp_off + o) = make_uint4(0, 0, 0, 0);
   __syncthreads();
 
-  const uint32_t rb = warp < kRowWarps ? warp_row_begin(warp) : kRows;
-  const uint32_t re = warp < kRowWarps ? warp_row_end(warp) : kRows;
-  const uint32_t col = (warp < kRowWarps ? (warp / kRowWarpsPerHalf) * kHalf : 0u) + lane * kLaneElems;
-
-  // Phase A (row warps): 16-B loads; sign/mantissa bytes to the image,
-  // exponent bytes to the staging area; sum the code lengths (pair table,
-  // which counts the 8 raw bits of an escape).
+  const uint32_t half = warp < kRowWarps ? warp / kRowWarpsPerHalf : 0u;
+  const uint32_t rb = warp < kRowWarps ? (warp % kRowWarpsPerHalf) * kRowsPerWarp : kRows;
+  const uint32_t col = half * kHalf + lane * kLaneElems;
   const bool full = nt == kTile && vec;
+
+  // Phase A (row warps): read each row group once; sign/mantissa bytes to
+  // the image, codewords to the private buffer.
+  uint32_t my_bits = 0;
   if (warp < kRowWarps) {
-    uint32_t bits = 0;
+    PrivSink sink;
+    sink.begin(priv + warp * (32 * kPrivWords) + lane);
     if (full) {
-      uint4 v[kMaxRowsPerWarp];
+      uint4 v[kRowsPerWarp];
 #pragma unroll
-      for (int r = 0; r < kMaxRowsPerWarp; ++r)
-        if (rb + r < re) v[r] = ld_stream_v4(x + (rb + r) * kRow + col);
+      for (int r = 0; r < kRowsPerWarp; ++r) v[r] = ld_stream_v4(x + (rb + r) * kRow + col);
 #pragma unroll
-      for (int r = 0; r < kMaxRowsPerWarp; ++r) {
-        if (rb + r < re) {
-          const uint32_t i0 = (rb + r) * kRow + col;
-          const uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
-          uint32_t sm0, sm1, ex0, ex1;
-          split8(w, sm0, sm1, ex0, ex1);
-          *reinterpret_cast<uint2*>(img + kTileHdr + i0) = make_uint2(sm0, sm1);
-          *reinterpret_cast<uint2*>(exps + i0) = make_uint2(ex0, ex1);
-          bits += (pair[pair_index(w[0], base)] >> 26) + (pair[pair_index(w[1], base)] >> 26) +
-                  (pair[pair_index(w[2], base)] >> 26) + (pair[pair_index(w[3], base)] >> 26);
-        }
+      for (int r = 0; r < kRowsPerWarp; ++r) {
+        uint32_t sm0, sm1, ex0, ex1;
+        split4(v[r].x, v[r].y, sm0, ex0);
+        split4(v[r].z, v[r].w, sm1, ex1);
+        *reinterpret_cast<uint2*>(img + kTileHdr + (rb + r) * kRow + col) = make_uint2(sm0, sm1);
+        pack_row8(sink, ex0, ex1, base4, pair, tab);
       }
     } else {
-      for (uint32_t row = rb; row < re; ++row) {
+      for (uint32_t row = rb; row < rb + kRowsPerWarp; ++row) {
         const uint32_t i0 = row * kRow + col;
         const uint32_t cnt = nt > i0 ? min(8u, nt - i0) : 0u;
+        if (cnt == 0) break;
         uint32_t w[4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const uint32_t lo = (2 * p < (int)cnt) ? x[i0 + 2 * p] : 0u;
-          const uint32_t hi = (2 * p + 1 < (int)cnt) ? x[i0 + 2 * p + 1] : 0u;
-          w[p] = lo | (hi << 16);
-        }
+        load_group(x + i0, cnt, vec, w);
         uint32_t sm0, sm1, ex0, ex1;
-        split8(w, sm0, sm1, ex0, ex1);
+        split4(w[0], w[1], sm0, ex0);
+        split4(w[2], w[3], sm1, ex1);
+        if (cnt == 8) {
+          *reinterpret_cast<uint2*>(img + kTileHdr + i0) = make_uint2(sm0, sm1);
+          pack_row8(sink, ex0, ex1, base4, pair, tab);
+        } else {
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          if (t < (int)cnt) {
-            const uint32_t e = ((t < 4 ? ex0 : ex1) >> (8 * (t & 3))) & 0xFFu;
-            img[kTileHdr + i0 + t] = (uint8_t)((t < 4 ? sm0 : sm1) >> (8 * (t & 3)));
-            exps[i0 + t] = (uint8_t)e;
-            bits += tab[e] >> 24;
+          for (int t = 0; t < 8; ++t) {
+            if (t < (int)cnt) {
+              img[kTileHdr + i0 + t] = (uint8_t)((t < 4 ? sm0 : sm1) >> (8 * (t & 3)));
+              const uint32_t en = tab[((t < 4 ? ex0 : ex1) >> (8 * (t & 3))) & 0xFFu];
+              sink.put(en & 0xFFFFFFu, en >> 24);
+            }
           }
         }
       }
     }
-    part[warp * 32 + lane] = bits;
+    sink.finish();
+    my_bits = sink.bits();
+    part[warp * 32 + lane] = my_bits;
+    if (__any_sync(kFull, my_bits > 32 * kPrivWords) && lane == 0) s_over = 1;
   }
   __syncthreads();
 
@@ -470,55 +537,74 @@ __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a)
       s_goff = goff;
       s_err = err ? 1u : 0u;
     }
-  } else if (s_mode == 0) {
-    // Phase D (row warps): pack codewords into the exponent region; raw tiles
-    // are stored straight from the staging area.
-    BitSink sink;
-    sink.begin(reinterpret_cast<uint32_t*>(img + exp_off + kSegTab),
-               s_segstart[(warp / kRowWarpsPerHalf) * 32 + lane] + part[warp * 32 + lane]);
-#pragma unroll 1
-    for (uint32_t row = rb; row < re; ++row) {
-      const uint32_t i0 = row * kRow + col;
-      const uint32_t cnt = full ? 8u : (nt > i0 ? min(8u, nt - i0) : 0u);
-      if (cnt == 0) break;
-      const uint2 e8 = *reinterpret_cast<const uint2*>(exps + i0);
-      uint32_t p0 = 0, p1 = 0, p2 = 0, p3 = 0;
-      if (cnt == 8) {
-        p0 = pair[pair_index_bytes(e8.x, 0, base)];
-        p1 = pair[pair_index_bytes(e8.x, 2, base)];
-        p2 = pair[pair_index_bytes(e8.y, 0, base)];
-        p3 = pair[pair_index_bytes(e8.y, 2, base)];
+  } else if (s_mode == 0 && !s_over) {
+    // Phase D (row warps): move each part from its private buffer to its bit
+    // position in the segment stream.
+    if (my_bits) {
+      const uint32_t S = s_segstart[half * 32 + lane] + part[warp * 32 + lane];
+      const uint32_t sh = S & 31, nw = (my_bits + 31) >> 5, nout = (sh + my_bits + 31) >> 5;
+      const uint32_t* src = priv + warp * (32 * kPrivWords) + lane;
+      uint32_t* dst = region + (S >> 5);
+      uint32_t prev = 0;
+      for (uint32_t j = 0; j < nout; ++j) {
+        const uint32_t cur = j < nw ? src[32 * j] : 0u;
+        const uint32_t v = __funnelshift_l(prev, cur, sh);
+        if (j == 0 || j + 1 == nout) atomicOr(dst + j, v);
+        else dst[j] = v;
+        prev = cur;
       }
-      if (__builtin_expect(cnt == 8 && !((p0 | p1 | p2 | p3) & kPairEsc), 1)) {
-        sink.put(p0 & 0xFFFFFu, p0 >> 26);
-        sink.put(p1 & 0xFFFFFu, p1 >> 26);
-        sink.put(p2 & 0xFFFFFu, p2 >> 26);
-        sink.put(p3 & 0xFFFFFu, p3 >> 26);
-      } else {
+    }
+  } else if (s_mode == 0) {
+    // Phase D, a part overflowed its buffer: re-read the rows and pack in place.
+    BitSink sink;
+    sink.begin(region, s_segstart[half * 32 + lane] + part[warp * 32 + lane]);
+#pragma unroll 1
+    for (uint32_t row = rb; row < rb + kRowsPerWarp; ++row) {
+      const uint32_t i0 = row * kRow + col;
+      const uint32_t cnt = nt > i0 ? min(8u, nt - i0) : 0u;
+      if (cnt == 0) break;
+      uint32_t w[4];
+      load_group(x + i0, cnt, vec, w);
+      uint32_t sm0, sm1, ex0, ex1;
+      split4(w[0], w[1], sm0, ex0);
+      split4(w[2], w[3], sm1, ex1);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          if (t < (int)cnt) {
-            const uint32_t en = tab[((t < 4 ? e8.x : e8.y) >> (8 * (t & 3))) & 0xFFu];
-            sink.put(en & 0xFFFFFFu, en >> 24);
-          }
+      for (int t = 0; t < 8; ++t) {
+        if (t < (int)cnt) {
+          const uint32_t en = tab[((t < 4 ? ex0 : ex1) >> (8 * (t & 3))) & 0xFFu];
+          sink.put(en & 0xFFFFFFu, en >> 24);
         }
       }
     }
     sink.finish();
+  } else {
+    // Phase D, raw tile: re-read the rows and store the exponent bytes.
+#pragma unroll 1
+    for (uint32_t row = rb; row < rb + kRowsPerWarp; ++row) {
+      const uint32_t i0 = row * kRow + col;
+      const uint32_t cnt = nt > i0 ? min(8u, nt - i0) : 0u;
+      if (cnt == 0) break;
+      uint32_t w[4];
+      load_group(x + i0, cnt, vec, w);
+      uint32_t sm0, sm1, ex0, ex1;
+      split4(w[0], w[1], sm0, ex0);
+      split4(w[2], w[3], sm1, ex1);
+      if (cnt == 8) {
+        *reinterpret_cast<uint2*>(img + exp_off + i0) = make_uint2(ex0, ex1);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          if (t < (int)cnt) img[exp_off + i0 + t] = (uint8_t)((t < 4 ? ex0 : ex1) >> (8 * (t & 3)));
+      }
+    }
   }
   fence_proxy_async_smem();
   __syncthreads();
 
-  // Phase E: TMA bulk store of the finished tile: one copy for a coded tile,
-  // image head + staged exponents for a raw tile.  The CTA leaves once shared
-  // memory has been read.
+  // Phase E: one TMA bulk store of the finished tile image.  The CTA leaves
+  // once shared memory has been read.
   if (tid == 0 && !s_err && s_size) {
-    if (s_mode == 0) {
-      bulk_store_issue(a.out + s_goff, img, s_size);
-    } else {
-      bulk_store_issue(a.out + s_goff, img, exp_off);
-      bulk_store_issue(a.out + s_goff + exp_off, exps, sm_pad);
-    }
+    bulk_store_issue(a.out + s_goff, img, s_size);
     bulk_commit_and_wait_read();
   }
 }
