@@ -24,7 +24,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 struct EncLayout {
   uint64_t n_items;
-  uint64_t off_chunks, off_tables, off_item_chunk, off_state, total;
+  uint64_t off_chunks, off_tables, off_items, off_state, total;
 };
 
 EncLayout enc_layout(const uint64_t* ce, uint32_t nc) {
@@ -35,8 +35,8 @@ EncLayout enc_layout(const uint64_t* ce, uint32_t nc) {
   }
   L.off_chunks = sizeof(WsHeader);
   L.off_tables = L.off_chunks + pad256(sizeof(EncChunk) * (uint64_t)nc);
-  L.off_item_chunk = L.off_tables + pad256(4ull * kEncTableWords * nc);
-  L.off_state = L.off_item_chunk + pad256(4 * L.n_items);
+  L.off_items = L.off_tables + pad256(4ull * kEncTableWords * nc);
+  L.off_state = L.off_items + pad256(sizeof(EncItem) * L.n_items);
   L.total = L.off_state + pad256(8 * L.n_items);
   return L;
 }
@@ -155,7 +155,7 @@ zipccl_status zipccl_compress(const uint16_t* d_in, uint64_t n, const uint64_t* 
   sa->in = d_in;
   sa->chunks = reinterpret_cast<EncChunk*>(ws + L.off_chunks);
   sa->tables = reinterpret_cast<uint32_t*>(ws + L.off_tables);
-  sa->item_chunk = reinterpret_cast<uint32_t*>(ws + L.off_item_chunk);
+  sa->items = reinterpret_cast<EncItem*>(ws + L.off_items);
   sa->item_state = reinterpret_cast<uint64_t*>(ws + L.off_state);
   sa->hdr = reinterpret_cast<WsHeader*>(ws);
   for (int r = 0; r < 16; ++r) {
@@ -196,7 +196,7 @@ zipccl_status zipccl_compress(const uint16_t* d_in, uint64_t n, const uint64_t* 
   ea.offsets = d_chunk_offsets;
   ea.chunks = sa->chunks;
   ea.tables = sa->tables;
-  ea.item_chunk = sa->item_chunk;
+  ea.items = sa->items;
   ea.item_state = sa->item_state;
   ea.hdr = sa->hdr;
   ea.n_chunks = n_chunks;

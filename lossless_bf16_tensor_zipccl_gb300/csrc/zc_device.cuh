@@ -29,6 +29,19 @@ __device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// Relaxed 64-bit loads and stores at GPU scope.  The look-back state words
+// and the chunk-start slot each carry their flag and value in one word, and
+// readers use only that word, so no fence is needed around them.
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 __device__ __forceinline__ void set_status(WsHeader* h, uint32_t code) {
   atomicCAS(&h->status, 0u, code);
 }
@@ -92,15 +105,17 @@ __device__ __forceinline__ void bulk_copy_g2s(void* sdst, const void* gsrc, uint
 }
 
 // Wait for phase `parity` of the barrier, giving up after kWaitLimitNs.
+// Each try_wait suspends the thread (up to the hint, 0.5 ms) until the phase
+// completes, so a waiting warp does not take issue slots from working ones.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_addr(bar);
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     uint32_t done;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
         : "=r"(done)
-        : "r"(a), "r"(parity)
+        : "r"(a), "r"(parity), "r"(500000u)
         : "memory");
     if (done) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;

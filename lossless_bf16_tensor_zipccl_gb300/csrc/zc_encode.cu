@@ -122,58 +122,115 @@ __global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ 
   }
   const uint32_t items = ca.n_tiles ? ca.n_tiles : 1u;
   for (uint32_t i = threadIdx.x; i < items; i += blockDim.x) {
-    a.item_chunk[ca.first_item + i] = ci;
+    EncItem r;
+    r.elem0 = ca.elem_start + (uint64_t)i * kTile;
+    r.c = ci;
+    r.k = i;
+    r.nt = ca.n_tiles ? (uint32_t)min((uint64_t)kTile, ca.n - (uint64_t)i * kTile) : 0u;
+    r.base = (uint32_t)base;
+    r.pad[0] = r.pad[1] = 0;
+    a.items[ca.first_item + i] = r;
     a.item_state[ca.first_item + i] = 0;
   }
 }
 
 // ---------------------------------------------------------------- encode
-// One CTA per tile.  Row warps 0..7 own the left half of every row
-// (segments 0..31), row warps 8..15 the right half (segments 32..63), eight
-// rows each; lane l of a row warp in half h works on segment 32 h + l.
-// Warp 16 is the control warp: it lays out the segments, publishes the
-// tile's size, runs the look-back and writes the chunk header while the row
-// warps assemble the exponent region.
+// Persistent CTAs, one per SM, all resident at once (cooperative launch);
+// CTA b takes tiles b, b + G, b + 2G, ... (G CTAs), so every tile's
+// predecessors are processed by running CTAs in the same order.
 //
-// Single pass over the input: a row warp reads its rows once, writes the
-// sign/mantissa bytes into the tile image and packs each lane's codewords
-// into a private word buffer in shared memory as it goes (bit 0 of the part
-// at bit 0 of word 0).  Once every part's length is known, each lane copies
-// its part to its bit position in the segment stream with funnel shifts:
-// words that only this part touches are stored, the two end words are OR-ed.
-// A part longer than its private buffer (a lane with many escapes) sends
-// the tile down a slower path that re-reads its input and packs in place; a
-// raw tile re-reads its input to store the exponent bytes.
+// Row warps 0..7 own the left half of every row (segments 0..31), row warps
+// 8..15 the right half (segments 32..63), eight rows each; lane l of a row
+// warp in half h works on segment 32 h + l.
 //
-// Shared memory: tile image (header | sign/mantissa plane | exponent region)
-// | private part buffers | code tables | per-(row warp, lane) bit counts.
+// Single pass over the input: a row warp reads its rows once (the loads were
+// issued one tile earlier), writes the sign/mantissa bytes into the tile
+// image and packs each lane's codewords into a private word buffer in shared
+// memory (bit 0 of the part at bit 0 of word 0) -- phase A.  The layout warp
+// (warp 16) then places the segments and publishes the tile's size -- phase
+// B; each lane copies its part to its bit position with funnel shifts: words
+// that only this part touches are stored, the two end words are OR-ed --
+// phase D.  A part longer than its private buffer (a lane with many escapes)
+// sends the tile down a slower path that re-reads its input and packs in
+// place; a raw tile re-reads its input to store the exponent bytes.
+//
+// The store warp (warp 17) runs the look-back for the tile's byte offset,
+// writes the chunk header, tile table and chunk offsets, and stores the tile
+// image with one TMA bulk copy -- phases C and E -- up to two tiles behind
+// the row warps: the image is triple-buffered.  Named barriers hand tiles
+// between the roles (i = tile number within the CTA, b = i mod 3):
+//   kBarParts     row warps arrive after phase A; the layout warp waits;
+//   kBarSeg       the layout warp arrives after phase B; row warps wait;
+//   kBarB0 + b    the layout warp arrives after phase B; the store warp waits;
+//   kBarImg0 + b  row warps arrive after phase D; the store warp waits;
+//   kBarFree0 + b the store warp arrives once image b has been read by its
+//                 store; row warps wait before packing tile i + 3 into it.
+// A barrier that a role may reach again before the other role has waited
+// gets one id per buffer, so arrivals of different tiles never mix.
+//
+// Shared memory: 3 tile images (header | sign/mantissa plane | exponent
+// region) | private part buffers | 3 code tables | per-(row warp, lane) bit
+// counts | 3 x per-(row warp, lane) first word of each part.
 constexpr uint32_t kImgBytes = kTileHdr + kTile + kTile;
+constexpr uint32_t kImgBufs = 3;
 constexpr int kRowWarpsPerHalf = 8;
 constexpr int kRowWarps = 2 * kRowWarpsPerHalf;
-constexpr int kCtlWarp = kRowWarps;
-constexpr int kEncThreads = 32 * (kRowWarps + 1);
+constexpr int kLayoutWarp = kRowWarps;
+constexpr int kRowThreads = 32 * kRowWarps;
+constexpr int kEncThreads = 32 * (kRowWarps + 2);
+constexpr uint32_t kBarThreads = kRowThreads + 32;      // row warps + one role warp
 constexpr int kRowsPerWarp = kRows / kRowWarpsPerHalf;   // 8
-constexpr uint32_t kPrivWords = 16;                       // 512 bits per lane part (8 bits per value)
+constexpr uint32_t kPrivWords = 8;                        // 256 bits per lane part (4 bits per value)
 constexpr uint32_t kPrivBytes = kRowWarps * 32 * kPrivWords * 4;
-constexpr uint32_t kEncSmem = kImgBytes + kPrivBytes + kEncTableWords * 4 + kRowWarps * 32 * 4;
+constexpr uint32_t kEncSmem =
+    kImgBufs * kImgBytes + kPrivBytes + kImgBufs * kEncTableWords * 4 + kRowWarps * 32 * 4 + kImgBufs * kRowThreads * 4;
+constexpr uint32_t kBarParts = 1, kBarSeg = 2, kBarB0 = 3, kBarImg0 = 6, kBarFree0 = 9, kBarRows = 12;
+
+__device__ __forceinline__ void bar_arrive(uint32_t id, uint32_t n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_wait(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 // Decoupled look-back over the flat tile list (warp-wide).  Each tile
-// publishes its byte count (aggregate), then its inclusive prefix.  Returns
-// the exclusive prefix; sets err on a timed-out wait or an upstream error.
-__device__ uint64_t lookback(uint64_t* state, uint32_t item, uint32_t lane, bool& err) {
+// publishes its byte count (aggregate), then its inclusive prefix.  One pass
+// reads the 256 nearest unfolded predecessors (8 per lane), folds them up to
+// and including the nearest inclusive prefix, and stops there.  Returns the
+// exclusive prefix; sets err on a timed-out wait or an upstream error.
+constexpr int kLookbackDepth = 8;  // states per lane per pass
+
+__device__ uint64_t lookback(const uint64_t* state, uint32_t item, uint32_t lane, bool& err) {
   uint64_t excl = 0;
-  int64_t pred = (int64_t)item - 1;
+  int64_t pred = (int64_t)item - 1;  // nearest predecessor not folded yet
   uint64_t t0 = 0;
   bool waiting = false;
   while (true) {
-    const int64_t idx = pred - (int64_t)lane;
-    const uint64_t s = idx >= 0 ? ld_acquire_u64(state + idx) : kFlagInc;
-    const uint32_t flag = (uint32_t)(s >> kFlagShift);
-    const uint32_t not_ready = __ballot_sync(kFull, flag == 0);
-    const uint32_t stop = __ballot_sync(kFull, flag >= 2);
-    const uint32_t lim = stop ? (uint32_t)(__ffs(stop) - 1) : 31u;
-    const uint32_t upto = lim == 31 ? kFull : ((2u << lim) - 1u);
-    if (not_ready & upto) {
+    uint64_t s[kLookbackDepth];
+#pragma unroll
+    for (int j = 0; j < kLookbackDepth; ++j) {
+      const int64_t idx = pred - (int64_t)lane - 32 * j;  // position 32 j + lane back from pred
+      s[j] = idx >= 0 ? ld_relaxed_u64(state + idx) : kFlagInc;
+    }
+    // nearest stop (inclusive prefix or error): group sj, lane sl
+    uint32_t sj = kLookbackDepth, sl = 31;
+#pragma unroll
+    for (int j = kLookbackDepth - 1; j >= 0; --j) {
+      const uint32_t b = __ballot_sync(kFull, (s[j] >> kFlagShift) >= 2);
+      if (b) {
+        sj = j;
+        sl = __ffs(b) - 1;
+      }
+    }
+    const uint32_t upto_sl = sl == 31 ? kFull : ((2u << sl) - 1u);
+    bool not_ready = false, upstream_err = false;
+#pragma unroll
+    for (int j = 0; j < kLookbackDepth; ++j) {
+      const uint32_t m = (uint32_t)j < sj ? kFull : ((uint32_t)j == sj ? upto_sl : 0u);
+      not_ready |= (__ballot_sync(kFull, (s[j] >> kFlagShift) == 0) & m) != 0;
+      upstream_err |= (__ballot_sync(kFull, (s[j] >> kFlagShift) == 3) & m) != 0;
+    }
+    if (not_ready) {
       // lane 0's clock decides for the whole warp, so all lanes leave together
       const uint64_t now = globaltimer_ns();
       if (!waiting) {
@@ -187,16 +244,19 @@ __device__ uint64_t lookback(uint64_t* state, uint32_t item, uint32_t lane, bool
       __nanosleep(64);
       continue;
     }
-    if (__ballot_sync(kFull, flag == 3) & upto) {
+    if (upstream_err) {
       err = true;
       return 0;
     }
-    uint64_t v = lane <= lim ? (s & kValMask) : 0;
+    uint64_t v = 0;
+#pragma unroll
+    for (int j = 0; j < kLookbackDepth; ++j)
+      if ((uint32_t)j < sj || ((uint32_t)j == sj && lane <= sl)) v += s[j] & kValMask;
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
     excl += v;
-    if (stop) return excl;
-    pred -= 32;
+    if (sj < (uint32_t)kLookbackDepth) return excl;
+    pred -= 32 * kLookbackDepth;
   }
 }
 
@@ -323,241 +383,193 @@ __device__ __forceinline__ void load_group(const uint16_t* x, uint32_t cnt, bool
   }
 }
 
-__global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* img = smem;
-  uint32_t* priv = reinterpret_cast<uint32_t*>(smem + kImgBytes);                    // [warp][word][lane]
-  uint32_t* tab = reinterpret_cast<uint32_t*>(smem + kImgBytes + kPrivBytes);       // per exponent
-  uint32_t* pair = tab + 256;                                                        // per symbol pair
-  uint32_t* part = tab + kEncTableWords;  // [row warp][lane] bits, then bit offsets
-  __shared__ uint32_t s_item, s_mode, s_err, s_size, s_over;
-  __shared__ uint32_t s_segstart[kSegs];
-  __shared__ unsigned long long s_goff;
+// Shared state of the encode CTA.
+struct EncShared {
+  uint8_t* img[kImgBufs];
+  uint32_t* priv;  // [warp][word][lane]
+  uint32_t* tabs;  // kImgBufs x kEncTableWords
+  uint32_t* part;  // [row warp][lane] bits, then bit offsets
+  uint32_t* first;     // per buffer: [row warp][lane] word 0 of each part
+  uint32_t* segstart;  // [kSegs]
+  uint32_t* mode;      // per buffer: 0 coded, 1 coded with an overflowed part, 2 raw
+  uint32_t* over;      // per buffer: a part overflowed its private buffer
+  uint32_t* size;      // per buffer: tile bytes
+};
 
-  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) {
-    s_item = atomicAdd(&a.hdr->counter, 1u);  // tiles start in claim order
-    s_err = 0;
-    s_over = 0;
+__device__ __forceinline__ EncItem load_item(const EncodeArgs& a, uint32_t t) {
+  EncItem r;
+  if (t < a.n_items) {
+    r = a.items[t];
+  } else {
+    r.elem0 = 0;
+    r.c = r.k = r.nt = r.base = 0;
+    r.pad[0] = r.pad[1] = 0;
   }
-  __syncthreads();
-  const uint32_t item = s_item;
-  const uint32_t c = a.item_chunk[item];
-  const EncChunk ci = a.chunks[c];
-  const uint32_t k = item - ci.first_item;
-  const uint32_t nt = ci.n_tiles ? (uint32_t)min((uint64_t)kTile, ci.n - (uint64_t)k * kTile) : 0u;
-  const uint64_t elem0 = ci.elem_start + (uint64_t)k * kTile;
-  const uint16_t* x = a.in + elem0;
-  const bool vec = (elem0 & 7) == 0;
-  const uint32_t base = ci.base;
-  const uint32_t base4 = base * 0x01010101u;
+  return r;
+}
+
+__device__ __forceinline__ bool full_tile(const EncItem& r) { return r.nt == kTile && (r.elem0 & 7) == 0; }
+
+// Row warps, one tile: phases A and D.  v holds this tile's rows rb..rb+7
+// (full tiles); each row's registers are refilled with the next tile's row
+// as soon as they are consumed, so the loads run a whole tile ahead.
+__device__ __forceinline__ void row_tile(const EncodeArgs& a, const EncShared& S, uint32_t buf, const EncItem& rec,
+                                         uint4 (&v)[kRowsPerWarp], const EncItem& fut, bool fut_ok) {
+  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t half = warp / kRowWarpsPerHalf;
+  const uint32_t rb = (warp % kRowWarpsPerHalf) * kRowsPerWarp;
+  const uint32_t col = half * kHalf + lane * kLaneElems;
+  uint8_t* img = S.img[buf];
+  const uint32_t* tab = S.tabs + buf * kEncTableWords;  // per exponent
+  const uint32_t* pair = tab + 256;                    // per symbol pair
+  const uint32_t nt = rec.nt;
+  const uint16_t* x = a.in + rec.elem0;
+  const bool vec = (rec.elem0 & 7) == 0;
+  const bool full = nt == kTile && vec;
+  const uint32_t base4 = rec.base * 0x01010101u;
   const uint32_t sm_pad = (uint32_t)pad16(nt);
   const uint32_t exp_off = kTileHdr + sm_pad;
   uint32_t* region = reinterpret_cast<uint32_t*>(img + exp_off + kSegTab);  // coded payload words
 
-  // Tables from the select kernel; zero the padding of the sign/mantissa
-  // plane and the exponent area (the end words of each part are OR-ed in).
-  for (uint32_t i = tid; i < kEncTableWords; i += kEncThreads) tab[i] = __ldg(a.tables + (size_t)c * kEncTableWords + i);
-  if (tid < 16 && nt + tid < sm_pad) img[kTileHdr + nt + tid] = 0;
-  for (uint32_t o = tid * 16; o < sm_pad; o += kEncThreads * 16)
-    *reinterpret_cast<uint4*>(img + exp_off + o) = make_uint4(0, 0, 0, 0);
-  __syncthreads();
+  // Other than full tiles: zero the padding of the sign/mantissa plane and
+  // the exponent area (the end words of each part are OR-ed in).
+  if (!full) {
+    if (tid < 16 && nt + tid < sm_pad) img[kTileHdr + nt + tid] = 0;
+    for (uint32_t o = tid * 16; o < sm_pad; o += kRowThreads * 16)
+      *reinterpret_cast<uint4*>(img + exp_off + o) = make_uint4(0, 0, 0, 0);
+  }
 
-  const uint32_t half = warp < kRowWarps ? warp / kRowWarpsPerHalf : 0u;
-  const uint32_t rb = warp < kRowWarps ? (warp % kRowWarpsPerHalf) * kRowsPerWarp : kRows;
-  const uint32_t col = half * kHalf + lane * kLaneElems;
-  const bool full = nt == kTile && vec;
-
-  // Phase A (row warps): read each row group once; sign/mantissa bytes to
-  // the image, codewords to the private buffer.
-  uint32_t my_bits = 0;
-  if (warp < kRowWarps) {
-    PrivSink sink;
-    sink.begin(priv + warp * (32 * kPrivWords) + lane);
-    if (full) {
-      uint4 v[kRowsPerWarp];
+  // Phase A: sign/mantissa bytes to the image, codewords to the private buffer.
+  PrivSink sink;
+  sink.begin(S.priv + warp * (32 * kPrivWords) + lane);
+  const bool fut_full = fut_ok && full_tile(fut);
+  const uint16_t* xf = a.in + fut.elem0 + rb * kRow + col;
+  if (full) {
 #pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) v[r] = ld_stream_v4(x + (rb + r) * kRow + col);
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) {
-        uint32_t sm0, sm1, ex0, ex1;
-        split4(v[r].x, v[r].y, sm0, ex0);
-        split4(v[r].z, v[r].w, sm1, ex1);
-        *reinterpret_cast<uint2*>(img + kTileHdr + (rb + r) * kRow + col) = make_uint2(sm0, sm1);
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      uint32_t sm0, sm1, ex0, ex1;
+      split4(v[r].x, v[r].y, sm0, ex0);
+      split4(v[r].z, v[r].w, sm1, ex1);
+      if (fut_full) v[r] = ld_stream_v4(xf + r * kRow);
+      *reinterpret_cast<uint2*>(img + kTileHdr + (rb + r) * kRow + col) = make_uint2(sm0, sm1);
+      pack_row8(sink, ex0, ex1, base4, pair, tab);
+    }
+  } else {
+    for (uint32_t row = rb; row < rb + kRowsPerWarp; ++row) {
+      const uint32_t i0 = row * kRow + col;
+      const uint32_t cnt = nt > i0 ? min(8u, nt - i0) : 0u;
+      if (cnt == 0) break;
+      uint32_t w[4];
+      load_group(x + i0, cnt, vec, w);
+      uint32_t sm0, sm1, ex0, ex1;
+      split4(w[0], w[1], sm0, ex0);
+      split4(w[2], w[3], sm1, ex1);
+      if (cnt == 8) {
+        *reinterpret_cast<uint2*>(img + kTileHdr + i0) = make_uint2(sm0, sm1);
         pack_row8(sink, ex0, ex1, base4, pair, tab);
-      }
-    } else {
-      for (uint32_t row = rb; row < rb + kRowsPerWarp; ++row) {
-        const uint32_t i0 = row * kRow + col;
-        const uint32_t cnt = nt > i0 ? min(8u, nt - i0) : 0u;
-        if (cnt == 0) break;
-        uint32_t w[4];
-        load_group(x + i0, cnt, vec, w);
-        uint32_t sm0, sm1, ex0, ex1;
-        split4(w[0], w[1], sm0, ex0);
-        split4(w[2], w[3], sm1, ex1);
-        if (cnt == 8) {
-          *reinterpret_cast<uint2*>(img + kTileHdr + i0) = make_uint2(sm0, sm1);
-          pack_row8(sink, ex0, ex1, base4, pair, tab);
-        } else {
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            if (t < (int)cnt) {
-              img[kTileHdr + i0 + t] = (uint8_t)((t < 4 ? sm0 : sm1) >> (8 * (t & 3)));
-              const uint32_t en = tab[((t < 4 ? ex0 : ex1) >> (8 * (t & 3))) & 0xFFu];
-              sink.put(en & 0xFFFFFFu, en >> 24);
-            }
-          }
-        }
-      }
-    }
-    sink.finish();
-    my_bits = sink.bits();
-    part[warp * 32 + lane] = my_bits;
-    if (__any_sync(kFull, my_bits > 32 * kPrivWords) && lane == 0) s_over = 1;
-  }
-  __syncthreads();
-
-  // Phase B (control warp): bit offset of each row warp's part inside its
-  // segment, bit-granular segment starts, raw/coded choice, publish the
-  // aggregate.  Lane l handles segments l and 32 + l.
-  uint64_t agg = 0;
-  if (warp == kCtlWarp) {
-    uint32_t seg[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t off = 0;
-#pragma unroll
-      for (int w = 0; w < kRowWarpsPerHalf; ++w) {
-        const uint32_t i = (h * kRowWarpsPerHalf + w) * 32 + lane;
-        const uint32_t v = part[i];
-        part[i] = off;
-        off += v;
-      }
-      seg[h] = off;
-    }
-    uint32_t start0 = seg[0], start1 = seg[1];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y0 = __shfl_up_sync(kFull, start0, o), y1 = __shfl_up_sync(kFull, start1, o);
-      if (lane >= (uint32_t)o) {
-        start0 += y0;
-        start1 += y1;
-      }
-    }
-    const uint32_t total0 = __shfl_sync(kFull, start0, 31), total1 = __shfl_sync(kFull, start1, 31);
-    s_segstart[lane] = start0 - seg[0];
-    s_segstart[32 + lane] = total0 + start1 - seg[1];
-    const uint32_t words = (total0 + total1 + 31) >> 5;
-    const bool coded = kSegTab + 4ull * words < nt;
-    const uint32_t exp_bytes = coded ? kSegTab + 4 * words : nt;
-    if (coded) {
-      reinterpret_cast<uint16_t*>(img + exp_off)[lane] = (uint16_t)seg[0];
-      reinterpret_cast<uint16_t*>(img + exp_off)[32 + lane] = (uint16_t)seg[1];
-    }
-    const uint32_t size = nt ? (uint32_t)(kTileHdr + sm_pad + pad16(exp_bytes)) : 0u;
-    agg = size + (k == 0 ? chunk_hdr_bytes(ci.n_tiles) : 0);
-    if (lane == 0) {
-      s_mode = coded ? 0u : 1u;
-      s_size = size;
-      *reinterpret_cast<uint4*>(img) = make_uint4(coded ? 0u : 1u, nt, exp_bytes, 0u);
-      st_release_u64(a.item_state + item, (item == 0 ? kFlagInc : kFlagAgg) | agg);
-    }
-  }
-  __syncthreads();
-
-  if (warp == kCtlWarp) {
-    // Phase C (control warp): look-back for this tile's byte offset, chunk
-    // header / tile table / chunk offsets.
-    bool err = false;
-    uint64_t excl = item == 0 ? 0 : lookback(a.item_state, item, lane, err);
-    if (item != 0 && lane == 0) st_release_u64(a.item_state + item, err ? kFlagErr : (kFlagInc | (excl + agg)));
-    uint64_t cs = 0;
-    if (!err) {
-      if (k == 0) {
-        cs = excl;
-        if (lane == 0) {
-          st_release_u64(&a.chunks[c].start_slot, kSlotValid | cs);
-          a.offsets[c] = cs;
-        }
       } else {
-        // lane 0 waits for the chunk's first tile to publish the chunk start
-        uint64_t v = 0;
-        uint32_t to = 0;
-        if (lane == 0) {
-          const uint64_t t0 = globaltimer_ns();
-          v = ld_acquire_u64(&a.chunks[c].start_slot);
-          while (!(v & kSlotValid)) {
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
-              to = 1;
-              break;
-            }
-            __nanosleep(64);
-            v = ld_acquire_u64(&a.chunks[c].start_slot);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          if (t < (int)cnt) {
+            img[kTileHdr + i0 + t] = (uint8_t)((t < 4 ? sm0 : sm1) >> (8 * (t & 3)));
+            const uint32_t en = tab[((t < 4 ? ex0 : ex1) >> (8 * (t & 3))) & 0xFFu];
+            sink.put(en & 0xFFFFFFu, en >> 24);
           }
         }
-        v = __shfl_sync(kFull, v, 0);
-        err = __shfl_sync(kFull, to, 0) != 0;
-        cs = v & ~kSlotValid;
       }
     }
-    const uint64_t hdr = chunk_hdr_bytes(ci.n_tiles);
-    const uint64_t goff = excl + (k == 0 ? hdr : 0);
-    if (!err && (goff + s_size > a.cap || cs + hdr > a.cap)) {
-      err = true;
-      if (lane == 0) set_status(a.hdr, kStCapacity);
-    } else if (err && lane == 0) {
-      set_status(a.hdr, kStTimeout);
-    }
-    if (!err) {
-      uint8_t* cp = a.out + cs;
-      if (k == 0) {
-        if (lane < 8) {
-          uint32_t v;
-          switch (lane) {
-            case 0: v = kMagic; break;
-            case 1: v = kVersion | (kTileLog2 << 16) | (kSegLog2 << 24); break;
-            case 2: v = (uint32_t)ci.n; break;
-            case 3: v = (uint32_t)(ci.n >> 32); break;
-            case 4: v = ci.n_tiles; break;
-            case 5: v = base | ((uint32_t)(uint16_t)(int16_t)ci.q << 16); break;
-            case 6: v = (uint32_t)ci.lens; break;
-            default: v = (uint32_t)(ci.lens >> 32); break;
-          }
-          reinterpret_cast<uint32_t*>(cp)[lane] = v;
-        }
-        // zero the tail of the tile table up to 16 bytes
-        const uint32_t tail0 = 4 * ci.n_tiles, tail1 = (uint32_t)pad16(4ull * ci.n_tiles);
-        if (tail0 + 4 * lane < tail1) reinterpret_cast<uint32_t*>(cp + kChunkHdr + tail0)[lane] = 0;
+  }
+  sink.finish();
+  const uint32_t my_bits = sink.bits();
+  S.part[warp * 32 + lane] = my_bits;
+  // word 0 of the part, for the part before it in the stream (phase D);
+  // kept per buffer because this warp's private words are reused by the
+  // next tile before every warp is past phase D
+  S.first[buf * kRowThreads + warp * 32 + lane] = S.priv[warp * (32 * kPrivWords) + lane];
+  if (__any_sync(kFull, my_bits > 32 * kPrivWords) && lane == 0) S.over[buf] = 1;
+  if (!full && fut_full) {
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) v[r] = ld_stream_v4(xf + r * kRow);
+  }
+  bar_arrive(kBarParts, kBarThreads);
+  bar_wait(kBarSeg, kBarThreads);
+
+  const uint32_t mode = S.mode[buf];
+  if (mode == 0 && full) {
+    // Phase D, full tile: every part holds >= 64 bits (64 codewords of >= 1
+    // bit), so a word of the stream holds bits of at most two parts.  Each
+    // word is written once, by the part that holds its first bit; where the
+    // part ends inside its last word, the rest of that word is the start of
+    // the next part (its private word 0).
+    const uint32_t w8 = warp % kRowWarpsPerHalf;
+    uint32_t nwarp = warp + 1, nlane = lane;  // the next part in stream order
+    bool has_next = true;
+    if (w8 + 1 == kRowWarpsPerHalf) {
+      nwarp = half * kRowWarpsPerHalf;
+      nlane = lane + 1;
+      if (lane == 31) {
+        nwarp = kRowWarpsPerHalf;
+        nlane = 0;
+        has_next = half == 0;
       }
-      if (nt && lane == 0) reinterpret_cast<uint32_t*>(cp + kChunkHdr)[k] = (uint32_t)(goff - cs);
-      if (item == a.n_items - 1 && lane == 0) a.offsets[a.n_chunks] = excl + agg;
     }
-    if (lane == 0) {
-      s_goff = goff;
-      s_err = err ? 1u : 0u;
+    const uint32_t next_w0 = has_next ? S.first[buf * kRowThreads + nwarp * 32 + nlane] : 0u;
+    const uint32_t St = S.segstart[half * 32 + lane] + S.part[warp * 32 + lane];
+    const uint32_t sh = St & 31, nw = (my_bits + 31) >> 5, e = (St + my_bits) & 31;
+    const uint32_t x0 = (St + 31) >> 5, x1 = (St + my_bits - 1) >> 5;
+    const uint32_t* src = S.priv + warp * (32 * kPrivWords) + lane;
+    uint32_t pw[kPrivWords + 1];
+#pragma unroll
+    for (uint32_t j = 0; j < kPrivWords; ++j) pw[j] = j < nw ? src[32 * j] : 0u;
+    pw[kPrivWords] = 0;
+#pragma unroll
+    for (uint32_t j = 0; j < kPrivWords; ++j) {
+      const uint32_t x = x0 + j;
+      if (x <= x1) {
+        uint32_t w = sh ? __funnelshift_r(pw[j], pw[j + 1], 32 - sh) : pw[j];
+        if (x == x1 && e) w |= next_w0 << e;
+        region[x] = w;
+      }
     }
-  } else if (s_mode == 0 && !s_over) {
-    // Phase D (row warps): move each part from its private buffer to its bit
-    // position in the segment stream.
+    if (!has_next) {
+      // the stream's last word: zero the padding words up to 16 bytes
+      const uint32_t pend = ((kSegTab / 4 + x1 + 1 + 3) & ~3u) - kSegTab / 4;
+      for (uint32_t x = x1 + 1; x < pend; ++x) region[x] = 0;
+    }
+  } else if (mode == 0) {
+    // Phase D: move each part from its private buffer to its bit position
+    // in the segment stream.
     if (my_bits) {
-      const uint32_t S = s_segstart[half * 32 + lane] + part[warp * 32 + lane];
-      const uint32_t sh = S & 31, nw = (my_bits + 31) >> 5, nout = (sh + my_bits + 31) >> 5;
-      const uint32_t* src = priv + warp * (32 * kPrivWords) + lane;
-      uint32_t* dst = region + (S >> 5);
+      const uint32_t St = S.segstart[half * 32 + lane] + S.part[warp * 32 + lane];
+      const uint32_t sh = St & 31, nw = (my_bits + 31) >> 5, nout = (sh + my_bits + 31) >> 5;
+      const uint32_t* src = S.priv + warp * (32 * kPrivWords) + lane;
+      uint32_t* dst = region + (St >> 5);
+      uint32_t pw[kPrivWords];
+#pragma unroll
+      for (uint32_t j = 0; j < kPrivWords; ++j) pw[j] = j < nw ? src[32 * j] : 0u;
       uint32_t prev = 0;
-      for (uint32_t j = 0; j < nout; ++j) {
-        const uint32_t cur = j < nw ? src[32 * j] : 0u;
-        const uint32_t v = __funnelshift_l(prev, cur, sh);
-        if (j == 0 || j + 1 == nout) atomicOr(dst + j, v);
-        else dst[j] = v;
+#pragma unroll
+      for (uint32_t j = 0; j <= kPrivWords; ++j) {
+        const uint32_t cur = j < kPrivWords ? pw[j] : 0u;
+        const uint32_t w = __funnelshift_l(prev, cur, sh);
+        if (j < nout) {
+          if (j == 0 || j + 1 == nout) atomicOr(dst + j, w);
+          else dst[j] = w;
+        }
         prev = cur;
       }
     }
-  } else if (s_mode == 0) {
-    // Phase D, a part overflowed its buffer: re-read the rows and pack in place.
-    BitSink sink;
-    sink.begin(region, s_segstart[half * 32 + lane] + part[warp * 32 + lane]);
+  } else if (mode == 1) {
+    // Phase D, a part overflowed its buffer: re-read the rows and pack in
+    // place (boundary words are OR-ed, so full tiles zero the payload area
+    // first; the segment table in front of it is already written).
+    if (full) {
+      for (uint32_t o = kSegTab + tid * 16; o < sm_pad; o += kRowThreads * 16)
+        *reinterpret_cast<uint4*>(img + exp_off + o) = make_uint4(0, 0, 0, 0);
+      bar_wait(kBarRows, kRowThreads);
+    }
+    BitSink bs;
+    bs.begin(region, S.segstart[half * 32 + lane] + S.part[warp * 32 + lane]);
 #pragma unroll 1
     for (uint32_t row = rb; row < rb + kRowsPerWarp; ++row) {
       const uint32_t i0 = row * kRow + col;
@@ -572,11 +584,11 @@ __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a)
       for (int t = 0; t < 8; ++t) {
         if (t < (int)cnt) {
           const uint32_t en = tab[((t < 4 ? ex0 : ex1) >> (8 * (t & 3))) & 0xFFu];
-          sink.put(en & 0xFFFFFFu, en >> 24);
+          bs.put(en & 0xFFFFFFu, en >> 24);
         }
       }
     }
-    sink.finish();
+    bs.finish();
   } else {
     // Phase D, raw tile: re-read the rows and store the exponent bytes.
 #pragma unroll 1
@@ -599,13 +611,243 @@ __global__ void __launch_bounds__(kEncThreads, 2) zc_encode_kernel(EncodeArgs a)
     }
   }
   fence_proxy_async_smem();
-  __syncthreads();
+  bar_arrive(kBarImg0 + buf, kBarThreads);
+}
 
-  // Phase E: one TMA bulk store of the finished tile image.  The CTA leaves
-  // once shared memory has been read.
-  if (tid == 0 && !s_err && s_size) {
-    bulk_store_issue(a.out + s_goff, img, s_size);
+// Layout warp, one tile: phase B.  Also stages the next tile's code tables.
+__device__ __forceinline__ void layout_tile(const EncodeArgs& a, const EncShared& S, uint32_t buf, uint32_t item,
+                                            uint32_t next) {
+  const uint32_t lane = threadIdx.x & 31;
+  const EncItem rec = a.items[item];
+  uint8_t* img = S.img[buf];
+  const uint32_t nt = rec.nt;
+  const uint32_t sm_pad = (uint32_t)pad16(nt);
+  const uint32_t exp_off = kTileHdr + sm_pad;
+  const uint32_t hdr = (uint32_t)chunk_hdr_bytes(a.chunks[rec.c].n_tiles);
+  // the next tile's code tables, staged in registers until the row warps are past this tile
+  uint4 nt4[kEncTableWords / 128];
+  const bool has_next = next < a.n_items;
+  if (has_next) {
+    const uint32_t cn = __ldg(&a.items[next].c);
+    const uint4* src = reinterpret_cast<const uint4*>(a.tables + (size_t)cn * kEncTableWords);
+#pragma unroll
+    for (uint32_t i = 0; i < kEncTableWords / 128; ++i) nt4[i] = __ldg(src + lane + 32 * i);
+  }
+
+  bar_wait(kBarParts, kBarThreads);
+  // Bit offset of each row warp's part inside its segment, bit-granular
+  // segment starts, raw/coded choice, publish the aggregate.  Lane l
+  // handles segments l and 32 + l.
+  uint32_t seg[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t pv[kRowWarpsPerHalf];
+#pragma unroll
+    for (int w = 0; w < kRowWarpsPerHalf; ++w) pv[w] = S.part[(h * kRowWarpsPerHalf + w) * 32 + lane];
+    uint32_t off = 0;
+#pragma unroll
+    for (int w = 0; w < kRowWarpsPerHalf; ++w) {
+      S.part[(h * kRowWarpsPerHalf + w) * 32 + lane] = off;
+      off += pv[w];
+    }
+    seg[h] = off;
+  }
+  uint32_t start0 = seg[0], start1 = seg[1];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y0 = __shfl_up_sync(kFull, start0, o), y1 = __shfl_up_sync(kFull, start1, o);
+    if (lane >= (uint32_t)o) {
+      start0 += y0;
+      start1 += y1;
+    }
+  }
+  const uint32_t total0 = __shfl_sync(kFull, start0, 31), total1 = __shfl_sync(kFull, start1, 31);
+  S.segstart[lane] = start0 - seg[0];
+  S.segstart[32 + lane] = total0 + start1 - seg[1];
+  const uint32_t words = (total0 + total1 + 31) >> 5;
+  const bool coded = kSegTab + 4ull * words < nt;
+  const uint32_t exp_bytes = coded ? kSegTab + 4 * words : nt;
+  if (coded) {
+    reinterpret_cast<uint16_t*>(img + exp_off)[lane] = (uint16_t)seg[0];
+    reinterpret_cast<uint16_t*>(img + exp_off)[32 + lane] = (uint16_t)seg[1];
+  }
+  const uint32_t size = nt ? (uint32_t)(kTileHdr + sm_pad + pad16(exp_bytes)) : 0u;
+  const uint64_t agg = size + (rec.k == 0 ? hdr : 0u);
+  if (lane == 0) {
+    S.mode[buf] = coded ? (S.over[buf] ? 1u : 0u) : 2u;
+    S.over[buf] = 0;
+    S.size[buf] = size;
+    *reinterpret_cast<uint4*>(img) = make_uint4(coded ? 0u : 1u, nt, exp_bytes, 0u);
+  }
+  if (has_next) {
+    uint4* dst = reinterpret_cast<uint4*>(S.tabs + ((buf + 1) % kImgBufs) * kEncTableWords);
+#pragma unroll
+    for (uint32_t i = 0; i < kEncTableWords / 128; ++i) dst[lane + 32 * i] = nt4[i];
+  }
+  // Header and segment table are read by the TMA store.  The fence comes
+  // before the aggregate's global store so that it does not wait for it.
+  fence_proxy_async_smem();
+  __syncwarp();
+  bar_arrive(kBarSeg, kBarThreads);
+  if (lane == 0) st_relaxed_u64(a.item_state + item, (item == 0 ? kFlagInc : kFlagAgg) | agg);
+  bar_arrive(kBarB0 + buf, 64);
+}
+
+// Store warp, one tile: phases C and E.  `reuse`: the row warps will pack a
+// later tile into this tile's image, so announce when its store has read it.
+__device__ __forceinline__ void store_tile(const EncodeArgs& a, const EncShared& S, uint32_t buf, uint32_t item,
+                                           const EncItem& rec, const EncChunk& ci, bool reuse) {
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t c = rec.c, k = rec.k, nt = rec.nt;
+  const uint64_t hdr = chunk_hdr_bytes(ci.n_tiles);
+  bar_wait(kBarB0 + buf, 64);
+  const uint32_t size = S.size[buf];
+  const uint64_t agg = size + (k == 0 ? hdr : 0);
+
+  // Phase C: look-back for this tile's byte offset, chunk header / tile
+  // table / chunk offsets.
+  bool err = false;
+  const uint64_t excl = item == 0 ? 0 : lookback(a.item_state, item, lane, err);
+  if (item != 0 && lane == 0) st_relaxed_u64(a.item_state + item, err ? kFlagErr : (kFlagInc | (excl + agg)));
+  uint64_t cs = 0;
+  if (!err) {
+    if (k == 0) {
+      cs = excl;
+      if (lane == 0) {
+        st_relaxed_u64(&a.chunks[c].start_slot, kSlotValid | cs);
+        a.offsets[c] = cs;
+      }
+    } else {
+      // lane 0 waits for the chunk's first tile to publish the chunk start
+      uint64_t v = 0;
+      uint32_t to = 0;
+      if (lane == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        v = ld_relaxed_u64(&a.chunks[c].start_slot);
+        while (!(v & kSlotValid)) {
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            to = 1;
+            break;
+          }
+          __nanosleep(64);
+          v = ld_relaxed_u64(&a.chunks[c].start_slot);
+        }
+      }
+      v = __shfl_sync(kFull, v, 0);
+      err = __shfl_sync(kFull, to, 0) != 0;
+      cs = v & ~kSlotValid;
+    }
+  }
+  const uint64_t goff = excl + (k == 0 ? hdr : 0);
+  if (!err && (goff + size > a.cap || cs + hdr > a.cap)) {
+    err = true;
+    if (lane == 0) set_status(a.hdr, kStCapacity);
+  } else if (err && lane == 0) {
+    set_status(a.hdr, kStTimeout);
+  }
+  if (!err) {
+    uint8_t* cp = a.out + cs;
+    if (k == 0) {
+      if (lane < 8) {
+        uint32_t v;
+        switch (lane) {
+          case 0: v = kMagic; break;
+          case 1: v = kVersion | (kTileLog2 << 16) | (kSegLog2 << 24); break;
+          case 2: v = (uint32_t)ci.n; break;
+          case 3: v = (uint32_t)(ci.n >> 32); break;
+          case 4: v = ci.n_tiles; break;
+          case 5: v = ci.base | ((uint32_t)(uint16_t)(int16_t)ci.q << 16); break;
+          case 6: v = (uint32_t)ci.lens; break;
+          default: v = (uint32_t)(ci.lens >> 32); break;
+        }
+        reinterpret_cast<uint32_t*>(cp)[lane] = v;
+      }
+      // zero the tail of the tile table up to 16 bytes
+      const uint32_t tail0 = 4 * ci.n_tiles, tail1 = (uint32_t)pad16(4ull * ci.n_tiles);
+      if (tail0 + 4 * lane < tail1) reinterpret_cast<uint32_t*>(cp + kChunkHdr + tail0)[lane] = 0;
+    }
+    if (nt && lane == 0) reinterpret_cast<uint32_t*>(cp + kChunkHdr)[k] = (uint32_t)(goff - cs);
+    if (item == a.n_items - 1 && lane == 0) a.offsets[a.n_chunks] = excl + agg;
+  }
+
+  bar_wait(kBarImg0 + buf, kBarThreads);
+  // Phase E: one TMA bulk store of the finished tile image.
+  if (lane == 0 && !err && size) {
+    bulk_store_issue(a.out + goff, S.img[buf], size);
     bulk_commit_and_wait_read();
+  }
+  __syncwarp();
+  if (reuse) bar_arrive(kBarFree0 + buf, kBarThreads);
+}
+
+__global__ void __launch_bounds__(kEncThreads, 1) zc_encode_kernel(EncodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint32_t s_segstart[kSegs], s_mode[kImgBufs], s_over[kImgBufs], s_size[kImgBufs];
+  EncShared S;
+#pragma unroll
+  for (uint32_t i = 0; i < kImgBufs; ++i) S.img[i] = smem + i * kImgBytes;
+  S.priv = reinterpret_cast<uint32_t*>(smem + kImgBufs * kImgBytes);
+  S.tabs = reinterpret_cast<uint32_t*>(smem + kImgBufs * kImgBytes + kPrivBytes);
+  S.part = S.tabs + kImgBufs * kEncTableWords;
+  S.first = S.part + kRowThreads;
+  S.segstart = s_segstart;
+  S.mode = s_mode;
+  S.over = s_over;
+  S.size = s_size;
+
+  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t G = gridDim.x;
+  const uint32_t t0 = blockIdx.x;
+  const uint32_t count = (a.n_items - t0 + G - 1) / G;  // tiles of this CTA
+
+  // Prologue: the first tile's tables.
+  {
+    const uint32_t c0 = a.items[t0].c;
+    for (uint32_t i = tid; i < kEncTableWords; i += kEncThreads) S.tabs[i] = __ldg(a.tables + (size_t)c0 * kEncTableWords + i);
+    if (tid < kImgBufs) s_over[tid] = 0;
+  }
+  if (warp < kRowWarps) {
+    const uint32_t half = warp / kRowWarpsPerHalf;
+    const uint32_t rb = (warp % kRowWarpsPerHalf) * kRowsPerWarp;
+    const uint32_t col = half * kHalf + lane * kLaneElems;
+    uint4 v[kRowsPerWarp];
+    EncItem rec = load_item(a, t0), nx = load_item(a, t0 + G);
+    if (full_tile(rec)) {
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r) v[r] = ld_stream_v4(a.in + rec.elem0 + (rb + r) * kRow + col);
+    }
+    __syncthreads();
+    uint32_t buf = 0;
+    for (uint32_t i = 0; i < count; ++i) {
+      const uint32_t t = t0 + i * G;
+      const EncItem nx2 = load_item(a, t + 2 * G);  // records run two tiles ahead
+      if (i >= kImgBufs) bar_wait(kBarFree0 + buf, kBarThreads);
+      row_tile(a, S, buf, rec, v, nx, t + G < a.n_items);
+      rec = nx;
+      nx = nx2;
+      buf = buf + 1 == kImgBufs ? 0 : buf + 1;
+    }
+  } else if (warp == kLayoutWarp) {
+    __syncthreads();
+    uint32_t buf = 0;
+    for (uint32_t i = 0; i < count; ++i) {
+      const uint32_t t = t0 + i * G;
+      layout_tile(a, S, buf, t, t + G);
+      buf = buf + 1 == kImgBufs ? 0 : buf + 1;
+    }
+  } else {
+    __syncthreads();
+    // records are loaded one tile ahead
+    EncItem rec = load_item(a, t0);
+    EncChunk ch = a.chunks[rec.c];
+    for (uint32_t i = 0; i < count; ++i) {
+      const uint32_t t = t0 + i * G;
+      const EncItem rn = load_item(a, t + G);
+      const EncChunk chn = a.chunks[rn.c];
+      store_tile(a, S, i % kImgBufs, t, rec, ch, i + kImgBufs < count);
+      rec = rn;
+      ch = chn;
+    }
   }
 }
 
@@ -616,19 +858,30 @@ cudaError_t launch_select(const SelectArgs& args, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-static int g_enc_attr_done[64];
+static int g_enc_ctas[64];  // co-resident encode CTAs per device (0: not set up)
 
 cudaError_t launch_encode(const EncodeArgs& args, uint32_t n_items, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && !g_enc_attr_done[dev]) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!g_enc_ctas[dev]) {
     e = cudaFuncSetAttribute(zc_encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEncSmem);
     if (e != cudaSuccess) return e;
-    g_enc_attr_done[dev] = 1;
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, zc_encode_kernel, kEncThreads, kEncSmem);
+    if (e != cudaSuccess) return e;
+    if (sms <= 0 || per_sm <= 0) return cudaErrorInvalidConfiguration;
+    g_enc_ctas[dev] = sms * per_sm;
   }
-  zc_encode_kernel<<<n_items, kEncThreads, kEncSmem, s>>>(args);
-  return cudaGetLastError();
+  // Every CTA must be resident for the look-back order to make progress:
+  // the cooperative launch guarantees it (or fails).
+  EncodeArgs a = args;
+  void* params[] = {&a};
+  const uint32_t grid = min(n_items, (uint32_t)g_enc_ctas[dev]);
+  return cudaLaunchCooperativeKernel((const void*)zc_encode_kernel, dim3(grid), dim3(kEncThreads), params, kEncSmem, s);
 }
 
 }  // namespace zc

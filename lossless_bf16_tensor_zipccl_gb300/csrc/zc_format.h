@@ -96,6 +96,17 @@ struct alignas(64) EncChunk {
 };
 static_assert(sizeof(EncChunk) == 64, "enc chunk");
 
+// Per-tile record of the compress workspace, written by the select kernel.
+struct alignas(32) EncItem {
+  uint64_t elem0;  // first input element of the tile
+  uint32_t c;      // chunk
+  uint32_t k;      // tile within the chunk
+  uint32_t nt;     // values in the tile (0 for an empty chunk's header-only item)
+  uint32_t base;   // window start exponent of the chunk
+  uint32_t pad[2];
+};
+static_assert(sizeof(EncItem) == 32, "enc item");
+
 // Per-chunk record of the decompress / reduce workspace.
 struct alignas(64) DecChunk {
   uint64_t stream_off;  // chunk byte offset in the stream

@@ -26,7 +26,7 @@ struct SelectArgs {
   const uint16_t* in;
   EncChunk* chunks;
   uint32_t* tables;  // per chunk: kEncTableWords code-table words
-  uint32_t* item_chunk;
+  EncItem* items;
   uint64_t* item_state;
   WsHeader* hdr;
   uint32_t chunk0;
@@ -43,7 +43,7 @@ struct EncodeArgs {
   uint64_t* offsets;
   EncChunk* chunks;
   const uint32_t* tables;
-  const uint32_t* item_chunk;
+  const EncItem* items;
   uint64_t* item_state;
   WsHeader* hdr;
   uint32_t n_chunks;
