@@ -255,22 +255,29 @@ __device__ __forceinline__ void store_row(uint16_t* y, uint32_t cnt, bool vec, u
 // ---------------------------------------------------------------- decompress
 // Block c < n_chunks: validate chunk c's header, build its table.  Block
 // n_chunks: prefix sums of element counts and tile counts over all chunks.
+// Each chunk's (or peer's) decode table is built by kLutParts blocks.
+constexpr uint32_t kLutParts = 8;
+constexpr uint32_t kLutPart = kLutEntries / kLutParts;
+
+// Blocks c * kLutParts + j (j < kLutParts): validate chunk c's header and
+// build part j of its table (part 0 also writes the chunk record).  The last
+// block: prefix sums of element counts and tile counts over all chunks.
 __global__ void __launch_bounds__(256) zc_dprep_kernel(DprepArgs a) {
   const uint32_t tid = threadIdx.x;
-  if (blockIdx.x < a.n_chunks) {
-    const uint32_t c = blockIdx.x;
+  if (blockIdx.x < a.n_chunks * kLutParts) {
+    const uint32_t c = blockIdx.x / kLutParts, part = blockIdx.x % kLutParts;
     const uint64_t o0 = a.offsets[c], o1 = a.offsets[c + 1], total = a.offsets[a.n_chunks];
     HeaderInfo h;
     uint32_t st = (o1 < o0 || o1 > total || (o0 & 15)) ? kStCorrupt : check_header(a.stream + o0, o1 - o0, h);
     if (st) {
-      if (tid == 0) {
+      if (tid == 0 && part == 0) {
         set_status(a.hdr, st);
         a.chunks[c].ok = 0;
       }
       return;
     }
-    build_lut(h.lens, a.luts + (size_t)c * kLutEntries);
-    if (tid == 0) {
+    build_lut(h.lens, a.luts + (size_t)c * kLutEntries, part * kLutPart, kLutPart);
+    if (tid == 0 && part == 0) {
       DecChunk& d = a.chunks[c];
       d.stream_off = o0;
       d.bytes = o1 - o0;
@@ -343,13 +350,16 @@ __global__ void __launch_bounds__(256) zc_dprep_kernel(DprepArgs a) {
 }
 
 // One CTA per tile: warp h decodes the tile's half h (segments 32h..32h+31).
-constexpr uint32_t kExpSlot = 12288;  // staged payload; larger ones are read in place
+// The coded payload comes into shared memory with one TMA bulk copy;
+// sign/mantissa bytes are read straight from global memory (256 contiguous
+// bytes per warp and row, four rows ahead).  Shared memory stays small
+// enough for 14 CTAs per SM, so a whole 64M-value bucket decodes in one wave.
+constexpr uint32_t kExpSlot = 11392;  // staged payload (~2.78 bits/value); larger ones are read in place
+constexpr uint32_t kSmAhead = 4;      // rows of sign/mantissa bytes in flight per lane
 
 __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
   __shared__ __align__(128) uint8_t s_exp[kExpSlot];
-  __shared__ __align__(128) uint8_t s_sm[2][2 * kSmBlkBytes];
   __shared__ __align__(16) uint32_t s_lut[kLutEntries];
-  __shared__ __align__(8) uint64_t s_bar[2][2];
   __shared__ __align__(8) uint64_t s_xbar;
   __shared__ uint32_t s_flag[3];
   const uint32_t tid = threadIdx.x, lane = tid & 31, half = tid >> 5;
@@ -390,18 +400,23 @@ __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
     mbar_arrive_expect_tx(&s_xbar, sbytes);
     bulk_copy_g2s(s_exp, payload, sbytes, &s_xbar);
   }
-  SmStager stg;
-  stg.buf = s_sm[half];
-  stg.bars = s_bar[half];
-  stg.g = src.tv.tile + kTileHdr;
-  stg.plane = (uint32_t)pad16(nt);
-  stg.half_off = half * kHalf;
-  const uint32_t rows = (nt + kRow - 1) / kRow;
-  stg.nblk = (rows + kSmBlkRows - 1) / kSmBlkRows;
-  stg.start(lane);
+  const uint64_t e0 = d.elem_start + (uint64_t)k * kTile;
+  uint16_t* y = a.out + e0 + src.col;
+  const bool vec = (e0 & 7) == 0;
+  const uint8_t* smp = src.tv.tile + kTileHdr + src.col;  // this lane's sign/mantissa bytes of row 0
+  const bool full = nt == kTile && vec && src.tv.mode == 0;
+  uint2 sq[kSmAhead];
+  if (full) {
+#pragma unroll
+    for (uint32_t r = 0; r < kSmAhead; ++r) sq[r] = ld_stream_v2(smp + r * kRow);
+  }
   __syncthreads();  // the payload barrier is initialised
-  bool timeout = sbytes && !mbar_wait(&s_xbar, 0);
-  timeout = __any_sync(kFull, timeout);
+  const bool timeout = sbytes && __any_sync(kFull, !mbar_wait(&s_xbar, 0));
+  if (timeout) {
+    // the copy never arrived: skip the rows; the status tells the caller
+    if (lane == 0) set_status(a.hdr, kStTimeout);
+    return;
+  }
   ExpSource xs;
   if (sbytes) {
     xs.words = reinterpret_cast<const uint32_t*>(s_exp);
@@ -413,69 +428,44 @@ __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
     xs.end = reinterpret_cast<const uint32_t*>(src.tv.tile + src.tv.exp_off + pad16(src.tv.exp_bytes));
   }
   src.start(s_lut, d.base, xs);
-  const uint64_t e0 = d.elem_start + (uint64_t)k * kTile;
-  uint16_t* y = a.out + e0 + src.col;
-  const bool vec = (e0 & 7) == 0;
-  uint32_t b = 0;  // first block not yet acquired
-  if (timeout) {
-    // skip the rows; the status tells the caller
-  } else if (nt == kTile && vec && src.tv.mode == 0) {
+  if (full) {
     // full coded tile: every lane has 8 values in every row
-    for (; b < stg.nblk; ++b) {
-      if (!stg.acquire(b)) {
-        timeout = true;
-        break;
-      }
-      const uint8_t* blk = stg.block(b) + lane * kLaneElems;
-      uint16_t* yb = y + b * kSmBlkRows * kRow;
-#pragma unroll
-      for (uint32_t j = 0; j < kSmBlkRows; ++j) {
-        const uint2 sm = *reinterpret_cast<const uint2*>(blk + j * kHalf);
-        uint32_t elo, ehi;
-        src.dec.fill_warp(8);
-        src.dec.take8(elo, ehi);
-        const uint2 u = merge4(elo, sm.x), v = merge4(ehi, sm.y);
-        *reinterpret_cast<uint4*>(yb + j * kRow) = make_uint4(u.x, u.y, v.x, v.y);
-      }
-      stg.release(b, lane);
+#pragma unroll kSmAhead
+    for (uint32_t r = 0; r < kRows; ++r) {
+      const uint2 sm = sq[r % kSmAhead];
+      if (r + kSmAhead < kRows) sq[r % kSmAhead] = ld_stream_v2(smp + (r + kSmAhead) * kRow);
+      uint32_t elo, ehi;
+      src.dec.fill_warp(8);
+      src.dec.take8(elo, ehi);
+      const uint2 u = merge4(elo, sm.x), v = merge4(ehi, sm.y);
+      *reinterpret_cast<uint4*>(y + r * kRow) = make_uint4(u.x, u.y, v.x, v.y);
     }
   } else {
-    for (; b < stg.nblk; ++b) {
-      if (!stg.acquire(b)) {
-        timeout = true;
-        break;
-      }
-      const uint8_t* blk = stg.block(b);
-      const uint32_t rend = min(rows, (b + 1) * kSmBlkRows);
-      for (uint32_t r = b * kSmBlkRows; r < rend; ++r) {
-        const uint32_t cnt = src.count(r);
-        const uint4 v = src.row(r, src.sm_staged(blk, r));
-        if (cnt) store_row(y + r * kRow, cnt, vec, v);
-      }
-      stg.release(b, lane);
+    const uint32_t rows = (nt + kRow - 1) / kRow;
+    for (uint32_t r = 0; r < rows; ++r) {
+      const uint32_t cnt = src.count(r);
+      const uint4 v = src.row(r, load_bytes8(smp + r * kRow, cnt));
+      if (cnt) store_row(y + r * kRow, cnt, vec, v);
     }
-  }
-  if (timeout) {
-    stg.drain(b);
-    if (lane == 0) set_status(a.hdr, kStTimeout);
   }
 }
 
 // ---------------------------------------------------------------- reduce
+// Blocks p * kLutParts + j: validate peer p's header, build part j of its table.
 __global__ void __launch_bounds__(256) zc_rprep_kernel(ReduceArgs a) {
-  const uint32_t p = blockIdx.x;
+  const uint32_t p = blockIdx.x / kLutParts, part = blockIdx.x % kLutParts;
   HeaderInfo h;
   uint32_t st = check_header(a.peers[p], a.bytes[p], h);
   if (!st && h.n != a.n) st = kStCorrupt;
   if (st) {
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && part == 0) {
       set_status(a.hdr, st);
       a.chunks[p].ok = 0;
     }
     return;
   }
-  build_lut(h.lens, a.luts + (size_t)p * kLutEntries);
-  if (threadIdx.x == 0) {
+  build_lut(h.lens, a.luts + (size_t)p * kLutEntries, part * kLutPart, kLutPart);
+  if (threadIdx.x == 0 && part == 0) {
     DecChunk& d = a.chunks[p];
     d.stream_off = 0;
     d.bytes = a.bytes[p];
@@ -632,7 +622,7 @@ __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
 static int g_red_attr_done[64];
 
 cudaError_t launch_decode(const DprepArgs& prep, const DecodeArgs& args, uint32_t max_items, cudaStream_t s) {
-  zc_dprep_kernel<<<prep.n_chunks + 1, 256, 0, s>>>(prep);
+  zc_dprep_kernel<<<prep.n_chunks * kLutParts + 1, 256, 0, s>>>(prep);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || max_items == 0) return e;
   zc_decode_kernel<<<max_items, 64, 0, s>>>(args);
@@ -649,7 +639,7 @@ cudaError_t launch_reduce(const ReduceArgs& args, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     g_red_attr_done[dev] = 1;
   }
-  zc_rprep_kernel<<<args.k, 256, 0, s>>>(args);
+  zc_rprep_kernel<<<args.k * kLutParts, 256, 0, s>>>(args);
   e = cudaGetLastError();
   if (e != cudaSuccess || args.n == 0) return e;
   const uint32_t tiles = (uint32_t)tiles_of(args.n);

@@ -185,12 +185,14 @@ __device__ __forceinline__ uint32_t lut_entry(uint32_t idx, uint64_t lens, const
   return nib | (pos << 20) | (ns << 24) | (esc << 27);
 }
 
-// Fill a 1024-entry table cooperatively (all threads of the block).
-__device__ __forceinline__ void build_lut(uint64_t lens, uint32_t* lut) {
+// Fill entries [first, first + count) of a 1024-entry table cooperatively
+// (all threads of the block).  Building a table is compute-bound, so it is
+// split across several blocks.
+__device__ __forceinline__ void build_lut(uint64_t lens, uint32_t* lut, uint32_t first, uint32_t count) {
   uint32_t rev[kNsym];
 #pragma unroll
   for (int s = 0; s < kNsym; ++s) rev[s] = bit_reverse(canonical_code(lens, s), (int)((lens >> (4 * s)) & 15));
-  for (uint32_t i = threadIdx.x; i < kLutEntries; i += blockDim.x) lut[i] = lut_entry(i, lens, rev);
+  for (uint32_t i = threadIdx.x; i < count; i += blockDim.x) lut[first + i] = lut_entry(first + i, lens, rev);
 }
 
 // ---------------------------------------------------------------- merge
