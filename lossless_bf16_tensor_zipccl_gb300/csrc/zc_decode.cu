@@ -464,9 +464,18 @@ __global__ void __launch_bounds__(256) zc_rprep_kernel(ReduceArgs a) {
     }
     return;
   }
-  build_lut(h.lens, a.luts + (size_t)p * kLutEntries, part * kLutPart, kLutPart);
+  // peers with the same code lengths share the first such peer's table
+  uint32_t owner = p;
+  for (uint32_t j = 0; j < p; ++j) {
+    if (a.bytes[j] >= kChunkHdr && ld_u64(a.peers[j] + 24) == h.lens) {
+      owner = j;
+      break;
+    }
+  }
+  if (owner == p) build_lut(h.lens, a.luts + (size_t)p * kLutEntries, part * kLutPart, kLutPart);
   if (threadIdx.x == 0 && part == 0) {
     DecChunk& d = a.chunks[p];
+    d.item_start = owner;
     d.stream_off = 0;
     d.bytes = a.bytes[p];
     d.n = h.n;
@@ -489,17 +498,20 @@ __device__ __forceinline__ void add_bf16x2(float& a0, float& a1, uint32_t w) {
   a1 = __fadd_rn(a1, __uint_as_float(w & 0xFFFF0000u));
 }
 
-// One block per half tile, one warp per peer.  Each warp stages its peer's
-// decode table, the payload bits of its half and the sign/mantissa blocks in
-// shared memory, decodes kRedRows half rows at a time into shared memory
-// (peer-major), then every thread folds 8 values across the peers in rank
-// order.
-constexpr uint32_t kRedRows = kSmBlkRows;
+// One block per half tile, one warp per peer.  Each warp stages the payload
+// bits of its peer's half tile in shared memory with one TMA bulk copy,
+// decodes kRedRows half rows at a time into shared memory (peer-major) with
+// the sign/mantissa bytes read straight from global memory, then every
+// thread folds 8 values across the peers in rank order.  Decode tables are
+// read through L1 (peers with the same code lengths share one table), so a
+// block of 8 peers needs 54 KB of shared memory and 4 blocks fit per SM: a
+// 64M-element reduce (512 half tiles) runs in one wave.
+constexpr uint32_t kRedRows = 2;
 constexpr uint32_t kRedStageBytes = kRedRows * kHalf * 2;  // decoded BF16 half rows per peer
-constexpr uint32_t kRedSlot = 6144;                        // staged half payload per peer
+constexpr uint32_t kRedSlot = 5696;                        // staged half payload per peer (~2.78 bits/value)
 
 __host__ __device__ constexpr size_t reduce_smem_bytes(uint32_t k) {
-  return (size_t)k * (kRedStageBytes + 2 * kSmBlkBytes + kLutEntries * 4 + kRedSlot + 32);
+  return (size_t)k * (kRedStageBytes + kRedSlot + 16);
 }
 
 __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
@@ -507,11 +519,9 @@ __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
   const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5, tid = threadIdx.x;
   const uint32_t t = blockIdx.x >> 1, half = blockIdx.x & 1;
   const uint32_t nthreads = 32 * a.k;
-  uint16_t* sbuf = reinterpret_cast<uint16_t*>(rsm);                                   // k x kRedRows half rows
-  uint8_t* smst = rsm + (size_t)a.k * kRedStageBytes;                                 // k x 2 s/m blocks
-  uint32_t* luts = reinterpret_cast<uint32_t*>(smst + (size_t)a.k * 2 * kSmBlkBytes);  // k x 1024
-  uint8_t* slots = reinterpret_cast<uint8_t*>(luts + (size_t)a.k * kLutEntries);       // k x kRedSlot
-  uint64_t* bars = reinterpret_cast<uint64_t*>(slots + (size_t)a.k * kRedSlot);       // k x 3
+  uint16_t* sbuf = reinterpret_cast<uint16_t*>(rsm);                          // k x kRedRows half rows
+  uint8_t* slots = rsm + (size_t)a.k * kRedStageBytes;                       // k x kRedSlot
+  uint64_t* bars = reinterpret_cast<uint64_t*>(slots + (size_t)a.k * kRedSlot);  // k x 2
   __shared__ int s_bad;
   // one read of the status word per block, so every thread takes the same path
   if (tid == 0) s_bad = *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0;
@@ -523,29 +533,20 @@ __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
   src.nt = nt;
   src.col = half * kHalf + lane * kLaneElems;
   const bool ok = d.ok && open_tile(a.peers[p], d.bytes, d.n_tiles, t, nt, half, lane, src.tv);
-  SmStager stg;
-  stg.buf = smst + (size_t)p * 2 * kSmBlkBytes;
-  stg.bars = bars + 3 * p;
-  stg.g = src.tv.tile + kTileHdr;
-  stg.plane = (uint32_t)pad16(nt);
-  stg.half_off = half * kHalf;
-  const uint32_t rows = (nt + kRow - 1) / kRow;
-  stg.nblk = (rows + kSmBlkRows - 1) / kSmBlkRows;
   const uint8_t* payload = src.tv.tile + src.tv.exp_off + kSegTab;
   uint8_t* slot = slots + (size_t)p * kRedSlot;
+  uint64_t* bar = bars + 2 * p;
   uint32_t slo = 0, sbytes = 0;
   bool timeout = false;
   if (ok) {
     if (src.tv.mode == 0) sbytes = stage_span(src.tv, src.tv.hbit0, src.tv.hbit1, kRedSlot, slo);
     if (lane == 0 && sbytes) {
-      mbar_init(bars + 3 * p + 2, 1);
-      mbar_arrive_expect_tx(bars + 3 * p + 2, sbytes);
-      bulk_copy_g2s(slot, payload + slo, sbytes, bars + 3 * p + 2);
+      mbar_init(bar, 1);
+      mbar_arrive_expect_tx(bar, sbytes);
+      bulk_copy_g2s(slot, payload + slo, sbytes, bar);
     }
-    stg.start(lane);
-    load_lut(luts + (size_t)p * kLutEntries, a.luts + (size_t)p * kLutEntries, lane, 32);
     __syncwarp();
-    timeout = sbytes && !mbar_wait(bars + 3 * p + 2, 0);
+    timeout = sbytes && !mbar_wait(bar, 0);
     timeout = __any_sync(kFull, timeout);
   }
   if (lane == 0 && (!ok || timeout)) {
@@ -553,10 +554,7 @@ __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
     set_status(a.hdr, ok ? kStTimeout : kStCorrupt);
   }
   __syncthreads();
-  if (s_bad) {  // uniform
-    if (ok) stg.drain(0);
-    return;
-  }
+  if (s_bad) return;  // uniform; a copy that did arrive has nothing left in flight
   ExpSource xs;
   if (sbytes) {
     xs.words = reinterpret_cast<const uint32_t*>(slot);
@@ -567,21 +565,33 @@ __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
     xs.bit_base = 0;
     xs.end = reinterpret_cast<const uint32_t*>(src.tv.tile + src.tv.exp_off + pad16(src.tv.exp_bytes));
   }
-  src.start(luts + (size_t)p * kLutEntries, d.base, xs);
+  src.start(a.luts + (size_t)d.item_start * kLutEntries, d.base, xs);  // item_start: the peer owning the table
   uint16_t* mine = sbuf + (size_t)p * kRedRows * kHalf;
   uint16_t* y = a.out + (uint64_t)t * kTile;
-  bool late = false;  // a bounded wait gave up: finish the loop, report it
-  uint32_t late_b = 0;
-  for (uint32_t b = 0; b < stg.nblk; ++b) {
-    if (!late && !stg.acquire(b)) {
-      late = true;
-      late_b = b;
+  const uint8_t* smp = src.tv.tile + kTileHdr + src.col;  // this lane's sign/mantissa bytes of row 0
+  const uint32_t rows = (nt + kRow - 1) / kRow;
+  uint2 sq[kSmAhead];
+#pragma unroll
+  for (uint32_t r = 0; r < kSmAhead; ++r) sq[r] = r < rows ? load_bytes8(smp + r * kRow, src.count(r)) : make_uint2(0, 0);
+  for (uint32_t r0 = 0; r0 < rows; r0 += kRedRows) {
+#pragma unroll
+    for (uint32_t j = 0; j < kRedRows; ++j) {
+      const uint32_t r = r0 + j;
+      if (r < rows) {
+        const uint2 sm = sq[j];  // kSmAhead is a multiple of kRedRows: the ring slot of row r
+        *reinterpret_cast<uint4*>(mine + j * kHalf + lane * kLaneElems) = src.row(r, sm);
+      }
     }
-    const uint8_t* blk = stg.block(b);
-    const uint32_t r0 = b * kRedRows, rend = min(rows, r0 + kRedRows);
-    for (uint32_t r = r0; r < rend; ++r)
-      *reinterpret_cast<uint4*>(mine + (r - r0) * kHalf + lane * kLaneElems) = src.row(r, src.sm_staged(blk, r));
-    if (!late) stg.release(b, lane);
+    // advance the ring by kRedRows rows
+#pragma unroll
+    for (uint32_t j = 0; j < kSmAhead; ++j) {
+      if (j + kRedRows < kSmAhead) {
+        sq[j] = sq[j + kRedRows];
+      } else {
+        const uint32_t r = r0 + kRedRows + j;
+        sq[j] = r < rows ? load_bytes8(smp + r * kRow, src.count(r)) : make_uint2(0, 0);
+      }
+    }
     __syncthreads();
     for (uint32_t e = tid * 8; e < kRedRows * kHalf; e += nthreads * 8) {
       const uint32_t gi = (r0 + e / kHalf) * kRow + half * kHalf + (e % kHalf);
@@ -611,10 +621,6 @@ __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
       store_row(y + gi, min(8u, nt - gi), true, o);
     }
     __syncthreads();
-  }
-  if (late) {
-    stg.drain(late_b);
-    if (lane == 0) set_status(a.hdr, kStTimeout);
   }
 }
 
