@@ -502,13 +502,13 @@ __device__ __forceinline__ void add_bf16x2(float& a0, float& a1, uint32_t w) {
 // bits of its peer's half tile in shared memory with one TMA bulk copy,
 // decodes kRedRows half rows at a time into shared memory (peer-major) with
 // the sign/mantissa bytes read straight from global memory, then every
-// thread folds 8 values across the peers in rank order.  Decode tables are
-// read through L1 (peers with the same code lengths share one table), so a
-// block of 8 peers needs 54 KB of shared memory and 4 blocks fit per SM: a
-// 64M-element reduce (512 half tiles) runs in one wave.
+// thread folds pairs of values across the peers in rank order.  Decode
+// tables are read through L1 (peers with the same code lengths share one
+// table), so a block of 8 peers needs 54 KB of shared memory and 4 blocks
+// fit per SM: a 64M-element reduce (512 half tiles) runs in one wave.
 constexpr uint32_t kRedRows = 2;
 constexpr uint32_t kRedStageBytes = kRedRows * kHalf * 2;  // decoded BF16 half rows per peer
-constexpr uint32_t kRedSlot = 5696;                        // staged half payload per peer (~2.78 bits/value)
+constexpr uint32_t kRedSlot = 5696;  // staged half payload per peer (~2.78 bits/value; a multiple of 16 for TMA)
 
 __host__ __device__ constexpr size_t reduce_smem_bytes(uint32_t k) {
   return (size_t)k * (kRedStageBytes + kRedSlot + 16);
@@ -593,32 +593,17 @@ __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
       }
     }
     __syncthreads();
-    for (uint32_t e = tid * 8; e < kRedRows * kHalf; e += nthreads * 8) {
+    // fold: every thread takes pairs of values, so the whole block works
+    for (uint32_t e = tid * 2; e < kRedRows * kHalf; e += nthreads * 2) {
       const uint32_t gi = (r0 + e / kHalf) * kRow + half * kHalf + (e % kHalf);
       if (gi >= nt) continue;
-      float acc[8];
-      {
-        const uint4 v = *reinterpret_cast<const uint4*>(sbuf + e);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[2 * i] = __uint_as_float(w[i] << 16);
-          acc[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-        }
-      }
-      for (uint32_t pp = 1; pp < a.k; ++pp) {
-        const uint4 v = *reinterpret_cast<const uint4*>(sbuf + (size_t)pp * kRedRows * kHalf + e);
-        add_bf16x2(acc[0], acc[1], v.x);
-        add_bf16x2(acc[2], acc[3], v.y);
-        add_bf16x2(acc[4], acc[5], v.z);
-        add_bf16x2(acc[6], acc[7], v.w);
-      }
-      uint4 o;
-      o.x = f32_to_bf16_rne(acc[0]) | (f32_to_bf16_rne(acc[1]) << 16);
-      o.y = f32_to_bf16_rne(acc[2]) | (f32_to_bf16_rne(acc[3]) << 16);
-      o.z = f32_to_bf16_rne(acc[4]) | (f32_to_bf16_rne(acc[5]) << 16);
-      o.w = f32_to_bf16_rne(acc[6]) | (f32_to_bf16_rne(acc[7]) << 16);
-      store_row(y + gi, min(8u, nt - gi), true, o);
+      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(sbuf + e);
+      float a0 = __uint_as_float(w0 << 16), a1 = __uint_as_float(w0 & 0xFFFF0000u);
+      for (uint32_t pp = 1; pp < a.k; ++pp)
+        add_bf16x2(a0, a1, *reinterpret_cast<const uint32_t*>(sbuf + (size_t)pp * kRedRows * kHalf + e));
+      const uint32_t o = f32_to_bf16_rne(a0) | (f32_to_bf16_rne(a1) << 16);
+      if (gi + 1 < nt) *reinterpret_cast<uint32_t*>(y + gi) = o;
+      else y[gi] = (uint16_t)o;
     }
     __syncthreads();
   }
