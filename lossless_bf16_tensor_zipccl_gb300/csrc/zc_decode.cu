@@ -573,13 +573,26 @@ __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
   uint2 sq[kSmAhead];
 #pragma unroll
   for (uint32_t r = 0; r < kSmAhead; ++r) sq[r] = r < rows ? load_bytes8(smp + r * kRow, src.count(r)) : make_uint2(0, 0);
+  const bool fast = nt == kTile && src.tv.mode == 0;  // same for every lane of the warp
   for (uint32_t r0 = 0; r0 < rows; r0 += kRedRows) {
+    if (fast) {
+      // full coded tile: 8 values per lane in every row
 #pragma unroll
-    for (uint32_t j = 0; j < kRedRows; ++j) {
-      const uint32_t r = r0 + j;
-      if (r < rows) {
-        const uint2 sm = sq[j];  // kSmAhead is a multiple of kRedRows: the ring slot of row r
-        *reinterpret_cast<uint4*>(mine + j * kHalf + lane * kLaneElems) = src.row(r, sm);
+      for (uint32_t j = 0; j < kRedRows; ++j) {
+        uint32_t elo, ehi;
+        src.dec.fill_warp(8);
+        src.dec.take8(elo, ehi);
+        const uint2 u = merge4(elo, sq[j].x), v = merge4(ehi, sq[j].y);
+        *reinterpret_cast<uint4*>(mine + j * kHalf + lane * kLaneElems) = make_uint4(u.x, u.y, v.x, v.y);
+      }
+    } else {
+#pragma unroll
+      for (uint32_t j = 0; j < kRedRows; ++j) {
+        const uint32_t r = r0 + j;
+        if (r < rows) {
+          const uint2 sm = sq[j];  // kSmAhead is a multiple of kRedRows: the ring slot of row r
+          *reinterpret_cast<uint4*>(mine + j * kHalf + lane * kLaneElems) = src.row(r, sm);
+        }
       }
     }
     // advance the ring by kRedRows rows
