@@ -244,3 +244,31 @@ def test_full_stress_escape_path():
 def test_full_fsdp_allgather():
     w = workloads.fsdp()
     full_size(w, [0, 9, 100, 223])
+
+
+# ------------------------------------------------------------------ wide exponent spread
+def wide_window_values(n: int, seed: int) -> np.ndarray:
+    """Random sign/mantissa with biased exponents uniform over 15 consecutive
+    values: about 3.9 bits per exponent, still coded.  The payload of a tile
+    (~16 KB) is larger than the shared-memory staging slots of the decode and
+    reduce kernels, so both read it in place, and lane parts overflow the
+    encoder's private buffers (its slower packing path)."""
+    rng = np.random.default_rng(seed)
+    e = rng.integers(110, 125, size=n, dtype=np.uint16)
+    sm = rng.integers(0, 256, size=n, dtype=np.uint16)
+    return (((sm & 0x80) << 8) | (e << 7) | (sm & 0x7F)).astype(np.uint16)
+
+
+def test_wide_exponent_spread_in_place_paths():
+    # a sigma hint of 2^-4 puts the code window on exponents 110..124: every
+    # tile is coded at ~6.4 bits per exponent
+    hint = 2.0 ** -4
+    x = wide_window_values(5 * 32768 + 777, 31)
+    c, s, offs = gpu_roundtrip(x, [3 * 32768, 2 * 32768 + 777], [hint, hint])
+    assert 8.0 * len(s) / x.size < 15.0  # coded, not raw
+    xs = [wide_window_values(70000, 40 + p) for p in range(4)]
+    chunks = [oracle.compress(v, [v.size], [hint])[0] for v in xs]
+    ref = oracle.decompress_reduce(chunks, 70000)
+    y = zc.decompress_reduce(dev_chunks(chunks), 70000)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), ref)
