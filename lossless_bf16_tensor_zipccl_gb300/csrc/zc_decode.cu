@@ -514,14 +514,16 @@ __host__ __device__ constexpr size_t reduce_smem_bytes(uint32_t k) {
   return (size_t)k * (kRedStageBytes + kRedSlot + 16);
 }
 
-__global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
+// Instantiated per peer count K (1..16), so the fold over the peers unrolls.
+template <uint32_t K>
+__global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
   extern __shared__ __align__(128) uint8_t rsm[];
   const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5, tid = threadIdx.x;
   const uint32_t t = blockIdx.x >> 1, half = blockIdx.x & 1;
-  const uint32_t nthreads = 32 * a.k;
+  constexpr uint32_t nthreads = 32 * K;
   uint16_t* sbuf = reinterpret_cast<uint16_t*>(rsm);                          // k x kRedRows half rows
-  uint8_t* slots = rsm + (size_t)a.k * kRedStageBytes;                       // k x kRedSlot
-  uint64_t* bars = reinterpret_cast<uint64_t*>(slots + (size_t)a.k * kRedSlot);  // k x 2
+  uint8_t* slots = rsm + (size_t)K * kRedStageBytes;                       // k x kRedSlot
+  uint64_t* bars = reinterpret_cast<uint64_t*>(slots + (size_t)K * kRedSlot);  // k x 2
   __shared__ int s_bad;
   // one read of the status word per block, so every thread takes the same path
   if (tid == 0) s_bad = *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0;
@@ -612,7 +614,8 @@ __global__ void __launch_bounds__(512) zc_reduce_kernel(ReduceArgs a) {
       if (gi >= nt) continue;
       const uint32_t w0 = *reinterpret_cast<const uint32_t*>(sbuf + e);
       float a0 = __uint_as_float(w0 << 16), a1 = __uint_as_float(w0 & 0xFFFF0000u);
-      for (uint32_t pp = 1; pp < a.k; ++pp)
+#pragma unroll
+      for (uint32_t pp = 1; pp < K; ++pp)
         add_bf16x2(a0, a1, *reinterpret_cast<const uint32_t*>(sbuf + (size_t)pp * kRedRows * kHalf + e));
       const uint32_t o = f32_to_bf16_rne(a0) | (f32_to_bf16_rne(a1) << 16);
       if (gi + 1 < nt) *reinterpret_cast<uint32_t*>(y + gi) = o;
@@ -633,21 +636,53 @@ cudaError_t launch_decode(const DprepArgs& prep, const DecodeArgs& args, uint32_
   return cudaGetLastError();
 }
 
+template <uint32_t K>
+static cudaError_t reduce_setup() {
+  return cudaFuncSetAttribute(zc_reduce_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)reduce_smem_bytes(K));
+}
+
+template <uint32_t K>
+static void reduce_launch(const ReduceArgs& args, uint32_t blocks, cudaStream_t s) {
+  zc_reduce_kernel<K><<<blocks, 32 * K, reduce_smem_bytes(K), s>>>(args);
+}
+
 cudaError_t launch_reduce(const ReduceArgs& args, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && !g_red_attr_done[dev]) {
-    e = cudaFuncSetAttribute(zc_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)reduce_smem_bytes(kMaxPeers));
-    if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!g_red_attr_done[dev]) {
+    const cudaError_t es[kMaxPeers] = {reduce_setup<1>(),  reduce_setup<2>(),  reduce_setup<3>(),  reduce_setup<4>(),
+                                       reduce_setup<5>(),  reduce_setup<6>(),  reduce_setup<7>(),  reduce_setup<8>(),
+                                       reduce_setup<9>(),  reduce_setup<10>(), reduce_setup<11>(), reduce_setup<12>(),
+                                       reduce_setup<13>(), reduce_setup<14>(), reduce_setup<15>(), reduce_setup<16>()};
+    for (const cudaError_t x : es)
+      if (x != cudaSuccess) return x;
     g_red_attr_done[dev] = 1;
   }
   zc_rprep_kernel<<<args.k * kLutParts, 256, 0, s>>>(args);
   e = cudaGetLastError();
   if (e != cudaSuccess || args.n == 0) return e;
-  const uint32_t tiles = (uint32_t)tiles_of(args.n);
-  zc_reduce_kernel<<<2 * tiles, 32 * args.k, reduce_smem_bytes(args.k), s>>>(args);
+  const uint32_t blocks = 2 * (uint32_t)tiles_of(args.n);
+  switch (args.k) {
+    case 1: reduce_launch<1>(args, blocks, s); break;
+    case 2: reduce_launch<2>(args, blocks, s); break;
+    case 3: reduce_launch<3>(args, blocks, s); break;
+    case 4: reduce_launch<4>(args, blocks, s); break;
+    case 5: reduce_launch<5>(args, blocks, s); break;
+    case 6: reduce_launch<6>(args, blocks, s); break;
+    case 7: reduce_launch<7>(args, blocks, s); break;
+    case 8: reduce_launch<8>(args, blocks, s); break;
+    case 9: reduce_launch<9>(args, blocks, s); break;
+    case 10: reduce_launch<10>(args, blocks, s); break;
+    case 11: reduce_launch<11>(args, blocks, s); break;
+    case 12: reduce_launch<12>(args, blocks, s); break;
+    case 13: reduce_launch<13>(args, blocks, s); break;
+    case 14: reduce_launch<14>(args, blocks, s); break;
+    case 15: reduce_launch<15>(args, blocks, s); break;
+    default: reduce_launch<16>(args, blocks, s); break;
+  }
   return cudaGetLastError();
 }
 
