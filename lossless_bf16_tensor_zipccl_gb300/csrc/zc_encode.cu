@@ -106,17 +106,23 @@ __global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ 
   // an escape flag (bit 20) | total length including 8 raw bits per escape
   // (bits 26-31); a pair with an escape is packed symbol by symbol.
   {
+    // the 16 reversed codewords, once per block
+    __shared__ uint32_t s_rev[kNsym];
+    if (threadIdx.x < (uint32_t)kNsym) {
+      const int sy = (int)threadIdx.x;
+      s_rev[sy] = bit_reverse(canonical_code(lens, sy), (int)((lens >> (4 * sy)) & 15));
+    }
+    __syncthreads();
     uint32_t* tab = a.tables + (size_t)ci * kEncTableWords;
     const uint32_t e = threadIdx.x;
     const int xs = (int)e - base;
     const int sym = (xs >= 0 && xs < kWindow) ? xs : kEsc;
     const int L = (int)((lens >> (4 * sym)) & 15);
-    const uint32_t rev = bit_reverse(canonical_code(lens, sym), L);
+    const uint32_t rev = s_rev[sym];
     tab[e] = sym == kEsc ? ((rev | (e << L)) | ((uint32_t)(L + 8) << 24)) : (rev | ((uint32_t)L << 24));
     const uint32_t s0 = e & 15, s1 = e >> 4;
     const uint32_t l0 = (uint32_t)((lens >> (4 * s0)) & 15), l1 = (uint32_t)((lens >> (4 * s1)) & 15);
-    const uint32_t c0 = bit_reverse(canonical_code(lens, (int)s0), (int)l0);
-    const uint32_t c1 = bit_reverse(canonical_code(lens, (int)s1), (int)l1);
+    const uint32_t c0 = s_rev[s0], c1 = s_rev[s1];
     const uint32_t raw = (s0 == (uint32_t)kEsc ? 8u : 0u) + (s1 == (uint32_t)kEsc ? 8u : 0u);
     tab[256 + e] = (c0 | (c1 << l0)) | (raw ? kPairEsc : 0u) | ((l0 + l1 + raw) << 26);
   }
