@@ -109,11 +109,9 @@ __device__ __forceinline__ uint2 load_bytes8(const uint8_t* p, uint32_t cnt) {
   return make_uint2(lo, hi);
 }
 
-constexpr uint32_t kSmBlkRows = 4;                     // rows per staged sign/mantissa block
-constexpr uint32_t kSmBlkBytes = kSmBlkRows * kHalf;   // one warp's half rows: 1 KB
-
-// A copy of payload bytes [lo, lo + bytes) staged in shared memory (or the
-// payload in place in global memory when lo == 0 and `global` is set).
+// Where a decoder reads the coded payload: a copy of payload bytes
+// [lo, lo + bytes) staged in shared memory, or the payload in place in global
+// memory (bit_base 0).
 struct ExpSource {
   const uint32_t* words;  // word holding payload bit 8 * lo
   uint32_t bit_base;      // 8 * lo
@@ -148,77 +146,6 @@ struct RowSource {
     }
     const uint2 a = merge4(lo, sm.x), b = merge4(hi, sm.y);
     return make_uint4(a.x, a.y, b.x, b.y);
-  }
-
-  // sign/mantissa bytes of row r from its staged block (shared memory)
-  __device__ __forceinline__ uint2 sm_staged(const uint8_t* blk, uint32_t r) const {
-    const uint32_t cnt = count(r);
-    const uint8_t* p = blk + (r % kSmBlkRows) * kHalf + (col % kHalf);
-    if (cnt == 8) return *reinterpret_cast<const uint2*>(p);
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      if (t < (int)cnt) {
-        const uint32_t b = p[t];
-        if (t < 4) lo |= b << (8 * t);
-        else hi |= b << (8 * (t - 4));
-      }
-    }
-    return make_uint2(lo, hi);
-  }
-};
-
-// Double-buffered TMA staging of one warp's half of the sign/mantissa plane,
-// kSmBlkRows rows per block (one bulk copy per row piece).  Block b lives in
-// stage b & 1; its barrier completes phase b >> 1.
-struct SmStager {
-  uint8_t* buf;       // 2 x kSmBlkBytes, 16-B aligned
-  uint64_t* bars;     // 2 barriers
-  const uint8_t* g;   // the plane in global memory (tile + 16)
-  uint32_t plane;     // padded plane bytes (multiple of 16)
-  uint32_t half_off;  // 0 or kHalf
-  uint32_t nblk;
-
-  __device__ __forceinline__ uint32_t piece(uint32_t r) const {
-    const uint32_t off = r * kRow + half_off;
-    return off < plane ? min(kHalf, plane - off) : 0u;
-  }
-  __device__ __forceinline__ void issue(uint32_t b) {  // lane 0
-    uint32_t tx = 0;
-#pragma unroll
-    for (uint32_t j = 0; j < kSmBlkRows; ++j) tx += piece(b * kSmBlkRows + j);
-    mbar_arrive_expect_tx(bars + (b & 1), tx);
-    uint8_t* dst = buf + (b & 1) * kSmBlkBytes;
-#pragma unroll
-    for (uint32_t j = 0; j < kSmBlkRows; ++j) {
-      const uint32_t r = b * kSmBlkRows + j, sz = piece(r);
-      if (sz) bulk_copy_g2s(dst + j * kHalf, g + r * kRow + half_off, sz, bars + (b & 1));
-    }
-  }
-  __device__ __forceinline__ void start(uint32_t lane) {
-    if (lane == 0) {
-      mbar_init(bars, 1);
-      mbar_init(bars + 1, 1);
-      if (nblk > 0) issue(0);
-      if (nblk > 1) issue(1);
-    }
-    __syncwarp();
-  }
-  // Wait for block b; false when the bounded wait gave up (warp-uniform).
-  __device__ __forceinline__ bool acquire(uint32_t b) {
-    const bool ok = mbar_wait(bars + (b & 1), (b >> 1) & 1);
-    return !__any_sync(kFull, !ok);
-  }
-  __device__ __forceinline__ const uint8_t* block(uint32_t b) const { return buf + (b & 1) * kSmBlkBytes; }
-  // Every lane is done with block b: refill its stage with block b + 2.
-  __device__ __forceinline__ void release(uint32_t b, uint32_t lane) {
-    __syncwarp();
-    if (lane == 0 && b + 2 < nblk) issue(b + 2);
-  }
-  // Before leaving early: wait (bounded) for the copies of blocks b and b + 1,
-  // the ones that may still be in flight when block b was not acquired.
-  __device__ __forceinline__ void drain(uint32_t b) {
-    for (uint32_t j = b; j < nblk && j < b + 2; ++j) (void)mbar_wait(bars + (j & 1), (j >> 1) & 1);
   }
 };
 
