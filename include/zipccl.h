@@ -86,6 +86,11 @@ zipccl_status zipccl_reduce_workspace_bytes(uint32_t k, uint64_t *out_bytes);
  * d_chunk_offsets (device, n_chunks + 1 uint64) receives each chunk's byte
  * offset in d_out and, last, the total size.  d_ws: workspace of at least
  * zipccl_compress_workspace_bytes bytes.
+ * The tiles are coded by one persistent kernel whose CTAs (one per SM) must
+ * all be resident at once, so it is issued as a cooperative launch; where the
+ * device or context cannot make that launch the call returns ZIPCCL_ERR_CUDA.
+ * The first call on a device sets the kernel's shared-memory limit and reads
+ * its occupancy; later calls reuse them.
  */
 zipccl_status zipccl_compress(const uint16_t *d_in, uint64_t n, const uint64_t *chunk_elems,
                               uint32_t n_chunks, const float *sigma_hint, void *d_out,

@@ -389,9 +389,10 @@ __device__ __forceinline__ void load_group(const uint16_t* x, uint32_t cnt, bool
   }
 }
 
-// Shared state of the encode CTA.
+// Shared state of the encode CTA.  Plain pointers only: an array of
+// pointers indexed by the buffer number would put the struct in local memory.
 struct EncShared {
-  uint8_t* img[kImgBufs];
+  uint8_t* img0;   // image b at img0 + b * kImgBytes
   uint32_t* priv;  // [warp][word][lane]
   uint32_t* tabs;  // kImgBufs x kEncTableWords
   uint32_t* part;  // [row warp][lane] bits, then bit offsets
@@ -400,6 +401,7 @@ struct EncShared {
   uint32_t* mode;      // per buffer: 0 coded, 1 coded with an overflowed part, 2 raw
   uint32_t* over;      // per buffer: a part overflowed its private buffer
   uint32_t* size;      // per buffer: tile bytes
+  __device__ __forceinline__ uint8_t* img(uint32_t b) const { return img0 + b * kImgBytes; }
 };
 
 __device__ __forceinline__ EncItem load_item(const EncodeArgs& a, uint32_t t) {
@@ -425,7 +427,7 @@ __device__ __forceinline__ void row_tile(const EncodeArgs& a, const EncShared& S
   const uint32_t half = warp / kRowWarpsPerHalf;
   const uint32_t rb = (warp % kRowWarpsPerHalf) * kRowsPerWarp;
   const uint32_t col = half * kHalf + lane * kLaneElems;
-  uint8_t* img = S.img[buf];
+  uint8_t* img = S.img(buf);
   const uint32_t* tab = S.tabs + buf * kEncTableWords;  // per exponent
   const uint32_t* pair = tab + 256;                    // per symbol pair
   const uint32_t nt = rec.nt;
@@ -625,7 +627,7 @@ __device__ __forceinline__ void layout_tile(const EncodeArgs& a, const EncShared
                                             uint32_t next) {
   const uint32_t lane = threadIdx.x & 31;
   const EncItem rec = a.items[item];
-  uint8_t* img = S.img[buf];
+  uint8_t* img = S.img(buf);
   const uint32_t nt = rec.nt;
   const uint32_t sm_pad = (uint32_t)pad16(nt);
   const uint32_t exp_off = kTileHdr + sm_pad;
@@ -779,7 +781,7 @@ __device__ __forceinline__ void store_tile(const EncodeArgs& a, const EncShared&
   bar_wait(kBarImg0 + buf, kBarThreads);
   // Phase E: one TMA bulk store of the finished tile image.
   if (lane == 0 && !err && size) {
-    bulk_store_issue(a.out + goff, S.img[buf], size);
+    bulk_store_issue(a.out + goff, S.img(buf), size);
     bulk_commit_and_wait_read();
   }
   __syncwarp();
@@ -790,8 +792,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) zc_encode_kernel(EncodeArgs a)
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t s_segstart[kSegs], s_mode[kImgBufs], s_over[kImgBufs], s_size[kImgBufs];
   EncShared S;
-#pragma unroll
-  for (uint32_t i = 0; i < kImgBufs; ++i) S.img[i] = smem + i * kImgBytes;
+  S.img0 = smem;
   S.priv = reinterpret_cast<uint32_t*>(smem + kImgBufs * kImgBytes);
   S.tabs = reinterpret_cast<uint32_t*>(smem + kImgBufs * kImgBytes + kPrivBytes);
   S.part = S.tabs + kImgBufs * kEncTableWords;
