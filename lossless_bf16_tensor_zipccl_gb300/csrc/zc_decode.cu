@@ -190,6 +190,7 @@ constexpr uint32_t kLutPart = kLutEntries / kLutParts;
 // build part j of its table (part 0 also writes the chunk record).  The last
 // block: prefix sums of element counts and tile counts over all chunks.
 __global__ void __launch_bounds__(256) zc_dprep_kernel(DprepArgs a) {
+  pdl_trigger();
   const uint32_t tid = threadIdx.x;
   if (blockIdx.x < a.n_chunks * kLutParts) {
     const uint32_t c = blockIdx.x / kLutParts, part = blockIdx.x % kLutParts;
@@ -285,6 +286,7 @@ constexpr uint32_t kExpSlot = 11392;  // staged payload (~2.78 bits/value); larg
 constexpr uint32_t kSmAhead = 4;      // rows of sign/mantissa bytes in flight per lane
 
 __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
+  pdl_wait();  // chunk records and tables come from the prep kernel
   __shared__ __align__(128) uint8_t s_exp[kExpSlot];
   __shared__ __align__(16) uint32_t s_lut[kLutEntries];
   __shared__ __align__(8) uint64_t s_xbar;
@@ -380,6 +382,7 @@ __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
 // ---------------------------------------------------------------- reduce
 // Blocks p * kLutParts + j: validate peer p's header, build part j of its table.
 __global__ void __launch_bounds__(256) zc_rprep_kernel(ReduceArgs a) {
+  pdl_trigger();
   const uint32_t p = blockIdx.x / kLutParts, part = blockIdx.x % kLutParts;
   HeaderInfo h;
   uint32_t st = check_header(a.peers[p], a.bytes[p], h);
@@ -444,6 +447,7 @@ __host__ __device__ constexpr size_t reduce_smem_bytes(uint32_t k) {
 // Instantiated per peer count K (1..16), so the fold over the peers unrolls.
 template <uint32_t K>
 __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
+  pdl_wait();  // peer records and tables come from the prep kernel
   extern __shared__ __align__(128) uint8_t rsm[];
   const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5, tid = threadIdx.x;
   const uint32_t t = blockIdx.x >> 1, half = blockIdx.x & 1;
@@ -559,8 +563,9 @@ cudaError_t launch_decode(const DprepArgs& prep, const DecodeArgs& args, uint32_
   zc_dprep_kernel<<<prep.n_chunks * kLutParts + 1, 256, 0, s>>>(prep);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || max_items == 0) return e;
-  zc_decode_kernel<<<max_items, 64, 0, s>>>(args);
-  return cudaGetLastError();
+  cudaLaunchAttribute at[2];
+  const cudaLaunchConfig_t cfg = follow_config(dim3(max_items), dim3(64), 0, s, false, at);
+  return cudaLaunchKernelEx(&cfg, zc_decode_kernel, args);
 }
 
 template <uint32_t K>
@@ -570,8 +575,10 @@ static cudaError_t reduce_setup() {
 }
 
 template <uint32_t K>
-static void reduce_launch(const ReduceArgs& args, uint32_t blocks, cudaStream_t s) {
-  zc_reduce_kernel<K><<<blocks, 32 * K, reduce_smem_bytes(K), s>>>(args);
+static cudaError_t reduce_launch(const ReduceArgs& args, uint32_t blocks, cudaStream_t s) {
+  cudaLaunchAttribute at[2];
+  const cudaLaunchConfig_t cfg = follow_config(dim3(blocks), dim3(32 * K), reduce_smem_bytes(K), s, false, at);
+  return cudaLaunchKernelEx(&cfg, zc_reduce_kernel<K>, args);
 }
 
 cudaError_t launch_reduce(const ReduceArgs& args, cudaStream_t s) {
@@ -593,24 +600,23 @@ cudaError_t launch_reduce(const ReduceArgs& args, cudaStream_t s) {
   if (e != cudaSuccess || args.n == 0) return e;
   const uint32_t blocks = 2 * (uint32_t)tiles_of(args.n);
   switch (args.k) {
-    case 1: reduce_launch<1>(args, blocks, s); break;
-    case 2: reduce_launch<2>(args, blocks, s); break;
-    case 3: reduce_launch<3>(args, blocks, s); break;
-    case 4: reduce_launch<4>(args, blocks, s); break;
-    case 5: reduce_launch<5>(args, blocks, s); break;
-    case 6: reduce_launch<6>(args, blocks, s); break;
-    case 7: reduce_launch<7>(args, blocks, s); break;
-    case 8: reduce_launch<8>(args, blocks, s); break;
-    case 9: reduce_launch<9>(args, blocks, s); break;
-    case 10: reduce_launch<10>(args, blocks, s); break;
-    case 11: reduce_launch<11>(args, blocks, s); break;
-    case 12: reduce_launch<12>(args, blocks, s); break;
-    case 13: reduce_launch<13>(args, blocks, s); break;
-    case 14: reduce_launch<14>(args, blocks, s); break;
-    case 15: reduce_launch<15>(args, blocks, s); break;
-    default: reduce_launch<16>(args, blocks, s); break;
+    case 1: return reduce_launch<1>(args, blocks, s);
+    case 2: return reduce_launch<2>(args, blocks, s);
+    case 3: return reduce_launch<3>(args, blocks, s);
+    case 4: return reduce_launch<4>(args, blocks, s);
+    case 5: return reduce_launch<5>(args, blocks, s);
+    case 6: return reduce_launch<6>(args, blocks, s);
+    case 7: return reduce_launch<7>(args, blocks, s);
+    case 8: return reduce_launch<8>(args, blocks, s);
+    case 9: return reduce_launch<9>(args, blocks, s);
+    case 10: return reduce_launch<10>(args, blocks, s);
+    case 11: return reduce_launch<11>(args, blocks, s);
+    case 12: return reduce_launch<12>(args, blocks, s);
+    case 13: return reduce_launch<13>(args, blocks, s);
+    case 14: return reduce_launch<14>(args, blocks, s);
+    case 15: return reduce_launch<15>(args, blocks, s);
+    default: return reduce_launch<16>(args, blocks, s);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace zc

@@ -46,6 +46,13 @@ __device__ __forceinline__ void set_status(WsHeader* h, uint32_t code) {
   atomicCAS(&h->status, 0u, code);
 }
 
+// Programmatic dependent launch.  A prep kernel lets the kernel after it in
+// the stream be scheduled at once (pdl_trigger); that kernel, launched with
+// programmatic stream serialisation, waits for the prep kernel to finish
+// and its writes to be visible (pdl_wait) before it reads anything.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Streaming 16-byte load (read once, keep out of L1).
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 v;

@@ -36,6 +36,7 @@ __device__ __forceinline__ int64_t floor_div_pos(int64_t a, int64_t b) {  // b >
 // below log2(sigma) for a centred Gaussian.  The block also writes the
 // chunk's code tables for the encoder.
 __global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ SelectArgs a) {
+  pdl_trigger();
   const SelectChunkArg ca = a.c[blockIdx.x];
   const uint32_t ci = a.chunk0 + blockIdx.x;
   __shared__ long long s_sum[8], s_cnt[8];
@@ -789,6 +790,7 @@ __device__ __forceinline__ void store_tile(const EncodeArgs& a, const EncShared&
 }
 
 __global__ void __launch_bounds__(kEncThreads, 1) zc_encode_kernel(EncodeArgs a) {
+  pdl_wait();  // records and tables come from the select kernel
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t s_segstart[kSegs], s_mode[kImgBufs], s_over[kImgBufs], s_size[kImgBufs];
   EncShared S;
@@ -885,10 +887,10 @@ cudaError_t launch_encode(const EncodeArgs& args, uint32_t n_items, cudaStream_t
   }
   // Every CTA must be resident for the look-back order to make progress:
   // the cooperative launch guarantees it (or fails).
-  EncodeArgs a = args;
-  void* params[] = {&a};
   const uint32_t grid = min(n_items, (uint32_t)g_enc_ctas[dev]);
-  return cudaLaunchCooperativeKernel((const void*)zc_encode_kernel, dim3(grid), dim3(kEncThreads), params, kEncSmem, s);
+  cudaLaunchAttribute at[2];
+  const cudaLaunchConfig_t cfg = follow_config(dim3(grid), dim3(kEncThreads), kEncSmem, s, true, at);
+  return cudaLaunchKernelEx(&cfg, zc_encode_kernel, args);
 }
 
 }  // namespace zc

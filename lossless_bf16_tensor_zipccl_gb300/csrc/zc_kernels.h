@@ -83,6 +83,25 @@ struct ReduceArgs {
   uint32_t k;
 };
 
+// Launch configuration of a kernel that follows a prep kernel in the same
+// stream: programmatic stream serialisation lets its CTAs be scheduled while
+// the prep kernel finishes (the kernel waits for it before reading).
+inline cudaLaunchConfig_t follow_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool cooperative,
+                                        cudaLaunchAttribute (&at)[2]) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeCooperative;
+  at[1].val.cooperative = cooperative ? 1 : 0;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cfg;
+}
+
 cudaError_t launch_select(const SelectArgs& args, cudaStream_t s);
 cudaError_t launch_encode(const EncodeArgs& args, uint32_t n_items, cudaStream_t s);
 cudaError_t launch_decode(const DprepArgs& prep, const DecodeArgs& args, uint32_t max_items, cudaStream_t s);
