@@ -118,20 +118,29 @@ struct ExpSource {
   const uint32_t* end;    // one past the last readable word
 };
 
+// Values of row r that this lane holds (col: its first value in a row).
+__device__ __forceinline__ uint32_t lane_count(uint32_t nt, uint32_t col, uint32_t r) {
+  const uint32_t i0 = r * kRow + col;
+  return nt > i0 ? min(8u, nt - i0) : 0u;
+}
+
 // Decode one warp's 8-value lane group of row r into 4 words (8 BF16).
+// kStaged: the payload words are a shared-memory copy (see LaneDecoder).
+template <bool kStaged>
 struct RowSource {
   TileView tv;
-  LaneDecoder dec;
+  LaneDecoder<kStaged> dec;
   uint32_t nt, col;  // col: first value of this lane in a row
 
-  __device__ __forceinline__ void start(const uint32_t* lut, uint32_t base, const ExpSource& xs) {
+  __device__ __forceinline__ void start(const TileView& view, uint32_t n, uint32_t c, const uint32_t* lut,
+                                        uint32_t base, const ExpSource& xs) {
+    tv = view;
+    nt = n;
+    col = c;
     if (tv.mode == 0) dec.init(xs.words, tv.start - xs.bit_base, xs.end, lut, base);
   }
 
-  __device__ __forceinline__ uint32_t count(uint32_t r) const {
-    const uint32_t i0 = r * kRow + col;
-    return nt > i0 ? min(8u, nt - i0) : 0u;
-  }
+  __device__ __forceinline__ uint32_t count(uint32_t r) const { return lane_count(nt, col, r); }
 
   __device__ __forceinline__ uint4 row(uint32_t r, uint2 sm) {
     const uint32_t cnt = count(r);
@@ -282,12 +291,39 @@ __global__ void __launch_bounds__(256) zc_dprep_kernel(DprepArgs a) {
 // sign/mantissa bytes are read straight from global memory (256 contiguous
 // bytes per warp and row, four rows ahead).  Shared memory stays small
 // enough for 14 CTAs per SM, so a whole 64M-value bucket decodes in one wave.
-constexpr uint32_t kExpSlot = 11392;  // staged payload (~2.78 bits/value); larger ones are read in place
+constexpr uint32_t kExpSlot = 11344;  // staged payload (~2.77 bits/value); larger ones are read in place
 constexpr uint32_t kSmAhead = 4;      // rows of sign/mantissa bytes in flight per lane
+
+// The rows of one warp's half tile.  sq: the first kSmAhead rows of this
+// lane's sign/mantissa bytes (full tiles), already in flight.
+template <bool kStaged>
+__device__ __forceinline__ void decode_rows(RowSource<kStaged>& src, bool full, const uint8_t* smp, uint16_t* y,
+                                            bool vec, uint2 (&sq)[kSmAhead]) {
+  if (full) {
+    // full coded tile: every lane has 8 values in every row
+#pragma unroll kSmAhead
+    for (uint32_t r = 0; r < kRows; ++r) {
+      const uint2 sm = sq[r % kSmAhead];
+      if (r + kSmAhead < kRows) sq[r % kSmAhead] = ld_stream_v2(smp + (r + kSmAhead) * kRow);
+      uint32_t elo, ehi;
+      src.dec.fill_warp(8);
+      src.dec.take8(elo, ehi);
+      const uint2 u = merge4(elo, sm.x), v = merge4(ehi, sm.y);
+      *reinterpret_cast<uint4*>(y + r * kRow) = make_uint4(u.x, u.y, v.x, v.y);
+    }
+  } else {
+    const uint32_t rows = (src.nt + kRow - 1) / kRow;
+    for (uint32_t r = 0; r < rows; ++r) {
+      const uint32_t cnt = src.count(r);
+      const uint4 v = src.row(r, load_bytes8(smp + r * kRow, cnt));
+      if (cnt) store_row(y + r * kRow, cnt, vec, v);
+    }
+  }
+}
 
 __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
   pdl_wait();  // chunk records and tables come from the prep kernel
-  __shared__ __align__(128) uint8_t s_exp[kExpSlot];
+  __shared__ __align__(128) uint8_t s_exp[kExpSlot + kStagePad];
   __shared__ __align__(16) uint32_t s_lut[kLutEntries];
   __shared__ __align__(8) uint64_t s_xbar;
   __shared__ uint32_t s_flag[3];
@@ -309,10 +345,9 @@ __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
   const bool chunk_ok = d.ok && k < d.n_tiles;
   const uint32_t nt = chunk_ok ? (uint32_t)min((uint64_t)kTile, d.n - (uint64_t)k * kTile) : 0u;
   const uint8_t* ch = a.stream + d.stream_off;
-  RowSource src;
-  src.nt = nt;
-  src.col = half * kHalf + lane * kLaneElems;
-  const bool ok = chunk_ok && open_tile(ch, d.bytes, d.n_tiles, k, nt, half, lane, src.tv);
+  const uint32_t col = half * kHalf + lane * kLaneElems;
+  TileView tv;
+  const bool ok = chunk_ok && open_tile(ch, d.bytes, d.n_tiles, k, nt, half, lane, tv);
   if (lane == 0) s_flag[1 + half] = ok ? 0u : 1u;
   load_lut(s_lut, a.luts + (size_t)(chunk_ok ? c : 0) * kLutEntries, tid, 64);
   __syncthreads();
@@ -321,19 +356,19 @@ __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
     return;
   }
   // The whole coded payload comes into shared memory with one TMA copy.
-  const uint8_t* payload = src.tv.tile + src.tv.exp_off + kSegTab;
+  const uint8_t* payload = tv.tile + tv.exp_off + kSegTab;
   uint32_t slo = 0;
-  const uint32_t sbytes = src.tv.mode == 0 ? stage_span(src.tv, 0, src.tv.bits, kExpSlot, slo) : 0u;
+  const uint32_t sbytes = tv.mode == 0 ? stage_span(tv, 0, tv.bits, kExpSlot, slo) : 0u;
   if (tid == 0 && sbytes) {
     mbar_init(&s_xbar, 1);
     mbar_arrive_expect_tx(&s_xbar, sbytes);
     bulk_copy_g2s(s_exp, payload, sbytes, &s_xbar);
   }
   const uint64_t e0 = d.elem_start + (uint64_t)k * kTile;
-  uint16_t* y = a.out + e0 + src.col;
+  uint16_t* y = a.out + e0 + col;
   const bool vec = (e0 & 7) == 0;
-  const uint8_t* smp = src.tv.tile + kTileHdr + src.col;  // this lane's sign/mantissa bytes of row 0
-  const bool full = nt == kTile && vec && src.tv.mode == 0;
+  const uint8_t* smp = tv.tile + kTileHdr + col;  // this lane's sign/mantissa bytes of row 0
+  const bool full = nt == kTile && vec && tv.mode == 0;
   uint2 sq[kSmAhead];
   if (full) {
 #pragma unroll
@@ -346,36 +381,17 @@ __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
     if (lane == 0) set_status(a.hdr, kStTimeout);
     return;
   }
-  ExpSource xs;
   if (sbytes) {
-    xs.words = reinterpret_cast<const uint32_t*>(s_exp);
-    xs.bit_base = 0;
-    xs.end = reinterpret_cast<const uint32_t*>(s_exp + sbytes);
+    RowSource<true> src;
+    const ExpSource xs{reinterpret_cast<const uint32_t*>(s_exp), 0u, nullptr};
+    src.start(tv, nt, col, s_lut, d.base, xs);
+    decode_rows(src, full, smp, y, vec, sq);
   } else {
-    xs.words = reinterpret_cast<const uint32_t*>(payload);
-    xs.bit_base = 0;
-    xs.end = reinterpret_cast<const uint32_t*>(src.tv.tile + src.tv.exp_off + pad16(src.tv.exp_bytes));
-  }
-  src.start(s_lut, d.base, xs);
-  if (full) {
-    // full coded tile: every lane has 8 values in every row
-#pragma unroll kSmAhead
-    for (uint32_t r = 0; r < kRows; ++r) {
-      const uint2 sm = sq[r % kSmAhead];
-      if (r + kSmAhead < kRows) sq[r % kSmAhead] = ld_stream_v2(smp + (r + kSmAhead) * kRow);
-      uint32_t elo, ehi;
-      src.dec.fill_warp(8);
-      src.dec.take8(elo, ehi);
-      const uint2 u = merge4(elo, sm.x), v = merge4(ehi, sm.y);
-      *reinterpret_cast<uint4*>(y + r * kRow) = make_uint4(u.x, u.y, v.x, v.y);
-    }
-  } else {
-    const uint32_t rows = (nt + kRow - 1) / kRow;
-    for (uint32_t r = 0; r < rows; ++r) {
-      const uint32_t cnt = src.count(r);
-      const uint4 v = src.row(r, load_bytes8(smp + r * kRow, cnt));
-      if (cnt) store_row(y + r * kRow, cnt, vec, v);
-    }
+    RowSource<false> src;
+    const ExpSource xs{reinterpret_cast<const uint32_t*>(payload), 0u,
+                       reinterpret_cast<const uint32_t*>(tv.tile + tv.exp_off + pad16(tv.exp_bytes))};
+    src.start(tv, nt, col, s_lut, d.base, xs);
+    decode_rows(src, full, smp, y, vec, sq);
   }
 }
 
@@ -441,71 +457,20 @@ constexpr uint32_t kRedStageBytes = kRedRows * kHalf * 2;  // decoded BF16 half 
 constexpr uint32_t kRedSlot = 5696;  // staged half payload per peer (~2.78 bits/value; a multiple of 16 for TMA)
 
 __host__ __device__ constexpr size_t reduce_smem_bytes(uint32_t k) {
-  return (size_t)k * (kRedStageBytes + kRedSlot + 16);
+  return (size_t)k * (kRedStageBytes + kRedSlot + 16) + kStagePad;
 }
 
-// Instantiated per peer count K (1..16), so the fold over the peers unrolls.
-template <uint32_t K>
-__global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
-  pdl_wait();  // peer records and tables come from the prep kernel
-  extern __shared__ __align__(128) uint8_t rsm[];
+// The rows of one half tile: each warp decodes kRedRows rows of its peer
+// into shared memory, then the block folds them.  sq: the first kSmAhead rows
+// of this lane's sign/mantissa bytes, already in flight.
+template <uint32_t K, bool kStaged>
+__device__ __forceinline__ void reduce_rows(RowSource<kStaged>& src, const uint8_t* smp, uint16_t* sbuf,
+                                            uint16_t* y, uint32_t half, uint2 (&sq)[kSmAhead]) {
   const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5, tid = threadIdx.x;
-  const uint32_t t = blockIdx.x >> 1, half = blockIdx.x & 1;
   constexpr uint32_t nthreads = 32 * K;
-  uint16_t* sbuf = reinterpret_cast<uint16_t*>(rsm);                          // k x kRedRows half rows
-  uint8_t* slots = rsm + (size_t)K * kRedStageBytes;                       // k x kRedSlot
-  uint64_t* bars = reinterpret_cast<uint64_t*>(slots + (size_t)K * kRedSlot);  // k x 2
-  __shared__ int s_bad;
-  // one read of the status word per block, so every thread takes the same path
-  if (tid == 0) s_bad = *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0;
-  __syncthreads();
-  if (s_bad) return;
-  const uint32_t nt = (uint32_t)min((uint64_t)kTile, a.n - (uint64_t)t * kTile);
-  const DecChunk d = a.chunks[p];
-  RowSource src;
-  src.nt = nt;
-  src.col = half * kHalf + lane * kLaneElems;
-  const bool ok = d.ok && open_tile(a.peers[p], d.bytes, d.n_tiles, t, nt, half, lane, src.tv);
-  const uint8_t* payload = src.tv.tile + src.tv.exp_off + kSegTab;
-  uint8_t* slot = slots + (size_t)p * kRedSlot;
-  uint64_t* bar = bars + 2 * p;
-  uint32_t slo = 0, sbytes = 0;
-  bool timeout = false;
-  if (ok) {
-    if (src.tv.mode == 0) sbytes = stage_span(src.tv, src.tv.hbit0, src.tv.hbit1, kRedSlot, slo);
-    if (lane == 0 && sbytes) {
-      mbar_init(bar, 1);
-      mbar_arrive_expect_tx(bar, sbytes);
-      bulk_copy_g2s(slot, payload + slo, sbytes, bar);
-    }
-    __syncwarp();
-    timeout = sbytes && !mbar_wait(bar, 0);
-    timeout = __any_sync(kFull, timeout);
-  }
-  if (lane == 0 && (!ok || timeout)) {
-    s_bad = 1;
-    set_status(a.hdr, ok ? kStTimeout : kStCorrupt);
-  }
-  __syncthreads();
-  if (s_bad) return;  // uniform; a copy that did arrive has nothing left in flight
-  ExpSource xs;
-  if (sbytes) {
-    xs.words = reinterpret_cast<const uint32_t*>(slot);
-    xs.bit_base = 8 * slo;
-    xs.end = reinterpret_cast<const uint32_t*>(slot + sbytes);
-  } else {
-    xs.words = reinterpret_cast<const uint32_t*>(payload);
-    xs.bit_base = 0;
-    xs.end = reinterpret_cast<const uint32_t*>(src.tv.tile + src.tv.exp_off + pad16(src.tv.exp_bytes));
-  }
-  src.start(a.luts + (size_t)d.item_start * kLutEntries, d.base, xs);  // item_start: the peer owning the table
+  const uint32_t nt = src.nt;
   uint16_t* mine = sbuf + (size_t)p * kRedRows * kHalf;
-  uint16_t* y = a.out + (uint64_t)t * kTile;
-  const uint8_t* smp = src.tv.tile + kTileHdr + src.col;  // this lane's sign/mantissa bytes of row 0
   const uint32_t rows = (nt + kRow - 1) / kRow;
-  uint2 sq[kSmAhead];
-#pragma unroll
-  for (uint32_t r = 0; r < kSmAhead; ++r) sq[r] = r < rows ? load_bytes8(smp + r * kRow, src.count(r)) : make_uint2(0, 0);
   const bool fast = nt == kTile && src.tv.mode == 0;  // same for every lane of the warp
   for (uint32_t r0 = 0; r0 < rows; r0 += kRedRows) {
     if (fast) {
@@ -553,6 +518,72 @@ __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
       else y[gi] = (uint16_t)o;
     }
     __syncthreads();
+  }
+}
+
+// Instantiated per peer count K (1..16), so the fold over the peers unrolls.
+template <uint32_t K>
+__global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
+  pdl_wait();  // peer records and tables come from the prep kernel
+  extern __shared__ __align__(128) uint8_t rsm[];
+  const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5, tid = threadIdx.x;
+  const uint32_t t = blockIdx.x >> 1, half = blockIdx.x & 1;
+  // k x kRedRows half rows | k x kRedSlot staged payloads | kStagePad | k x 2 barrier words
+  uint16_t* sbuf = reinterpret_cast<uint16_t*>(rsm);
+  uint8_t* slots = rsm + (size_t)K * kRedStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(slots + (size_t)K * kRedSlot + kStagePad);
+  __shared__ int s_bad;
+  // one read of the status word per block, so every thread takes the same path
+  if (tid == 0) s_bad = *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0;
+  __syncthreads();
+  if (s_bad) return;
+  const uint32_t nt = (uint32_t)min((uint64_t)kTile, a.n - (uint64_t)t * kTile);
+  const DecChunk d = a.chunks[p];
+  const uint32_t col = half * kHalf + lane * kLaneElems;
+  TileView tv;
+  const bool ok = d.ok && open_tile(a.peers[p], d.bytes, d.n_tiles, t, nt, half, lane, tv);
+  const uint8_t* payload = tv.tile + tv.exp_off + kSegTab;
+  uint8_t* slot = slots + (size_t)p * kRedSlot;
+  uint64_t* bar = bars + 2 * p;
+  uint32_t slo = 0, sbytes = 0;
+  bool timeout = false;
+  if (ok) {
+    if (tv.mode == 0) sbytes = stage_span(tv, tv.hbit0, tv.hbit1, kRedSlot, slo);
+    if (lane == 0 && sbytes) {
+      mbar_init(bar, 1);
+      mbar_arrive_expect_tx(bar, sbytes);
+      bulk_copy_g2s(slot, payload + slo, sbytes, bar);
+    }
+    __syncwarp();
+    timeout = sbytes && !mbar_wait(bar, 0);
+    timeout = __any_sync(kFull, timeout);
+  }
+  if (lane == 0 && (!ok || timeout)) {
+    s_bad = 1;
+    set_status(a.hdr, ok ? kStTimeout : kStCorrupt);
+  }
+  const uint8_t* smp = tv.tile + kTileHdr + col;  // this lane's sign/mantissa bytes of row 0
+  const uint32_t rows = (nt + kRow - 1) / kRow;
+  uint2 sq[kSmAhead];
+#pragma unroll
+  for (uint32_t r = 0; r < kSmAhead; ++r)
+    sq[r] = ok && r < rows ? load_bytes8(smp + r * kRow, lane_count(nt, col, r)) : make_uint2(0, 0);
+  // every coded peer staged (or raw): the staged decoders for the whole block
+  const bool staged = __syncthreads_and(sbytes != 0 || tv.mode != 0) != 0;
+  if (s_bad) return;  // uniform; a copy that did arrive has nothing left in flight
+  const uint32_t* lut = a.luts + (size_t)d.item_start * kLutEntries;  // item_start: the peer owning the table
+  uint16_t* y = a.out + (uint64_t)t * kTile;
+  if (staged) {
+    RowSource<true> src;
+    const ExpSource xs{reinterpret_cast<const uint32_t*>(slot), 8 * slo, nullptr};
+    src.start(tv, nt, col, lut, d.base, xs);
+    reduce_rows<K>(src, smp, sbuf, y, half, sq);
+  } else {
+    RowSource<false> src;
+    const ExpSource xs{reinterpret_cast<const uint32_t*>(payload), 0u,
+                       reinterpret_cast<const uint32_t*>(tv.tile + tv.exp_off + pad16(tv.exp_bytes))};
+    src.start(tv, nt, col, lut, d.base, xs);
+    reduce_rows<K>(src, smp, sbuf, y, half, sq);
   }
 }
 

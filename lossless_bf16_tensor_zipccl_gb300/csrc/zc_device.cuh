@@ -162,12 +162,13 @@ __host__ __device__ __forceinline__ bool lens_complete(uint64_t lens) {
 
 // Multi-symbol decode table: entry i describes the symbols that the 10-bit
 // window i (next bits of the stream, LSB first) starts with, packed in 32 bits:
-//   bits 0-19  up to 5 symbols, 4 bits each (first symbol lowest)
+//   bits 0-19  up to 5 symbols, 4 bits each (last symbol lowest, so that a
+//              queue shifted left by the entry's width takes them in order)
 //   bits 20-23 bits consumed (<= 10)
-//   bits 24-26 symbols decoded (1..5)
-//   bit  27    the last symbol is the escape
+//   bits 24-28 4 x symbols decoded (4..20): the entry's width in the queue
+//   bit  29    the last symbol is the escape
 // Decoding stops after an escape; its 8 raw bits are not in the window count.
-constexpr uint32_t kLutEsc = 1u << 27;
+constexpr uint32_t kLutEsc = 1u << 29;
 
 __device__ __forceinline__ uint32_t lut_entry(uint32_t idx, uint64_t lens, const uint32_t (&rev)[kNsym]) {
   uint32_t pos = 0, ns = 0, nib = 0, esc = 0;
@@ -184,12 +185,12 @@ __device__ __forceinline__ uint32_t lut_entry(uint32_t idx, uint64_t lens, const
       }
     }
     if (found < 0) break;
-    nib |= (uint32_t)found << (4 * ns);
+    nib = (nib << 4) | (uint32_t)found;
     ++ns;
     pos += flen;
     esc = found == kEsc;
   }
-  return nib | (pos << 20) | (ns << 24) | (esc << 27);
+  return nib | (pos << 20) | ((4 * ns) << 24) | (esc << 29);
 }
 
 // Fill entries [first, first + count) of a 1024-entry table cooperatively
@@ -214,25 +215,38 @@ __device__ __forceinline__ uint2 merge4(uint32_t e4, uint32_t sm4) {
 }
 
 // ---------------------------------------------------------------- lane decoder
+// Readable bytes a staged payload copy needs after its span.  A lane runs at
+// most 8 symbols of at most kLmax + 8 bits past its segment's end (its queue
+// holds 16, the last row takes 8), so its last table step starts before
+// bit E + 144 (E: the span's last payload bit) and reads words up to two past
+// the one holding that bit: less than E / 8 + 31 bytes.
+constexpr uint32_t kStagePad = 48;
+
 // Decodes one segment of a coded tile.  Symbols come 1-5 at a time from a
-// 1024-entry table (shared memory) indexed by the next 10 stream bits; the
-// window is a funnel shift over two words (boff < 32) and a third word is
-// loaded one step ahead.  Words are read through a plain pointer: a copy of
-// the exponent region staged in shared memory, or the region in place in
-// global memory, never past its last word.  Up to 16 decoded symbols wait as
-// nibbles in a 64-bit accumulator, so a lane can decode ahead of the row its
-// warp emits; escape exponents wait as bytes in esc0..esc3 with a mask.
+// 1024-entry table indexed by the next 10 stream bits; the window is a
+// funnel shift over two words (boff < 32) and a third word is loaded one step
+// ahead.  kStaged: the words are a copy in shared memory followed by at least
+// kStagePad readable bytes, so loads need no bound; otherwise they are the
+// region in place in global memory, never read past `end`.  Up to 16
+// decoded symbols wait as nibbles in a 64-bit queue (qhi:qlo, newest lowest;
+// a table entry enters it with one left shift by its own width), so a lane
+// can decode ahead of the row its warp emits; escape exponents wait as bytes
+// in esc0..esc3 with a mask, indexed by queue position from the oldest
+// pending symbol.
+template <bool kStaged>
 struct LaneDecoder {
   const uint32_t* wp;    // next word to load
-  const uint32_t* wend;  // one past the last readable word
+  const uint32_t* wend;  // one past the last readable word (in place)
   const uint32_t* lut;
-  uint64_t acc;
-  uint32_t w0, w1, w2, boff, cnt;
+  uint32_t qlo, qhi;     // pending symbols; the oldest at nibble cnt4 / 4 - 1
+  uint32_t w0, w1, w2, boff, cnt4;  // cnt4: 4 x pending symbols
   uint32_t escm, esc0, esc1, esc2, esc3;
   uint32_t base4;
 
   __device__ __forceinline__ uint32_t next_word() {
-    const uint32_t w = wp < wend ? *wp : 0u;
+    uint32_t w;
+    if constexpr (kStaged) w = *wp;
+    else w = wp < wend ? *wp : 0u;
     ++wp;
     return w;
   }
@@ -248,8 +262,8 @@ struct LaneDecoder {
     w1 = next_word();
     w2 = next_word();
     boff = start & 31;
-    acc = 0;
-    cnt = 0;
+    qlo = qhi = 0;
+    cnt4 = 0;
     escm = esc0 = esc1 = esc2 = esc3 = 0;
     base4 = base * 0x01010101u;
   }
@@ -265,15 +279,17 @@ struct LaneDecoder {
     escm |= 1u << p;
   }
 
-  // One table step.  Requires cnt <= 11 (room for 5 more symbols).
+  // One table step.  Requires cnt4 <= 44 (room for 5 more symbols).
   __device__ __forceinline__ void step() {
     const uint32_t win = __funnelshift_r(w0, w1, boff);
     const uint32_t en = lut[win & (kLutEntries - 1)];
-    acc |= (uint64_t)(en & 0xFFFFFu) << (4 * cnt);
+    const uint32_t sh = (en >> 24) & 31u;
+    qhi = __funnelshift_l(qlo, qhi, sh);
+    qlo = (qlo << sh) | (en & 0xFFFFFu);
+    cnt4 += sh;
     uint32_t nb = (en >> 20) & 15u;
-    cnt += (en >> 24) & 7u;
     if (__builtin_expect((en & kLutEsc) != 0, 0)) {
-      place_escape(cnt - 1, (win >> nb) & 0xFFu);
+      place_escape((cnt4 >> 2) - 1, (win >> nb) & 0xFFu);
       nb += 8;
     }
     boff += nb;
@@ -289,19 +305,21 @@ struct LaneDecoder {
   // <= 8); lanes that are there already keep decoding while they have room,
   // so the next row starts ahead.  All 32 lanes must call this together.
   __device__ __forceinline__ void fill_warp(uint32_t need) {
-    if (cnt <= 11) step();
-    if (cnt <= 11) step();
-    while (__any_sync(kFull, cnt < need)) {
-      if (cnt <= 11) step();
+    if (cnt4 <= 44) step();
+    if (cnt4 <= 44) step();
+    while (__any_sync(kFull, cnt4 < 4 * need)) {
+      if (cnt4 <= 44) step();
     }
   }
 
-  // Pop 8 pending symbols as exponent bytes (e0..e3, e4..e7).
+  // Pop 8 pending symbols as exponent bytes (e0..e3, e4..e7); with fewer
+  // pending (a segment's last row) the missing ones are garbage.
   __device__ __forceinline__ void take8(uint32_t& e_lo, uint32_t& e_hi) {
-    const uint32_t lo = (uint32_t)acc;
-    const uint32_t ev = lo & 0x0F0F0F0Fu, od = (lo >> 4) & 0x0F0F0F0Fu;
-    e_lo = __byte_perm(ev, od, 0x5140) + base4;
-    e_hi = __byte_perm(ev, od, 0x7362) + base4;
+    // the oldest 8 symbols, oldest in the top nibble
+    const uint32_t e32 = cnt4 >= 32 ? __funnelshift_rc(qlo, qhi, cnt4 - 32) : __funnelshift_lc(0u, qlo, 32 - cnt4);
+    const uint32_t ev = e32 & 0x0F0F0F0Fu, od = (e32 >> 4) & 0x0F0F0F0Fu;
+    e_lo = __byte_perm(ev, od, 0x2637) + base4;
+    e_hi = __byte_perm(ev, od, 0x0415) + base4;
     if (__builtin_expect((escm & 0xFFu) != 0, 0)) {  // substitute the raw exponents of escapes
       const uint32_t m = escm;
       const uint32_t m0 = (m & 1 ? 0xFFu : 0u) | (m & 2 ? 0xFF00u : 0u) | (m & 4 ? 0xFF0000u : 0u) |
@@ -311,8 +329,7 @@ struct LaneDecoder {
       e_lo = (e_lo & ~m0) | (esc0 & m0);
       e_hi = (e_hi & ~m1) | (esc1 & m1);
     }
-    acc >>= 32;
-    cnt = cnt > 8 ? cnt - 8 : 0;  // fewer than 8 only on a segment's last row
+    cnt4 = cnt4 > 32 ? cnt4 - 32 : 0;  // fewer than 8 only on a segment's last row
     esc0 = esc2;
     esc1 = esc3;
     esc2 = esc3 = 0;
