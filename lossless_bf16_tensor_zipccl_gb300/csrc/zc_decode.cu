@@ -448,16 +448,17 @@ __device__ __forceinline__ void add_bf16x2(float& a0, float& a1, uint32_t w) {
 // bits of its peer's half tile in shared memory with one TMA bulk copy,
 // decodes kRedRows half rows at a time into shared memory (peer-major) with
 // the sign/mantissa bytes read straight from global memory, then every
-// thread folds pairs of values across the peers in rank order.  Decode
-// tables are read through L1 (peers with the same code lengths share one
-// table), so a block of 8 peers needs 54 KB of shared memory and 4 blocks
-// fit per SM: a 64M-element reduce (512 half tiles) runs in one wave.
+// thread folds pairs of values across the peers in rank order.  Peers with
+// the same code lengths share one decode table; when all share peer 0's, it
+// sits in shared memory, else the tables are read through L1.  A block of 8
+// peers needs 56 KB of shared memory and 4 blocks fit per SM: a 64M-element
+// reduce (512 half tiles) runs in one wave.
 constexpr uint32_t kRedRows = 2;
 constexpr uint32_t kRedStageBytes = kRedRows * kHalf * 2;  // decoded BF16 half rows per peer
-constexpr uint32_t kRedSlot = 5696;  // staged half payload per peer (~2.78 bits/value; a multiple of 16 for TMA)
+constexpr uint32_t kRedSlot = 5584;  // staged half payload per peer (~2.72 bits/value; a multiple of 16 for TMA)
 
 __host__ __device__ constexpr size_t reduce_smem_bytes(uint32_t k) {
-  return (size_t)k * (kRedStageBytes + kRedSlot + 16) + kStagePad;
+  return kLutEntries * 4 + (size_t)k * (kRedStageBytes + kRedSlot + 16) + kStagePad;
 }
 
 // The rows of one half tile: each warp decodes kRedRows rows of its peer
@@ -528,9 +529,11 @@ __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
   extern __shared__ __align__(128) uint8_t rsm[];
   const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5, tid = threadIdx.x;
   const uint32_t t = blockIdx.x >> 1, half = blockIdx.x & 1;
-  // k x kRedRows half rows | k x kRedSlot staged payloads | kStagePad | k x 2 barrier words
-  uint16_t* sbuf = reinterpret_cast<uint16_t*>(rsm);
-  uint8_t* slots = rsm + (size_t)K * kRedStageBytes;
+  // peer 0's decode table | k x kRedRows half rows | k x kRedSlot staged
+  // payloads | kStagePad | k x 2 barrier words
+  uint32_t* s_lut = reinterpret_cast<uint32_t*>(rsm);
+  uint16_t* sbuf = reinterpret_cast<uint16_t*>(rsm + kLutEntries * 4);
+  uint8_t* slots = reinterpret_cast<uint8_t*>(sbuf) + (size_t)K * kRedStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(slots + (size_t)K * kRedSlot + kStagePad);
   __shared__ int s_bad;
   // one read of the status word per block, so every thread takes the same path
@@ -568,15 +571,23 @@ __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
 #pragma unroll
   for (uint32_t r = 0; r < kSmAhead; ++r)
     sq[r] = ok && r < rows ? load_bytes8(smp + r * kRow, lane_count(nt, col, r)) : make_uint2(0, 0);
-  // every coded peer staged (or raw): the staged decoders for the whole block
+  if (p == 0 && d.ok) load_lut(s_lut, a.luts, lane, 32);  // peer 0 always owns its table
+  // Decoders for the whole block: staged when every coded peer is staged (a
+  // raw peer has none), with peer 0's table in shared memory when every peer
+  // uses it (item_start: the peer owning a peer's table).
   const bool staged = __syncthreads_and(sbytes != 0 || tv.mode != 0) != 0;
+  const bool one_table = __syncthreads_and(d.item_start == 0) != 0;
   if (s_bad) return;  // uniform; a copy that did arrive has nothing left in flight
-  const uint32_t* lut = a.luts + (size_t)d.item_start * kLutEntries;  // item_start: the peer owning the table
+  const uint32_t* lut = a.luts + (size_t)d.item_start * kLutEntries;
   uint16_t* y = a.out + (uint64_t)t * kTile;
-  if (staged) {
+  const ExpSource sx{reinterpret_cast<const uint32_t*>(slot), 8 * slo, nullptr};
+  if (staged && one_table) {
     RowSource<true> src;
-    const ExpSource xs{reinterpret_cast<const uint32_t*>(slot), 8 * slo, nullptr};
-    src.start(tv, nt, col, lut, d.base, xs);
+    src.start(tv, nt, col, s_lut, d.base, sx);
+    reduce_rows<K>(src, smp, sbuf, y, half, sq);
+  } else if (staged) {
+    RowSource<true> src;
+    src.start(tv, nt, col, lut, d.base, sx);
     reduce_rows<K>(src, smp, sbuf, y, half, sq);
   } else {
     RowSource<false> src;

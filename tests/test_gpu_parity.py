@@ -148,6 +148,19 @@ def test_reduce_parity(k, n):
     assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), ref)
 
 
+def test_reduce_peers_with_different_tables():
+    # scales a decade apart land on different code phases, so the peers'
+    # code lengths (chunk header bytes 24..31) and decode tables differ
+    n = 70001
+    xs = [workloads.gaussian_bf16(n, s, 77, p) for p, s in enumerate([1e-2, 1e-1, 1.0, 10.0])]
+    chunks = oracle_chunks(xs)
+    assert len({bytes(c[24:32]) for c in chunks}) > 1
+    ref = oracle.decompress_reduce(chunks, n)
+    y = zc.decompress_reduce(dev_chunks(chunks), n)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), ref)
+
+
 def test_reduce_raw_and_coded_tiles_mixed():
     n = 100000
     a = workloads.gaussian_bf16(n, 0.3, 1)
