@@ -170,37 +170,50 @@ __host__ __device__ __forceinline__ bool lens_complete(uint64_t lens) {
 // Decoding stops after an escape; its 8 raw bits are not in the window count.
 constexpr uint32_t kLutEsc = 1u << 29;
 
-__device__ __forceinline__ uint32_t lut_entry(uint32_t idx, uint64_t lens, const uint32_t (&rev)[kNsym]) {
-  uint32_t pos = 0, ns = 0, nib = 0, esc = 0;
-#pragma unroll 1
-  while (ns < 5 && !esc) {
-    int found = -1;
-    uint32_t flen = 0;
-#pragma unroll
-    for (int s = 0; s < kNsym; ++s) {
-      const uint32_t l = (uint32_t)((lens >> (4 * s)) & 15);
-      if (l + pos <= (uint32_t)kLmax && ((idx >> pos) & ((1u << l) - 1u)) == rev[s]) {
-        found = s;
-        flen = l;
-      }
-    }
-    if (found < 0) break;
-    nib = (nib << 4) | (uint32_t)found;
-    ++ns;
-    pos += flen;
-    esc = found == kEsc;
-  }
-  return nib | (pos << 20) | ((4 * ns) << 24) | (esc << 29);
-}
-
-// Fill entries [first, first + count) of a 1024-entry table cooperatively
-// (all threads of the block).  Building a table is compute-bound, so it is
-// split across several blocks.
+// Fill entries [first, first + count) of a 1024-entry table; every thread
+// of the block calls it, with complete lengths (lens_complete holds).  First
+// the symbol that each 10-bit window starts with is found by matching the
+// reversed codewords (the code is complete, so exactly one matches); then
+// each entry chains up to five lookups in that first-symbol table.  A symbol
+// found in the window shifted right by pos bits is real only if it ends
+// within the 10 bits, since the shift brings in zeros from above.  Building
+// a table is still split across several blocks.
 __device__ __forceinline__ void build_lut(uint64_t lens, uint32_t* lut, uint32_t first, uint32_t count) {
-  uint32_t rev[kNsym];
+  __shared__ uint32_t s_rev[kNsym];
+  __shared__ uint8_t s_sym[kLutEntries];
+  if (threadIdx.x < (uint32_t)kNsym) {
+    const int s = (int)threadIdx.x;
+    s_rev[s] = bit_reverse(canonical_code(lens, s), (int)((lens >> (4 * s)) & 15));
+  }
+  __syncthreads();
+  uint32_t rev[kNsym], len[kNsym];
 #pragma unroll
-  for (int s = 0; s < kNsym; ++s) rev[s] = bit_reverse(canonical_code(lens, s), (int)((lens >> (4 * s)) & 15));
-  for (uint32_t i = threadIdx.x; i < count; i += blockDim.x) lut[first + i] = lut_entry(first + i, lens, rev);
+  for (int s = 0; s < kNsym; ++s) {
+    rev[s] = s_rev[s];
+    len[s] = (uint32_t)((lens >> (4 * s)) & 15);
+  }
+  for (uint32_t w = threadIdx.x; w < kLutEntries; w += blockDim.x) {
+    uint32_t sym = 0;
+#pragma unroll
+    for (int s = 0; s < kNsym; ++s)
+      if ((w & ((1u << len[s]) - 1u)) == rev[s]) sym = (uint32_t)s;
+    s_sym[w] = (uint8_t)sym;
+  }
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < count; i += blockDim.x) {
+    const uint32_t idx = first + i;
+    uint32_t pos = 0, ns = 0, nib = 0, esc = 0;
+    while (ns < 5 && !esc) {
+      const uint32_t s = s_sym[idx >> pos];
+      const uint32_t l = (uint32_t)((lens >> (4 * s)) & 15);
+      if (pos + l > (uint32_t)kLmax) break;
+      nib = (nib << 4) | s;
+      ++ns;
+      pos += l;
+      esc = s == (uint32_t)kEsc;
+    }
+    lut[idx] = nib | (pos << 20) | ((4 * ns) << 24) | (esc << 29);
+  }
 }
 
 // ---------------------------------------------------------------- merge
