@@ -525,7 +525,6 @@ __device__ __forceinline__ void reduce_rows(RowSource<kStaged>& src, const uint8
 // Instantiated per peer count K (1..16), so the fold over the peers unrolls.
 template <uint32_t K>
 __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
-  pdl_wait();  // peer records and tables come from the prep kernel
   extern __shared__ __align__(128) uint8_t rsm[];
   const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5, tid = threadIdx.x;
   const uint32_t t = blockIdx.x >> 1, half = blockIdx.x & 1;
@@ -536,41 +535,49 @@ __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
   uint8_t* slots = reinterpret_cast<uint8_t*>(sbuf) + (size_t)K * kRedStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(slots + (size_t)K * kRedSlot + kStagePad);
   __shared__ int s_bad;
-  // one read of the status word per block, so every thread takes the same path
-  if (tid == 0) s_bad = *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0;
+  if (tid == 0) s_bad = 0;
   __syncthreads();
-  if (s_bad) return;
+  // While the prep kernel runs: locate this half tile in the peer's chunk,
+  // start the copy of its payload and the first sign/mantissa loads.  These
+  // reads are bounded by the caller's byte count alone; the header is
+  // validated by the prep kernel, and its tile count is checked against the
+  // one used here after the wait.
   const uint32_t nt = (uint32_t)min((uint64_t)kTile, a.n - (uint64_t)t * kTile);
-  const DecChunk d = a.chunks[p];
+  const uint8_t* ch = a.peers[p];
+  const uint64_t bytes = a.bytes[p];
+  const uint32_t n_tiles = bytes >= kChunkHdr ? ld_u32(ch + 16) : 0u;
   const uint32_t col = half * kHalf + lane * kLaneElems;
-  TileView tv;
-  const bool ok = d.ok && open_tile(a.peers[p], d.bytes, d.n_tiles, t, nt, half, lane, tv);
+  TileView tv = {};
+  const bool located = t < n_tiles && kChunkHdr + 4ull * (t + 1) <= bytes &&  // same for the whole warp
+                       open_tile(ch, bytes, n_tiles, t, nt, half, lane, tv);
   const uint8_t* payload = tv.tile + tv.exp_off + kSegTab;
   uint8_t* slot = slots + (size_t)p * kRedSlot;
   uint64_t* bar = bars + 2 * p;
   uint32_t slo = 0, sbytes = 0;
-  bool timeout = false;
-  if (ok) {
-    if (tv.mode == 0) sbytes = stage_span(tv, tv.hbit0, tv.hbit1, kRedSlot, slo);
-    if (lane == 0 && sbytes) {
-      mbar_init(bar, 1);
-      mbar_arrive_expect_tx(bar, sbytes);
-      bulk_copy_g2s(slot, payload + slo, sbytes, bar);
-    }
-    __syncwarp();
-    timeout = sbytes && !mbar_wait(bar, 0);
-    timeout = __any_sync(kFull, timeout);
+  if (located && tv.mode == 0) sbytes = stage_span(tv, tv.hbit0, tv.hbit1, kRedSlot, slo);
+  if (lane == 0 && sbytes) {
+    mbar_init(bar, 1);
+    mbar_arrive_expect_tx(bar, sbytes);
+    bulk_copy_g2s(slot, payload + slo, sbytes, bar);
   }
-  if (lane == 0 && (!ok || timeout)) {
-    s_bad = 1;
-    set_status(a.hdr, ok ? kStTimeout : kStCorrupt);
-  }
+  __syncwarp();
   const uint8_t* smp = tv.tile + kTileHdr + col;  // this lane's sign/mantissa bytes of row 0
   const uint32_t rows = (nt + kRow - 1) / kRow;
   uint2 sq[kSmAhead];
 #pragma unroll
   for (uint32_t r = 0; r < kSmAhead; ++r)
-    sq[r] = ok && r < rows ? load_bytes8(smp + r * kRow, lane_count(nt, col, r)) : make_uint2(0, 0);
+    sq[r] = located && r < rows ? load_bytes8(smp + r * kRow, lane_count(nt, col, r)) : make_uint2(0, 0);
+
+  pdl_wait();  // peer records and tables come from the prep kernel
+  const bool timeout = __any_sync(kFull, sbytes && !mbar_wait(bar, 0));
+  const DecChunk d = a.chunks[p];
+  const bool ok = located && d.ok && d.n_tiles == n_tiles;
+  // one read of the status word per block, so every thread takes the same path
+  if (tid == 0 && *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0) s_bad = 1;
+  if (lane == 0 && (!ok || timeout)) {
+    s_bad = 1;
+    set_status(a.hdr, ok ? kStTimeout : kStCorrupt);
+  }
   if (p == 0 && d.ok) load_lut(s_lut, a.luts, lane, 32);  // peer 0 always owns its table
   // Decoders for the whole block: staged when every coded peer is staged (a
   // raw peer has none), with peer 0's table in shared memory when every peer
