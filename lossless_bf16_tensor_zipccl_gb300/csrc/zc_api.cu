@@ -229,6 +229,7 @@ zipccl_status zipccl_decompress(const void* d_stream, const uint64_t* d_chunk_of
   pa.n = n;
   DecodeArgs da;
   da.stream = pa.stream;
+  da.offsets = d_chunk_offsets;
   da.chunks = pa.chunks;
   da.item_start = pa.item_start;
   da.luts = pa.luts;

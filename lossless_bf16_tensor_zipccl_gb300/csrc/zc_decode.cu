@@ -321,66 +321,137 @@ __device__ __forceinline__ void decode_rows(RowSource<kStaged>& src, bool full, 
   }
 }
 
+// Chunks up to this count are found by each decode CTA itself while the prep
+// kernel runs (one offset and one header per thread of the 64-thread CTA).
+constexpr uint32_t kEarlyChunks = 64;
+
 __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
-  pdl_wait();  // chunk records and tables come from the prep kernel
   __shared__ __align__(128) uint8_t s_exp[kExpSlot + kStagePad];
   __shared__ __align__(16) uint32_t s_lut[kLutEntries];
   __shared__ __align__(8) uint64_t s_xbar;
   __shared__ uint32_t s_flag[3];
+  __shared__ uint32_t s_map[2];  // early chunk search: chunk + 1 (0: none), first tile of the chunk
+  __shared__ uint32_t s_wtot;    // early chunk search: warp 0's tile total
   const uint32_t tid = threadIdx.x, lane = tid & 31, half = tid >> 5;
   const uint32_t item = blockIdx.x;
+  const uint32_t col = half * kHalf + lane * kLaneElems;
+  if (tid == 0) s_map[0] = 0;
+  __syncthreads();
+
+  // This tile's chunk c and index k in it; its tile view, payload copy and
+  // first sign/mantissa loads.
+  uint32_t c = 0, k = 0, nt = 0, n_tiles = 0, sbytes = 0;
+  const uint8_t* ch = nullptr;
+  TileView tv = {};
+  bool located = false;
+  uint2 sq[kSmAhead];
+  auto locate = [&](uint64_t chunk_bytes, uint64_t chunk_n) {
+    nt = (uint32_t)min((uint64_t)kTile, chunk_n - (uint64_t)k * kTile);
+    located = k < n_tiles && kChunkHdr + 4ull * (k + 1) <= chunk_bytes &&  // same in every thread
+              open_tile(ch, chunk_bytes, n_tiles, k, nt, half, lane, tv);
+    uint32_t slo = 0;
+    sbytes = located && tv.mode == 0 ? stage_span(tv, 0, tv.bits, kExpSlot, slo) : 0u;  // the same in both warps
+    if (tid == 0 && sbytes) {
+      mbar_init(&s_xbar, 1);
+      mbar_arrive_expect_tx(&s_xbar, sbytes);
+      bulk_copy_g2s(s_exp, tv.tile + tv.exp_off + kSegTab, sbytes, &s_xbar);
+    }
+    if (located && nt == kTile && tv.mode == 0) {
+      const uint8_t* smp = tv.tile + kTileHdr + col;
+#pragma unroll
+      for (uint32_t r = 0; r < kSmAhead; ++r) sq[r] = ld_stream_v2(smp + r * kRow);
+    }
+  };
+
+  // While the prep kernel runs (few chunks): the prefix of tile counts over
+  // the chunks, as the prep kernel forms it, from the caller's offsets and
+  // the headers' value counts.  Reads stay within the chunks' extents; after
+  // the wait the prep kernel's validated records must agree.
+  uint32_t early_first = 0;
+  if (a.n_chunks <= kEarlyChunks) {
+    uint32_t tiles = 0;
+    uint64_t o0 = 0, o1 = 0, cn = 0;
+    if (tid < a.n_chunks) {
+      o0 = a.offsets[tid];
+      o1 = a.offsets[tid + 1];
+      if (o1 >= o0 + kChunkHdr && o1 <= a.offsets[a.n_chunks] && !(o0 & 15)) {
+        cn = ld_u64(a.stream + o0 + 8);
+        tiles = cn < (1ull << 40) ? (uint32_t)tiles_of(cn) : 0u;
+      }
+    }
+    uint32_t incl = tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= (uint32_t)o) incl += y;
+    }
+    if (tid == 31) s_wtot = incl;
+    __syncthreads();
+    if (half) incl += s_wtot;
+    const uint32_t excl = incl - tiles;
+    if (tid < a.n_chunks && item >= excl && item < incl) {  // at most one thread
+      s_map[0] = tid + 1;
+      s_map[1] = excl;
+    }
+    __syncthreads();
+    if (s_map[0]) {
+      c = s_map[0] - 1;
+      early_first = s_map[1];
+      k = item - early_first;
+      const uint64_t c0 = a.offsets[c], c1 = a.offsets[c + 1];
+      ch = a.stream + c0;
+      n_tiles = ld_u32(ch + 16);
+      locate(c1 - c0, ld_u64(ch + 8));
+    }
+  }
+  const bool early = s_map[0] != 0;
+
+  pdl_wait();  // chunk records and tables come from the prep kernel
   // one read of the status word per block, so both warps take the same path
   if (tid == 0) s_flag[0] = *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0 || item >= a.hdr->total_items;
   __syncthreads();
-  if (s_flag[0]) return;
-  uint32_t lo = 0, hi = a.n_chunks;  // largest c with item_start[c] <= item
-  while (hi - lo > 1) {
-    const uint32_t mid = (lo + hi) >> 1;
-    if (a.item_start[mid] <= item) lo = mid;
-    else hi = mid;
-  }
-  const uint32_t c = lo;
-  const DecChunk d = a.chunks[c];
-  const uint32_t k = item - a.item_start[c];
-  const bool chunk_ok = d.ok && k < d.n_tiles;
-  const uint32_t nt = chunk_ok ? (uint32_t)min((uint64_t)kTile, d.n - (uint64_t)k * kTile) : 0u;
-  const uint8_t* ch = a.stream + d.stream_off;
-  const uint32_t col = half * kHalf + lane * kLaneElems;
-  TileView tv;
-  const bool ok = chunk_ok && open_tile(ch, d.bytes, d.n_tiles, k, nt, half, lane, tv);
-  if (lane == 0) s_flag[1 + half] = ok ? 0u : 1u;
-  load_lut(s_lut, a.luts + (size_t)(chunk_ok ? c : 0) * kLutEntries, tid, 64);
-  __syncthreads();
-  if (s_flag[1] | s_flag[2]) {
-    if (tid == 0) set_status(a.hdr, kStCorrupt);
+  if (s_flag[0]) {
+    if (tid == 0 && sbytes) mbar_wait(&s_xbar, 0);  // nothing left in flight
     return;
   }
-  // The whole coded payload comes into shared memory with one TMA copy.
-  const uint8_t* payload = tv.tile + tv.exp_off + kSegTab;
-  uint32_t slo = 0;
-  const uint32_t sbytes = tv.mode == 0 ? stage_span(tv, 0, tv.bits, kExpSlot, slo) : 0u;
-  if (tid == 0 && sbytes) {
-    mbar_init(&s_xbar, 1);
-    mbar_arrive_expect_tx(&s_xbar, sbytes);
-    bulk_copy_g2s(s_exp, payload, sbytes, &s_xbar);
+  if (!early) {
+    uint32_t lo = 0, hi = a.n_chunks;  // largest c with item_start[c] <= item
+    while (hi - lo > 1) {
+      const uint32_t mid = (lo + hi) >> 1;
+      if (a.item_start[mid] <= item) lo = mid;
+      else hi = mid;
+    }
+    c = lo;
+  }
+  const DecChunk d = a.chunks[c];
+  bool ok;
+  if (early) {
+    ok = d.ok && d.n_tiles == n_tiles && a.item_start[c] == early_first && located;
+  } else {
+    k = item - a.item_start[c];
+    ok = d.ok && k < d.n_tiles;
+    if (ok) {
+      ch = a.stream + d.stream_off;
+      n_tiles = d.n_tiles;
+      locate(d.bytes, d.n);
+      ok = located;
+    }
+  }
+  if (lane == 0) s_flag[1 + half] = ok ? 0u : 1u;
+  load_lut(s_lut, a.luts + (size_t)(d.ok ? c : 0) * kLutEntries, tid, 64);
+  __syncthreads();  // the table is in place; the payload barrier is initialised
+  const bool bad = s_flag[1] | s_flag[2];
+  const bool timeout = sbytes && __any_sync(kFull, !mbar_wait(&s_xbar, 0));
+  if (bad || timeout) {
+    // the copy has arrived or was given up on; the status tells the caller
+    if (lane == 0) set_status(a.hdr, bad ? kStCorrupt : kStTimeout);
+    return;
   }
   const uint64_t e0 = d.elem_start + (uint64_t)k * kTile;
   uint16_t* y = a.out + e0 + col;
   const bool vec = (e0 & 7) == 0;
   const uint8_t* smp = tv.tile + kTileHdr + col;  // this lane's sign/mantissa bytes of row 0
   const bool full = nt == kTile && vec && tv.mode == 0;
-  uint2 sq[kSmAhead];
-  if (full) {
-#pragma unroll
-    for (uint32_t r = 0; r < kSmAhead; ++r) sq[r] = ld_stream_v2(smp + r * kRow);
-  }
-  __syncthreads();  // the payload barrier is initialised
-  const bool timeout = sbytes && __any_sync(kFull, !mbar_wait(&s_xbar, 0));
-  if (timeout) {
-    // the copy never arrived: skip the rows; the status tells the caller
-    if (lane == 0) set_status(a.hdr, kStTimeout);
-    return;
-  }
   if (sbytes) {
     RowSource<true> src;
     const ExpSource xs{reinterpret_cast<const uint32_t*>(s_exp), 0u, nullptr};
@@ -388,7 +459,7 @@ __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
     decode_rows(src, full, smp, y, vec, sq);
   } else {
     RowSource<false> src;
-    const ExpSource xs{reinterpret_cast<const uint32_t*>(payload), 0u,
+    const ExpSource xs{reinterpret_cast<const uint32_t*>(tv.tile + tv.exp_off + kSegTab), 0u,
                        reinterpret_cast<const uint32_t*>(tv.tile + tv.exp_off + pad16(tv.exp_bytes))};
     src.start(tv, nt, col, s_lut, d.base, xs);
     decode_rows(src, full, smp, y, vec, sq);

@@ -64,6 +64,7 @@ struct DprepArgs {
 
 struct DecodeArgs {
   const uint8_t* stream;
+  const uint64_t* offsets;  // the caller's chunk offsets (n_chunks + 1)
   const DecChunk* chunks;
   const uint32_t* item_start;
   const uint32_t* luts;
