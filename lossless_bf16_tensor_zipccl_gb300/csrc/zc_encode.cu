@@ -152,34 +152,40 @@ __global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ 
 //
 // Single pass over the input: a row warp reads its rows once (the loads were
 // issued one tile earlier), writes the sign/mantissa bytes into the tile
-// image and packs each lane's codewords into a private word buffer in shared
-// memory (bit 0 of the part at bit 0 of word 0) -- phase A.  The layout warp
-// (warp 16) then places the segments and publishes the tile's size -- phase
-// B; each lane copies its part to its bit position with funnel shifts: words
-// that only this part touches are stored, the two end words are OR-ed --
-// phase D.  A part longer than its private buffer (a lane with many escapes)
-// sends the tile down a slower path that re-reads its input and packs in
-// place; a raw tile re-reads its input to store the exponent bytes.
+// image and packs each lane's codewords into its part slot, in the upper
+// half of the image's exponent region (bit 0 of the part at bit 0 of word
+// 0) -- phase A.  The layout warp (warp 16) then places the segments and
+// publishes the tile's size -- phase B; each lane copies its part to its bit
+// position in the lower half with funnel shifts -- phase D.  A row warp runs
+// phase D of a tile after phase A of the next one, so it does not wait for
+// the slowest row warp and the layout warp in between.  Parts fit their
+// slots at up to 4 bits per value, so a coded stream of fitting parts is at
+// most 16 KB and never reaches the slots; a part longer than its slot (a lane
+// with many escapes) sends the tile down a slower path that re-reads its
+// input and packs in place; a raw tile re-reads its input to store the
+// exponent bytes.
 //
 // The store warp (warp 17) runs the look-back for the tile's byte offset,
 // writes the chunk header, tile table and chunk offsets, and stores the tile
 // image with one TMA bulk copy -- phases C and E -- up to two tiles behind
 // the row warps: the image is triple-buffered.  Named barriers hand tiles
 // between the roles (i = tile number within the CTA, b = i mod 3):
-//   kBarParts     row warps arrive after phase A; the layout warp waits;
-//   kBarSeg       the layout warp arrives after phase B; row warps wait;
-//   kBarB0 + b    the layout warp arrives after phase B; the store warp waits;
-//   kBarImg0 + b  row warps arrive after phase D; the store warp waits;
-//   kBarFree0 + b the store warp arrives once image b has been read by its
-//                 store; row warps wait before packing tile i + 3 into it.
-// A barrier that a role may reach again before the other role has waited
-// gets one id per buffer, so arrivals of different tiles never mix.
+//   kBarParts0 + b  row warps arrive after phase A; the layout warp waits;
+//   kBarSeg0 + b    the layout warp arrives after phase B; row warps wait
+//                   before phase D (after phase A of tile i + 1);
+//   kBarB0 + b      the layout warp arrives after phase B; the store warp
+//                   waits;
+//   kBarImg0 + b    row warps arrive after phase D; the store warp waits;
+//   kBarFree0 + b   the store warp arrives once image b has been read by its
+//                   store; row warps wait before packing tile i + 3 into it.
+// Each barrier has one id per buffer, since a role may reach it again
+// before the other role has waited; barrier 0 is the block barrier.
 //
 // Shared memory: 3 tile images (header | sign/mantissa plane | exponent
-// region) | private part buffers | 3 code tables | per-(row warp, lane) bit
-// counts | 3 x per-(row warp, lane) first word of each part.
-constexpr uint32_t kImgBytes = kTileHdr + kTile + kTile;
-constexpr uint32_t kImgBufs = 3;
+// region with the part slots above kSlotOff) | 4 code tables (the layout
+// warp stages tile i + 2's while tile i - 1's may still be in use) |
+// per buffer: per-(row warp, lane) part bits, then offsets | per buffer:
+// per-(row warp, lane) first word of each part.
 constexpr int kRowWarpsPerHalf = 8;
 constexpr int kRowWarps = 2 * kRowWarpsPerHalf;
 constexpr int kLayoutWarp = kRowWarps;
@@ -189,9 +195,16 @@ constexpr uint32_t kBarThreads = kRowThreads + 32;      // row warps + one role 
 constexpr int kRowsPerWarp = kRows / kRowWarpsPerHalf;   // 8
 constexpr uint32_t kPrivWords = 8;                        // 256 bits per lane part (4 bits per value)
 constexpr uint32_t kPrivBytes = kRowWarps * 32 * kPrivWords * 4;
-constexpr uint32_t kEncSmem =
-    kImgBufs * kImgBytes + kPrivBytes + kImgBufs * kEncTableWords * 4 + kRowWarps * 32 * 4 + kImgBufs * kRowThreads * 4;
-constexpr uint32_t kBarParts = 1, kBarSeg = 2, kBarB0 = 3, kBarImg0 = 6, kBarFree0 = 9, kBarRows = 12;
+// Part slots, from the exponent region's start: above the segment table, a
+// stream of fitting parts (kPrivBytes) and its padding to 16 bytes.
+constexpr uint32_t kSlotOff = kSegTab + kPrivBytes + 16;
+constexpr uint32_t kImgBytes = kTileHdr + kTile + kSlotOff + kPrivBytes;  // >= header + planes of a raw tile
+constexpr uint32_t kImgBufs = 3;
+constexpr uint32_t kTabBufs = 4;
+constexpr uint32_t kEncSmem = kImgBufs * kImgBytes + kTabBufs * kEncTableWords * 4 + 2 * kImgBufs * kRowThreads * 4;
+constexpr uint32_t kBarParts0 = 1, kBarSeg0 = 4, kBarB0 = 7, kBarImg0 = 10, kBarFree0 = 13;
+static_assert(kBarFree0 + kImgBufs <= 16, "named barriers");
+static_assert(kImgBytes >= kTileHdr + 2 * kTile, "raw tile image");
 
 __device__ __forceinline__ void bar_arrive(uint32_t id, uint32_t n) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -393,16 +406,19 @@ __device__ __forceinline__ void load_group(const uint16_t* x, uint32_t cnt, bool
 // Shared state of the encode CTA.  Plain pointers only: an array of
 // pointers indexed by the buffer number would put the struct in local memory.
 struct EncShared {
-  uint8_t* img0;   // image b at img0 + b * kImgBytes
-  uint32_t* priv;  // [warp][word][lane]
-  uint32_t* tabs;  // kImgBufs x kEncTableWords
-  uint32_t* part;  // [row warp][lane] bits, then bit offsets
+  uint8_t* img0;       // image b at img0 + b * kImgBytes
+  uint32_t* tabs;      // kTabBufs x kEncTableWords
+  uint32_t* part;      // per buffer: [row warp][lane] bits, then bit offsets in the segment
   uint32_t* first;     // per buffer: [row warp][lane] word 0 of each part
-  uint32_t* segstart;  // [kSegs]
+  uint32_t* segstart;  // per buffer: [kSegs]
   uint32_t* mode;      // per buffer: 0 coded, 1 coded with an overflowed part, 2 raw
-  uint32_t* over;      // per buffer: a part overflowed its private buffer
+  uint32_t* over;      // per buffer: a part overflowed its slot
   uint32_t* size;      // per buffer: tile bytes
   __device__ __forceinline__ uint8_t* img(uint32_t b) const { return img0 + b * kImgBytes; }
+  // word 0 of this thread's part slot (words at a stride of 32)
+  __device__ __forceinline__ uint32_t* slot(uint32_t b, uint32_t exp_off, uint32_t warp, uint32_t lane) const {
+    return reinterpret_cast<uint32_t*>(img(b) + exp_off + kSlotOff) + warp * (32 * kPrivWords) + lane;
+  }
 };
 
 __device__ __forceinline__ EncItem load_item(const EncodeArgs& a, uint32_t t) {
@@ -419,18 +435,20 @@ __device__ __forceinline__ EncItem load_item(const EncodeArgs& a, uint32_t t) {
 
 __device__ __forceinline__ bool full_tile(const EncItem& r) { return r.nt == kTile && (r.elem0 & 7) == 0; }
 
-// Row warps, one tile: phases A and D.  v holds this tile's rows rb..rb+7
-// (full tiles); each row's registers are refilled with the next tile's row
-// as soon as they are consumed, so the loads run a whole tile ahead.
-__device__ __forceinline__ void row_tile(const EncodeArgs& a, const EncShared& S, uint32_t buf, const EncItem& rec,
-                                         uint4 (&v)[kRowsPerWarp], const EncItem& fut, bool fut_ok) {
+// Row warps, phase A of one tile in image b with code tables tb.  v holds
+// this tile's rows rb..rb+7 (full tiles); each row's registers are refilled
+// with the next tile's row as soon as they are consumed, so the loads run a
+// whole tile ahead.  Returns this lane's part length in bits.
+__device__ __forceinline__ uint32_t phase_a(const EncodeArgs& a, const EncShared& S, uint32_t b, uint32_t tb,
+                                            const EncItem& rec, uint4 (&v)[kRowsPerWarp], const EncItem& fut,
+                                            bool fut_ok) {
   const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t half = warp / kRowWarpsPerHalf;
   const uint32_t rb = (warp % kRowWarpsPerHalf) * kRowsPerWarp;
   const uint32_t col = half * kHalf + lane * kLaneElems;
-  uint8_t* img = S.img(buf);
-  const uint32_t* tab = S.tabs + buf * kEncTableWords;  // per exponent
-  const uint32_t* pair = tab + 256;                    // per symbol pair
+  uint8_t* img = S.img(b);
+  const uint32_t* tab = S.tabs + tb * kEncTableWords;  // per exponent
+  const uint32_t* pair = tab + 256;                   // per symbol pair
   const uint32_t nt = rec.nt;
   const uint16_t* x = a.in + rec.elem0;
   const bool vec = (rec.elem0 & 7) == 0;
@@ -438,19 +456,21 @@ __device__ __forceinline__ void row_tile(const EncodeArgs& a, const EncShared& S
   const uint32_t base4 = rec.base * 0x01010101u;
   const uint32_t sm_pad = (uint32_t)pad16(nt);
   const uint32_t exp_off = kTileHdr + sm_pad;
-  uint32_t* region = reinterpret_cast<uint32_t*>(img + exp_off + kSegTab);  // coded payload words
 
   // Other than full tiles: zero the padding of the sign/mantissa plane and
-  // the exponent area (the end words of each part are OR-ed in).
+  // the exponent area below the slots (the end words of each part are OR-ed
+  // in; a raw tile's phase D zeroes its own padding).
   if (!full) {
     if (tid < 16 && nt + tid < sm_pad) img[kTileHdr + nt + tid] = 0;
-    for (uint32_t o = tid * 16; o < sm_pad; o += kRowThreads * 16)
+    const uint32_t zend = min(sm_pad, kSlotOff);
+    for (uint32_t o = tid * 16; o < zend; o += kRowThreads * 16)
       *reinterpret_cast<uint4*>(img + exp_off + o) = make_uint4(0, 0, 0, 0);
   }
 
-  // Phase A: sign/mantissa bytes to the image, codewords to the private buffer.
+  // sign/mantissa bytes to the image, codewords to the part slot
   PrivSink sink;
-  sink.begin(S.priv + warp * (32 * kPrivWords) + lane);
+  uint32_t* my_slot = S.slot(b, exp_off, warp, lane);
+  sink.begin(my_slot);
   const bool fut_full = fut_ok && full_tile(fut);
   const uint16_t* xf = a.in + fut.elem0 + rb * kRow + col;
   if (full) {
@@ -490,26 +510,44 @@ __device__ __forceinline__ void row_tile(const EncodeArgs& a, const EncShared& S
   }
   sink.finish();
   const uint32_t my_bits = sink.bits();
-  S.part[warp * 32 + lane] = my_bits;
-  // word 0 of the part, for the part before it in the stream (phase D);
-  // kept per buffer because this warp's private words are reused by the
-  // next tile before every warp is past phase D
-  S.first[buf * kRowThreads + warp * 32 + lane] = S.priv[warp * (32 * kPrivWords) + lane];
-  if (__any_sync(kFull, my_bits > 32 * kPrivWords) && lane == 0) S.over[buf] = 1;
+  S.part[b * kRowThreads + warp * 32 + lane] = my_bits;
+  // word 0 of the part, for the part before it in the stream (phase D)
+  S.first[b * kRowThreads + warp * 32 + lane] = my_slot[0];
+  if (__any_sync(kFull, my_bits > 32 * kPrivWords) && lane == 0) S.over[b] = 1;
   if (!full && fut_full) {
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) v[r] = ld_stream_v4(xf + r * kRow);
   }
-  bar_arrive(kBarParts, kBarThreads);
-  bar_wait(kBarSeg, kBarThreads);
+  return my_bits;
+}
 
-  const uint32_t mode = S.mode[buf];
+// Row warps, phase D of one tile in image b (code tables tb), after the
+// layout warp's phase B: move each part from its slot to its bit position in
+// the segment stream, or take the overflow or raw path.
+__device__ __forceinline__ void phase_d(const EncodeArgs& a, const EncShared& S, uint32_t b, uint32_t tb,
+                                        const EncItem& rec, uint32_t my_bits) {
+  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t half = warp / kRowWarpsPerHalf;
+  const uint32_t rb = (warp % kRowWarpsPerHalf) * kRowsPerWarp;
+  const uint32_t col = half * kHalf + lane * kLaneElems;
+  uint8_t* img = S.img(b);
+  const uint32_t* tab = S.tabs + tb * kEncTableWords;
+  const uint32_t nt = rec.nt;
+  const uint16_t* x = a.in + rec.elem0;
+  const bool vec = (rec.elem0 & 7) == 0;
+  const bool full = nt == kTile && vec;
+  const uint32_t sm_pad = (uint32_t)pad16(nt);
+  const uint32_t exp_off = kTileHdr + sm_pad;
+  uint32_t* region = reinterpret_cast<uint32_t*>(img + exp_off + kSegTab);  // coded payload words
+  const uint32_t* part = S.part + b * kRowThreads;
+  const uint32_t* segstart = S.segstart + b * kSegs;
+  const uint32_t mode = S.mode[b];
   if (mode == 0 && full) {
-    // Phase D, full tile: every part holds >= 64 bits (64 codewords of >= 1
-    // bit), so a word of the stream holds bits of at most two parts.  Each
-    // word is written once, by the part that holds its first bit; where the
-    // part ends inside its last word, the rest of that word is the start of
-    // the next part (its private word 0).
+    // Full tile: every part holds >= 64 bits (64 codewords of >= 1 bit), so
+    // a word of the stream holds bits of at most two parts.  Each word is
+    // written once, by the part that holds its first bit; where the part
+    // ends inside its last word, the rest of that word is the start of the
+    // next part (its word 0).
     const uint32_t w8 = warp % kRowWarpsPerHalf;
     uint32_t nwarp = warp + 1, nlane = lane;  // the next part in stream order
     bool has_next = true;
@@ -522,36 +560,35 @@ __device__ __forceinline__ void row_tile(const EncodeArgs& a, const EncShared& S
         has_next = half == 0;
       }
     }
-    const uint32_t next_w0 = has_next ? S.first[buf * kRowThreads + nwarp * 32 + nlane] : 0u;
-    const uint32_t St = S.segstart[half * 32 + lane] + S.part[warp * 32 + lane];
+    const uint32_t next_w0 = has_next ? S.first[b * kRowThreads + nwarp * 32 + nlane] : 0u;
+    const uint32_t St = segstart[half * 32 + lane] + part[warp * 32 + lane];
     const uint32_t sh = St & 31, nw = (my_bits + 31) >> 5, e = (St + my_bits) & 31;
     const uint32_t x0 = (St + 31) >> 5, x1 = (St + my_bits - 1) >> 5;
-    const uint32_t* src = S.priv + warp * (32 * kPrivWords) + lane;
+    const uint32_t* src = S.slot(b, exp_off, warp, lane);
     uint32_t pw[kPrivWords + 1];
 #pragma unroll
     for (uint32_t j = 0; j < kPrivWords; ++j) pw[j] = j < nw ? src[32 * j] : 0u;
     pw[kPrivWords] = 0;
 #pragma unroll
     for (uint32_t j = 0; j < kPrivWords; ++j) {
-      const uint32_t x = x0 + j;
-      if (x <= x1) {
+      const uint32_t xw = x0 + j;
+      if (xw <= x1) {
         uint32_t w = sh ? __funnelshift_r(pw[j], pw[j + 1], 32 - sh) : pw[j];
-        if (x == x1 && e) w |= next_w0 << e;
-        region[x] = w;
+        if (xw == x1 && e) w |= next_w0 << e;
+        region[xw] = w;
       }
     }
     if (!has_next) {
       // the stream's last word: zero the padding words up to 16 bytes
       const uint32_t pend = ((kSegTab / 4 + x1 + 1 + 3) & ~3u) - kSegTab / 4;
-      for (uint32_t x = x1 + 1; x < pend; ++x) region[x] = 0;
+      for (uint32_t xw = x1 + 1; xw < pend; ++xw) region[xw] = 0;
     }
   } else if (mode == 0) {
-    // Phase D: move each part from its private buffer to its bit position
-    // in the segment stream.
+    // the part's end words are OR-ed into the zeroed area, the rest stored
     if (my_bits) {
-      const uint32_t St = S.segstart[half * 32 + lane] + S.part[warp * 32 + lane];
+      const uint32_t St = segstart[half * 32 + lane] + part[warp * 32 + lane];
       const uint32_t sh = St & 31, nw = (my_bits + 31) >> 5, nout = (sh + my_bits + 31) >> 5;
-      const uint32_t* src = S.priv + warp * (32 * kPrivWords) + lane;
+      const uint32_t* src = S.slot(b, exp_off, warp, lane);
       uint32_t* dst = region + (St >> 5);
       uint32_t pw[kPrivWords];
 #pragma unroll
@@ -569,16 +606,10 @@ __device__ __forceinline__ void row_tile(const EncodeArgs& a, const EncShared& S
       }
     }
   } else if (mode == 1) {
-    // Phase D, a part overflowed its buffer: re-read the rows and pack in
-    // place (boundary words are OR-ed, so full tiles zero the payload area
-    // first; the segment table in front of it is already written).
-    if (full) {
-      for (uint32_t o = kSegTab + tid * 16; o < sm_pad; o += kRowThreads * 16)
-        *reinterpret_cast<uint4*>(img + exp_off + o) = make_uint4(0, 0, 0, 0);
-      bar_wait(kBarRows, kRowThreads);
-    }
+    // A part overflowed its slot: re-read the rows and pack in place (the
+    // layout warp has zeroed the payload area; boundary words are OR-ed).
     BitSink bs;
-    bs.begin(region, S.segstart[half * 32 + lane] + S.part[warp * 32 + lane]);
+    bs.begin(region, segstart[half * 32 + lane] + part[warp * 32 + lane]);
 #pragma unroll 1
     for (uint32_t row = rb; row < rb + kRowsPerWarp; ++row) {
       const uint32_t i0 = row * kRow + col;
@@ -599,7 +630,9 @@ __device__ __forceinline__ void row_tile(const EncodeArgs& a, const EncShared& S
     }
     bs.finish();
   } else {
-    // Phase D, raw tile: re-read the rows and store the exponent bytes.
+    // Raw tile: re-read the rows and store the exponent bytes, then zero the
+    // padding up to 16 bytes.
+    if (tid < 16 && nt + tid < sm_pad) img[exp_off + nt + tid] = 0;
 #pragma unroll 1
     for (uint32_t row = rb; row < rb + kRowsPerWarp; ++row) {
       const uint32_t i0 = row * kRow + col;
@@ -620,43 +653,48 @@ __device__ __forceinline__ void row_tile(const EncodeArgs& a, const EncShared& S
     }
   }
   fence_proxy_async_smem();
-  bar_arrive(kBarImg0 + buf, kBarThreads);
+  bar_arrive(kBarImg0 + b, kBarThreads);
 }
 
-// Layout warp, one tile: phase B.  Also stages the next tile's code tables.
-__device__ __forceinline__ void layout_tile(const EncodeArgs& a, const EncShared& S, uint32_t buf, uint32_t item,
-                                            uint32_t next) {
+// Layout warp, phase B of tile i (image b).  Also stages the code tables of
+// tile i + 2 (`next2`) into table buffer (i + 2) mod kTabBufs: the row warps
+// are past phase D of tile i - 2 once they have all finished phase A of
+// tile i, and tile i - 1's tables may still be in use by its phase D.
+__device__ __forceinline__ void layout_tile(const EncodeArgs& a, const EncShared& S, uint32_t b, uint32_t i,
+                                            uint32_t item, uint32_t next2) {
   const uint32_t lane = threadIdx.x & 31;
   const EncItem rec = a.items[item];
-  uint8_t* img = S.img(buf);
+  uint8_t* img = S.img(b);
   const uint32_t nt = rec.nt;
   const uint32_t sm_pad = (uint32_t)pad16(nt);
   const uint32_t exp_off = kTileHdr + sm_pad;
   const uint32_t hdr = (uint32_t)chunk_hdr_bytes(a.chunks[rec.c].n_tiles);
-  // the next tile's code tables, staged in registers until the row warps are past this tile
+  // tile i + 2's code tables, staged in registers until the row warps are
+  // past tile i's phase A
   uint4 nt4[kEncTableWords / 128];
-  const bool has_next = next < a.n_items;
-  if (has_next) {
-    const uint32_t cn = __ldg(&a.items[next].c);
+  const bool has_next2 = next2 < a.n_items;
+  if (has_next2) {
+    const uint32_t cn = __ldg(&a.items[next2].c);
     const uint4* src = reinterpret_cast<const uint4*>(a.tables + (size_t)cn * kEncTableWords);
 #pragma unroll
-    for (uint32_t i = 0; i < kEncTableWords / 128; ++i) nt4[i] = __ldg(src + lane + 32 * i);
+    for (uint32_t j = 0; j < kEncTableWords / 128; ++j) nt4[j] = __ldg(src + lane + 32 * j);
   }
 
-  bar_wait(kBarParts, kBarThreads);
+  bar_wait(kBarParts0 + b, kBarThreads);
   // Bit offset of each row warp's part inside its segment, bit-granular
   // segment starts, raw/coded choice, publish the aggregate.  Lane l
   // handles segments l and 32 + l.
+  uint32_t* part = S.part + b * kRowThreads;
   uint32_t seg[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t pv[kRowWarpsPerHalf];
 #pragma unroll
-    for (int w = 0; w < kRowWarpsPerHalf; ++w) pv[w] = S.part[(h * kRowWarpsPerHalf + w) * 32 + lane];
+    for (int w = 0; w < kRowWarpsPerHalf; ++w) pv[w] = part[(h * kRowWarpsPerHalf + w) * 32 + lane];
     uint32_t off = 0;
 #pragma unroll
     for (int w = 0; w < kRowWarpsPerHalf; ++w) {
-      S.part[(h * kRowWarpsPerHalf + w) * 32 + lane] = off;
+      part[(h * kRowWarpsPerHalf + w) * 32 + lane] = off;
       off += pv[w];
     }
     seg[h] = off;
@@ -671,35 +709,42 @@ __device__ __forceinline__ void layout_tile(const EncodeArgs& a, const EncShared
     }
   }
   const uint32_t total0 = __shfl_sync(kFull, start0, 31), total1 = __shfl_sync(kFull, start1, 31);
-  S.segstart[lane] = start0 - seg[0];
-  S.segstart[32 + lane] = total0 + start1 - seg[1];
+  S.segstart[b * kSegs + lane] = start0 - seg[0];
+  S.segstart[b * kSegs + 32 + lane] = total0 + start1 - seg[1];
   const uint32_t words = (total0 + total1 + 31) >> 5;
   const bool coded = kSegTab + 4ull * words < nt;
   const uint32_t exp_bytes = coded ? kSegTab + 4 * words : nt;
+  const uint32_t over = S.over[b];
   if (coded) {
     reinterpret_cast<uint16_t*>(img + exp_off)[lane] = (uint16_t)seg[0];
     reinterpret_cast<uint16_t*>(img + exp_off)[32 + lane] = (uint16_t)seg[1];
+    if (over) {
+      // the overflow path packs in place over the whole payload area
+      for (uint32_t o = kSegTab + lane * 16; o < sm_pad; o += 32 * 16)
+        *reinterpret_cast<uint4*>(img + exp_off + o) = make_uint4(0, 0, 0, 0);
+    }
   }
   const uint32_t size = nt ? (uint32_t)(kTileHdr + sm_pad + pad16(exp_bytes)) : 0u;
   const uint64_t agg = size + (rec.k == 0 ? hdr : 0u);
+  __syncwarp();
   if (lane == 0) {
-    S.mode[buf] = coded ? (S.over[buf] ? 1u : 0u) : 2u;
-    S.over[buf] = 0;
-    S.size[buf] = size;
+    S.mode[b] = coded ? (over ? 1u : 0u) : 2u;
+    S.over[b] = 0;
+    S.size[b] = size;
     *reinterpret_cast<uint4*>(img) = make_uint4(coded ? 0u : 1u, nt, exp_bytes, 0u);
   }
-  if (has_next) {
-    uint4* dst = reinterpret_cast<uint4*>(S.tabs + ((buf + 1) % kImgBufs) * kEncTableWords);
+  if (has_next2) {
+    uint4* dst = reinterpret_cast<uint4*>(S.tabs + ((i + 2) % kTabBufs) * kEncTableWords);
 #pragma unroll
-    for (uint32_t i = 0; i < kEncTableWords / 128; ++i) dst[lane + 32 * i] = nt4[i];
+    for (uint32_t j = 0; j < kEncTableWords / 128; ++j) dst[lane + 32 * j] = nt4[j];
   }
   // Header and segment table are read by the TMA store.  The fence comes
   // before the aggregate's global store so that it does not wait for it.
   fence_proxy_async_smem();
   __syncwarp();
-  bar_arrive(kBarSeg, kBarThreads);
+  bar_arrive(kBarSeg0 + b, kBarThreads);
   if (lane == 0) st_relaxed_u64(a.item_state + item, (item == 0 ? kFlagInc : kFlagAgg) | agg);
-  bar_arrive(kBarB0 + buf, 64);
+  bar_arrive(kBarB0 + b, 64);
 }
 
 // Store warp, one tile: phases C and E.  `reuse`: the row warps will pack a
@@ -792,13 +837,12 @@ __device__ __forceinline__ void store_tile(const EncodeArgs& a, const EncShared&
 __global__ void __launch_bounds__(kEncThreads, 1) zc_encode_kernel(EncodeArgs a) {
   pdl_wait();  // records and tables come from the select kernel
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ uint32_t s_segstart[kSegs], s_mode[kImgBufs], s_over[kImgBufs], s_size[kImgBufs];
+  __shared__ uint32_t s_segstart[kImgBufs * kSegs], s_mode[kImgBufs], s_over[kImgBufs], s_size[kImgBufs];
   EncShared S;
   S.img0 = smem;
-  S.priv = reinterpret_cast<uint32_t*>(smem + kImgBufs * kImgBytes);
-  S.tabs = reinterpret_cast<uint32_t*>(smem + kImgBufs * kImgBytes + kPrivBytes);
-  S.part = S.tabs + kImgBufs * kEncTableWords;
-  S.first = S.part + kRowThreads;
+  S.tabs = reinterpret_cast<uint32_t*>(smem + kImgBufs * kImgBytes);
+  S.part = S.tabs + kTabBufs * kEncTableWords;
+  S.first = S.part + kImgBufs * kRowThreads;
   S.segstart = s_segstart;
   S.mode = s_mode;
   S.over = s_over;
@@ -809,10 +853,15 @@ __global__ void __launch_bounds__(kEncThreads, 1) zc_encode_kernel(EncodeArgs a)
   const uint32_t t0 = blockIdx.x;
   const uint32_t count = (a.n_items - t0 + G - 1) / G;  // tiles of this CTA
 
-  // Prologue: the first tile's tables.
+  // Prologue: the code tables of the first two tiles.
   {
     const uint32_t c0 = a.items[t0].c;
     for (uint32_t i = tid; i < kEncTableWords; i += kEncThreads) S.tabs[i] = __ldg(a.tables + (size_t)c0 * kEncTableWords + i);
+    if (t0 + G < a.n_items) {
+      const uint32_t c1 = a.items[t0 + G].c;
+      for (uint32_t i = tid; i < kEncTableWords; i += kEncThreads)
+        S.tabs[kEncTableWords + i] = __ldg(a.tables + (size_t)c1 * kEncTableWords + i);
+    }
     if (tid < kImgBufs) s_over[tid] = 0;
   }
   if (warp < kRowWarps) {
@@ -820,29 +869,43 @@ __global__ void __launch_bounds__(kEncThreads, 1) zc_encode_kernel(EncodeArgs a)
     const uint32_t rb = (warp % kRowWarpsPerHalf) * kRowsPerWarp;
     const uint32_t col = half * kHalf + lane * kLaneElems;
     uint4 v[kRowsPerWarp];
-    EncItem rec = load_item(a, t0), nx = load_item(a, t0 + G);
+    EncItem rec = load_item(a, t0), nx = load_item(a, t0 + G), prv = rec;
     if (full_tile(rec)) {
 #pragma unroll
       for (int r = 0; r < kRowsPerWarp; ++r) v[r] = ld_stream_v4(a.in + rec.elem0 + (rb + r) * kRow + col);
     }
     __syncthreads();
-    uint32_t buf = 0;
+    uint32_t b = 0, tb = 0, pb = 0, ptb = 0, prv_bits = 0;
     for (uint32_t i = 0; i < count; ++i) {
       const uint32_t t = t0 + i * G;
       const EncItem nx2 = load_item(a, t + 2 * G);  // records run two tiles ahead
-      if (i >= kImgBufs) bar_wait(kBarFree0 + buf, kBarThreads);
-      row_tile(a, S, buf, rec, v, nx, t + G < a.n_items);
+      if (i >= kImgBufs) bar_wait(kBarFree0 + b, kBarThreads);
+      const uint32_t bits = phase_a(a, S, b, tb, rec, v, nx, t + G < a.n_items);
+      bar_arrive(kBarParts0 + b, kBarThreads);
+      if (i > 0) {  // the previous tile, now that this one is packed
+        bar_wait(kBarSeg0 + pb, kBarThreads);
+        phase_d(a, S, pb, ptb, prv, prv_bits);
+      }
+      prv = rec;
+      prv_bits = bits;
+      pb = b;
+      ptb = tb;
       rec = nx;
       nx = nx2;
-      buf = buf + 1 == kImgBufs ? 0 : buf + 1;
+      b = b + 1 == kImgBufs ? 0 : b + 1;
+      tb = tb + 1 == kTabBufs ? 0 : tb + 1;
+    }
+    if (count > 0) {
+      bar_wait(kBarSeg0 + pb, kBarThreads);
+      phase_d(a, S, pb, ptb, prv, prv_bits);
     }
   } else if (warp == kLayoutWarp) {
     __syncthreads();
-    uint32_t buf = 0;
+    uint32_t b = 0;
     for (uint32_t i = 0; i < count; ++i) {
       const uint32_t t = t0 + i * G;
-      layout_tile(a, S, buf, t, t + G);
-      buf = buf + 1 == kImgBufs ? 0 : buf + 1;
+      layout_tile(a, S, b, i, t, t + 2 * G);
+      b = b + 1 == kImgBufs ? 0 : b + 1;
     }
   } else {
     __syncthreads();
