@@ -97,6 +97,16 @@ def test_empty_and_tiny_chunks():
     gpu_roundtrip(x, sizes)
 
 
+@pytest.mark.parametrize("n_chunks", [63, 64, 65])
+def test_chunk_counts_around_the_early_tile_search(n_chunks):
+    # up to 64 chunks a decode CTA finds its chunk itself before the prep
+    # kernel finishes; more chunks use the prep kernel's tile prefix
+    sizes = [int(v) for v in np.random.default_rng(n_chunks).integers(1, 70000, size=n_chunks)]
+    sizes[n_chunks // 2] = 0  # an empty chunk inside the prefix
+    x = workloads.gaussian_bf16(sum(sizes), 0.05, 13, n_chunks)
+    gpu_roundtrip(x, sizes)
+
+
 def test_many_chunks_more_than_one_select_batch():
     sizes = [int(v) for v in np.random.default_rng(5).integers(0, 3000, size=600)]
     x = workloads.gaussian_bf16(sum(sizes), 0.01, 9)
@@ -142,6 +152,20 @@ def test_reduce_parity(k, n):
     if n > 100:
         xs[0][:5] = np.array([0x7F80, 0xFF80, 0x7FC1, 0x0001, 0x8001], np.uint16)
     chunks = oracle_chunks(xs)
+    ref = oracle.decompress_reduce(chunks, n)
+    y = zc.decompress_reduce(dev_chunks(chunks), n)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), ref)
+
+
+def test_reduce_peers_with_one_table():
+    # peers with the same values share peer 0's code lengths: the decode
+    # table sits in shared memory
+    n = 3 * 32768 + 1234
+    base = workloads.gaussian_bf16(n, 0.01, 91)
+    xs = [base, base[::-1].copy(), base, np.roll(base, 7)]
+    chunks = oracle_chunks(xs)
+    assert len({bytes(c[24:32]) for c in chunks}) == 1
     ref = oracle.decompress_reduce(chunks, n)
     y = zc.decompress_reduce(dev_chunks(chunks), n)
     torch.cuda.synchronize()
