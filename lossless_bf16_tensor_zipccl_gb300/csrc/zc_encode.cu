@@ -157,8 +157,9 @@ __global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ 
 // 0) -- phase A.  The layout warp (warp 16) then places the segments and
 // publishes the tile's size -- phase B; each lane copies its part to its bit
 // position in the lower half with funnel shifts -- phase D.  A row warp runs
-// phase D of a tile after phase A of the next one, so it does not wait for
-// the slowest row warp and the layout warp in between.  Parts fit their
+// phase D of a tile after phase A of the next one: rather than wait at every
+// tile boundary for the slowest row warp and the layout warp, it waits only
+// when it gets a whole tile ahead of them.  Parts fit their
 // slots at up to 4 bits per value, so a coded stream of fitting parts is at
 // most 16 KB and never reaches the slots; a part longer than its slot (a lane
 // with many escapes) sends the tile down a slower path that re-reads its
@@ -314,7 +315,7 @@ struct BitSink {
   }
 };
 
-// Bit packer into a lane's private buffer (word j at p[32 j]).  Counts every
+// Bit packer into a lane's part slot (word j at p[32 j]).  Counts every
 // bit; words past kPrivWords are dropped and the caller sees the overflow in
 // bits().  code < 2^len, len <= 32.
 struct PrivSink {
