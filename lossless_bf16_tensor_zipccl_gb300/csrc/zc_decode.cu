@@ -510,103 +510,114 @@ __device__ __forceinline__ uint32_t f32_to_bf16_rne(float f) {
   return u >> 16;
 }
 
-__device__ __forceinline__ void add_bf16x2(float& a0, float& a1, uint32_t w) {
-  a0 = __fadd_rn(a0, __uint_as_float(w << 16));
-  a1 = __fadd_rn(a1, __uint_as_float(w & 0xFFFF0000u));
-}
-
 // One block per half tile, one warp per peer.  Each warp stages the payload
-// bits of its peer's half tile in shared memory with one TMA bulk copy,
-// decodes kRedRows half rows at a time into shared memory (peer-major) with
-// the sign/mantissa bytes read straight from global memory, then every
-// thread folds pairs of values across the peers in rank order.  Peers with
-// the same code lengths share one decode table; when all share peer 0's, it
-// sits in shared memory, else the tables are read through L1.  A block of 8
-// peers needs 56 KB of shared memory and 4 blocks fit per SM: a 64M-element
-// reduce (512 half tiles) runs in one wave.
-constexpr uint32_t kRedRows = 2;
-constexpr uint32_t kRedStageBytes = kRedRows * kHalf * 2;  // decoded BF16 half rows per peer
-constexpr uint32_t kRedSlot = 5584;  // staged half payload per peer (~2.72 bits/value; a multiple of 16 for TMA)
+// bits of its peer's half tile in shared memory with one TMA bulk copy and
+// decodes its half rows with the sign/mantissa bytes read straight from
+// global memory.  The fold runs along the warps in rank order: warp 0 writes
+// its row into an fp32 row accumulator, warp p adds its row once warp p - 1
+// has added its own, and the last warp rounds to BF16 and stores.  Each
+// hand-off is an mbarrier phase; the accumulator is double-buffered, so warp
+// 0 starts row r + 2 once the last warp has finished row r.  Peers with the
+// same code lengths share one decode table; when the block's peers use at
+// most two tables they sit in shared memory, else the tables are read
+// through L1.  A block of 8 peers needs 55 KB of shared memory and 4 blocks
+// fit per SM: a 64M-element reduce (512 half tiles) runs in one wave.
+constexpr uint32_t kRedSlot = 5696;  // staged half payload per peer (~2.78 bits/value; a multiple of 16 for TMA)
+constexpr uint32_t kRedAcc = 2 * kHalf * 4;  // two fp32 half rows
 
 __host__ __device__ constexpr size_t reduce_smem_bytes(uint32_t k) {
-  return kLutEntries * 4 + (size_t)k * (kRedStageBytes + kRedSlot + 16) + kStagePad;
+  return 2 * kLutEntries * 4 + kRedAcc + (size_t)k * (kRedSlot + 32) + kStagePad;
 }
 
-// The rows of one half tile: each warp decodes kRedRows rows of its peer
-// into shared memory, then the block folds them.  sq: the first kSmAhead rows
-// of this lane's sign/mantissa bytes, already in flight.
+// The rows of one half tile for warp p: decode, then take part in the fold.
+// done: 2 x K mbarriers (buffer j, warp q at done[2 q + j]), 32 arrivals
+// each.  sq: the first kSmAhead rows of this lane's sign/mantissa bytes,
+// already in flight.  Returns false if a hand-off wait gave up.
 template <uint32_t K, bool kStaged>
-__device__ __forceinline__ void reduce_rows(RowSource<kStaged>& src, const uint8_t* smp, uint16_t* sbuf,
-                                            uint16_t* y, uint32_t half, uint2 (&sq)[kSmAhead]) {
-  const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5, tid = threadIdx.x;
-  constexpr uint32_t nthreads = 32 * K;
-  const uint32_t nt = src.nt;
-  uint16_t* mine = sbuf + (size_t)p * kRedRows * kHalf;
+__device__ __forceinline__ bool reduce_rows(RowSource<kStaged>& src, const uint8_t* smp, float* acc, uint64_t* done,
+                                            uint16_t* y, uint2 (&sq)[kSmAhead]) {
+  const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5;
+  const uint32_t nt = src.nt, col = src.col;
   const uint32_t rows = (nt + kRow - 1) / kRow;
   const bool fast = nt == kTile && src.tv.mode == 0;  // same for every lane of the warp
-  for (uint32_t r0 = 0; r0 < rows; r0 += kRedRows) {
-    if (fast) {
-      // full coded tile: 8 values per lane in every row
+  bool live = true;  // hand-off waits still bounded by their own limit
+  // fold this lane's 8 values of row r (4 words of 2 BF16) into the row
+  auto fold = [&](uint32_t r, uint4 v) {
+    const uint32_t j = r & 1;
+    // wait for the previous warp's row r, or (warp 0) for the last warp to
+    // have finished row r - 2 in this buffer
+    if (live) {
+      if (p > 0) live = mbar_wait(done + 2 * (p - 1) + j, (r >> 1) & 1);
+      else if (K > 1 && r >= 2) live = mbar_wait(done + 2 * (K - 1) + j, ((r >> 1) - 1) & 1);
+    }
+    float* a = acc + j * kHalf + lane * kLaneElems;
+    float f[8];
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (uint32_t j = 0; j < kRedRows; ++j) {
-        uint32_t elo, ehi;
-        src.dec.fill_warp(8);
-        src.dec.take8(elo, ehi);
-        const uint2 u = merge4(elo, sq[j].x), v = merge4(ehi, sq[j].y);
-        *reinterpret_cast<uint4*>(mine + j * kHalf + lane * kLaneElems) = make_uint4(u.x, u.y, v.x, v.y);
-      }
+    for (int q = 0; q < 4; ++q) {
+      f[2 * q] = __uint_as_float(w4[q] << 16);
+      f[2 * q + 1] = __uint_as_float(w4[q] & 0xFFFF0000u);
+    }
+    if (p > 0) {
+      const float4 a0 = *reinterpret_cast<const float4*>(a), a1 = *reinterpret_cast<const float4*>(a + 4);
+      const float prev[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) f[q] = __fadd_rn(prev[q], f[q]);
+    }
+    if (p + 1 < K) {
+      *reinterpret_cast<float4*>(a) = make_float4(f[0], f[1], f[2], f[3]);
+      *reinterpret_cast<float4*>(a + 4) = make_float4(f[4], f[5], f[6], f[7]);
     } else {
+      const uint32_t cnt = src.count(r);
+      uint32_t o[4];
 #pragma unroll
-      for (uint32_t j = 0; j < kRedRows; ++j) {
-        const uint32_t r = r0 + j;
-        if (r < rows) {
-          const uint2 sm = sq[j];  // kSmAhead is a multiple of kRedRows: the ring slot of row r
-          *reinterpret_cast<uint4*>(mine + j * kHalf + lane * kLaneElems) = src.row(r, sm);
-        }
-      }
+      for (int q = 0; q < 4; ++q) o[q] = f32_to_bf16_rne(f[2 * q]) | (f32_to_bf16_rne(f[2 * q + 1]) << 16);
+      if (cnt) store_row(y + r * kRow + col, cnt, (reinterpret_cast<uintptr_t>(y) & 15) == 0, make_uint4(o[0], o[1], o[2], o[3]));
     }
-    // advance the ring by kRedRows rows
+    mbar_arrive(done + 2 * p + j);
+  };
+  if (fast) {
+    // full coded tile: 8 values per lane in every row
+#pragma unroll kSmAhead
+    for (uint32_t r = 0; r < kRows; ++r) {
+      uint32_t elo, ehi;
+      src.dec.fill_warp(8);
+      src.dec.take8(elo, ehi);
+      const uint2 sm = sq[r % kSmAhead];
+      if (r + kSmAhead < kRows) sq[r % kSmAhead] = ld_stream_v2(smp + (r + kSmAhead) * kRow);
+      const uint2 u = merge4(elo, sm.x), w = merge4(ehi, sm.y);
+      fold(r, make_uint4(u.x, u.y, w.x, w.y));
+    }
+  } else {
+    for (uint32_t r = 0; r < rows; ++r) {
+      const uint4 v = src.row(r, sq[0]);
 #pragma unroll
-    for (uint32_t j = 0; j < kSmAhead; ++j) {
-      if (j + kRedRows < kSmAhead) {
-        sq[j] = sq[j + kRedRows];
-      } else {
-        const uint32_t r = r0 + kRedRows + j;
-        sq[j] = r < rows ? load_bytes8(smp + r * kRow, src.count(r)) : make_uint2(0, 0);
-      }
+      for (uint32_t q = 0; q + 1 < kSmAhead; ++q) sq[q] = sq[q + 1];
+      const uint32_t rn = r + kSmAhead;
+      sq[kSmAhead - 1] = rn < rows ? load_bytes8(smp + rn * kRow, src.count(rn)) : make_uint2(0, 0);
+      fold(r, v);
     }
-    __syncthreads();
-    // fold: every thread takes pairs of values, so the whole block works
-    for (uint32_t e = tid * 2; e < kRedRows * kHalf; e += nthreads * 2) {
-      const uint32_t gi = (r0 + e / kHalf) * kRow + half * kHalf + (e % kHalf);
-      if (gi >= nt) continue;
-      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(sbuf + e);
-      float a0 = __uint_as_float(w0 << 16), a1 = __uint_as_float(w0 & 0xFFFF0000u);
-#pragma unroll
-      for (uint32_t pp = 1; pp < K; ++pp)
-        add_bf16x2(a0, a1, *reinterpret_cast<const uint32_t*>(sbuf + (size_t)pp * kRedRows * kHalf + e));
-      const uint32_t o = f32_to_bf16_rne(a0) | (f32_to_bf16_rne(a1) << 16);
-      if (gi + 1 < nt) *reinterpret_cast<uint32_t*>(y + gi) = o;
-      else y[gi] = (uint16_t)o;
-    }
-    __syncthreads();
   }
+  return live;
 }
 
-// Instantiated per peer count K (1..16), so the fold over the peers unrolls.
+// Instantiated per peer count K (1..16), so the fold unrolls.
 template <uint32_t K>
 __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
   extern __shared__ __align__(128) uint8_t rsm[];
   const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5, tid = threadIdx.x;
   const uint32_t t = blockIdx.x >> 1, half = blockIdx.x & 1;
-  // peer 0's decode table | k x kRedRows half rows | k x kRedSlot staged
-  // payloads | kStagePad | k x 2 barrier words
+  // two decode tables | two fp32 half rows | k x kRedSlot staged payloads |
+  // kStagePad | k x (2 copy + 2 hand-off) barrier words
   uint32_t* s_lut = reinterpret_cast<uint32_t*>(rsm);
-  uint16_t* sbuf = reinterpret_cast<uint16_t*>(rsm + kLutEntries * 4);
-  uint8_t* slots = reinterpret_cast<uint8_t*>(sbuf) + (size_t)K * kRedStageBytes;
+  float* acc = reinterpret_cast<float*>(rsm + 2 * kLutEntries * 4);
+  uint8_t* slots = rsm + 2 * kLutEntries * 4 + kRedAcc;
   uint64_t* bars = reinterpret_cast<uint64_t*>(slots + (size_t)K * kRedSlot + kStagePad);
+  uint64_t* done = bars + 2 * K;
   __shared__ int s_bad;
+  __shared__ uint32_t s_own[kMaxPeers];
   if (tid == 0) s_bad = 0;
+  if (tid < 2 * K) mbar_init(done + tid, 32);
   __syncthreads();
   // While the prep kernel runs: locate this half tile in the peer's chunk,
   // start the copy of its payload and the first sign/mantissa loads.  These
@@ -645,35 +656,48 @@ __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
   const bool ok = located && d.ok && d.n_tiles == n_tiles;
   // one read of the status word per block, so every thread takes the same path
   if (tid == 0 && *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0) s_bad = 1;
-  if (lane == 0 && (!ok || timeout)) {
-    s_bad = 1;
-    set_status(a.hdr, ok ? kStTimeout : kStCorrupt);
+  if (lane == 0) {
+    s_own[p] = d.item_start;  // the peer owning this peer's table
+    if (!ok || timeout) {
+      s_bad = 1;
+      set_status(a.hdr, ok ? kStTimeout : kStCorrupt);
+    }
   }
-  if (p == 0 && d.ok) load_lut(s_lut, a.luts, lane, 32);  // peer 0 always owns its table
   // Decoders for the whole block: staged when every coded peer is staged (a
-  // raw peer has none), with peer 0's table in shared memory when every peer
-  // uses it (item_start: the peer owning a peer's table).
+  // raw peer has none)
   const bool staged = __syncthreads_and(sbytes != 0 || tv.mode != 0) != 0;
-  const bool one_table = __syncthreads_and(d.item_start == 0) != 0;
   if (s_bad) return;  // uniform; a copy that did arrive has nothing left in flight
-  const uint32_t* lut = a.luts + (size_t)d.item_start * kLutEntries;
+  // At most two tables (peer 0's and the first other one) go to shared memory.
+  uint32_t o1 = 0;
+  bool two = true;
+#pragma unroll
+  for (uint32_t q = 0; q < K; ++q) {
+    const uint32_t o = s_own[q];
+    if (o != 0 && o1 == 0) o1 = o;
+    two = two && (o == 0 || o == o1);
+  }
+  if (p == 0) load_lut(s_lut, a.luts, lane, 32);  // peer 0 always owns its table
+  if (p == (K > 1 ? 1u : 0u) && o1) load_lut(s_lut + kLutEntries, a.luts + (size_t)o1 * kLutEntries, lane, 32);
+  __syncthreads();
   uint16_t* y = a.out + (uint64_t)t * kTile;
   const ExpSource sx{reinterpret_cast<const uint32_t*>(slot), 8 * slo, nullptr};
-  if (staged && one_table) {
+  bool live;
+  if (staged && two) {
     RowSource<true> src;
-    src.start(tv, nt, col, s_lut, d.base, sx);
-    reduce_rows<K>(src, smp, sbuf, y, half, sq);
+    src.start(tv, nt, col, d.item_start == 0 ? s_lut : s_lut + kLutEntries, d.base, sx);
+    live = reduce_rows<K>(src, smp, acc, done, y, sq);
   } else if (staged) {
     RowSource<true> src;
-    src.start(tv, nt, col, lut, d.base, sx);
-    reduce_rows<K>(src, smp, sbuf, y, half, sq);
+    src.start(tv, nt, col, a.luts + (size_t)d.item_start * kLutEntries, d.base, sx);
+    live = reduce_rows<K>(src, smp, acc, done, y, sq);
   } else {
     RowSource<false> src;
     const ExpSource xs{reinterpret_cast<const uint32_t*>(payload), 0u,
                        reinterpret_cast<const uint32_t*>(tv.tile + tv.exp_off + pad16(tv.exp_bytes))};
-    src.start(tv, nt, col, lut, d.base, xs);
-    reduce_rows<K>(src, smp, sbuf, y, half, sq);
+    src.start(tv, nt, col, a.luts + (size_t)d.item_start * kLutEntries, d.base, xs);
+    live = reduce_rows<K>(src, smp, acc, done, y, sq);
   }
+  if (!live && lane == 0) set_status(a.hdr, kStTimeout);
 }
 
 // ---------------------------------------------------------------- launchers
