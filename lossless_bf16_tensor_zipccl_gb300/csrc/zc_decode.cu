@@ -516,22 +516,24 @@ __device__ __forceinline__ uint32_t f32_to_bf16_rne(float f) {
 // global memory.  The fold runs along the warps in rank order: warp 0 writes
 // its row into an fp32 row accumulator, warp p adds its row once warp p - 1
 // has added its own, and the last warp rounds to BF16 and stores.  Each
-// hand-off is an mbarrier phase; the accumulator is double-buffered, so warp
-// 0 starts row r + 2 once the last warp has finished row r.  Peers with the
+// hand-off is an mbarrier phase; the accumulators form a ring of kRedBufs
+// rows, so warp 0 starts row r + kRedBufs once the last warp has finished
+// row r.  Peers with the
 // same code lengths share one decode table; when the block's peers use at
 // most two tables they sit in shared memory, else the tables are read
 // through L1.  A block of 8 peers needs 55 KB of shared memory and 4 blocks
 // fit per SM: a 64M-element reduce (512 half tiles) runs in one wave.
 constexpr uint32_t kRedSlot = 5696;  // staged half payload per peer (~2.78 bits/value; a multiple of 16 for TMA)
-constexpr uint32_t kRedAcc = 2 * kHalf * 4;  // two fp32 half rows
+constexpr uint32_t kRedBufs = 2;     // fp32 half-row accumulators in the ring
+constexpr uint32_t kRedAcc = kRedBufs * kHalf * 4;
 
 __host__ __device__ constexpr size_t reduce_smem_bytes(uint32_t k) {
-  return 2 * kLutEntries * 4 + kRedAcc + (size_t)k * (kRedSlot + 32) + kStagePad;
+  return 2 * kLutEntries * 4 + kRedAcc + (size_t)k * (kRedSlot + 16 + 8 * kRedBufs) + kStagePad;
 }
 
 // The rows of one half tile for warp p: decode, then take part in the fold.
-// done: 2 x K mbarriers (buffer j, warp q at done[2 q + j]), 32 arrivals
-// each.  sq: the first kSmAhead rows of this lane's sign/mantissa bytes,
+// done: kRedBufs x K mbarriers (buffer j, warp q at done[kRedBufs q + j]),
+// 32 arrivals each.  sq: the first kSmAhead rows of this lane's sign/mantissa bytes,
 // already in flight.  Returns false if a hand-off wait gave up.
 template <uint32_t K, bool kStaged>
 __device__ __forceinline__ bool reduce_rows(RowSource<kStaged>& src, const uint8_t* smp, float* acc, uint64_t* done,
@@ -543,12 +545,12 @@ __device__ __forceinline__ bool reduce_rows(RowSource<kStaged>& src, const uint8
   bool live = true;  // hand-off waits still bounded by their own limit
   // fold this lane's 8 values of row r (4 words of 2 BF16) into the row
   auto fold = [&](uint32_t r, uint4 v) {
-    const uint32_t j = r & 1;
+    const uint32_t j = r % kRedBufs, use = r / kRedBufs;  // buffer, and its use count before row r
     // wait for the previous warp's row r, or (warp 0) for the last warp to
-    // have finished row r - 2 in this buffer
+    // have finished the previous row in this buffer
     if (live) {
-      if (p > 0) live = mbar_wait(done + 2 * (p - 1) + j, (r >> 1) & 1);
-      else if (K > 1 && r >= 2) live = mbar_wait(done + 2 * (K - 1) + j, ((r >> 1) - 1) & 1);
+      if (p > 0) live = mbar_wait(done + kRedBufs * (p - 1) + j, use & 1);
+      else if (K > 1 && use > 0) live = mbar_wait(done + kRedBufs * (K - 1) + j, (use - 1) & 1);
     }
     float* a = acc + j * kHalf + lane * kLaneElems;
     float f[8];
@@ -574,7 +576,7 @@ __device__ __forceinline__ bool reduce_rows(RowSource<kStaged>& src, const uint8
       for (int q = 0; q < 4; ++q) o[q] = f32_to_bf16_rne(f[2 * q]) | (f32_to_bf16_rne(f[2 * q + 1]) << 16);
       if (cnt) store_row(y + r * kRow + col, cnt, (reinterpret_cast<uintptr_t>(y) & 15) == 0, make_uint4(o[0], o[1], o[2], o[3]));
     }
-    mbar_arrive(done + 2 * p + j);
+    mbar_arrive(done + kRedBufs * p + j);
   };
   if (fast) {
     // full coded tile: 8 values per lane in every row
@@ -607,8 +609,8 @@ __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
   extern __shared__ __align__(128) uint8_t rsm[];
   const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5, tid = threadIdx.x;
   const uint32_t t = blockIdx.x >> 1, half = blockIdx.x & 1;
-  // two decode tables | two fp32 half rows | k x kRedSlot staged payloads |
-  // kStagePad | k x (2 copy + 2 hand-off) barrier words
+  // two decode tables | kRedBufs fp32 half rows | k x kRedSlot staged
+  // payloads | kStagePad | k x (2 copy + kRedBufs hand-off) barrier words
   uint32_t* s_lut = reinterpret_cast<uint32_t*>(rsm);
   float* acc = reinterpret_cast<float*>(rsm + 2 * kLutEntries * 4);
   uint8_t* slots = rsm + 2 * kLutEntries * 4 + kRedAcc;
@@ -617,7 +619,7 @@ __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
   __shared__ int s_bad;
   __shared__ uint32_t s_own[kMaxPeers];
   if (tid == 0) s_bad = 0;
-  if (tid < 2 * K) mbar_init(done + tid, 32);
+  if (tid < kRedBufs * K) mbar_init(done + tid, 32);
   __syncthreads();
   // While the prep kernel runs: locate this half tile in the peer's chunk,
   // start the copy of its payload and the first sign/mantissa loads.  These
