@@ -165,6 +165,35 @@ zipccl_status zipccl_decompress_reduce_noalloc(const void *const *d_peer_chunks,
 zipccl_status zipccl_get_device_status(const void *d_ws, void *stream);
 
 /*
+ * Cost model of the switch between compressed and plain exchange ("ZipCCL:
+ * Efficient Lossless Data Compression of Communication Collectives for
+ * Accelerating LLM Training", abstract, technique (3): collectives switch
+ * between compressed and uncompressed operation from workload and system
+ * characteristics).  Host only; nothing is launched.
+ *
+ * zipccl_predict_chunk_bytes: the size in bytes of the stream of one chunk
+ * of n values drawn from N(0, sigma^2) and compressed with a sigma hint of
+ * `sigma`: the format's header, tile table and tile headers, the raw
+ * sign/mantissa plane, and per tile an exponent region of
+ * ceil(n_t * E / 32) words plus the segment table, E being the expected code
+ * bits of one exponent under that code (closed-form masses); raw exponent
+ * bytes where those are not larger.  out_bits_per_value (nullable): 8 x
+ * bytes / n.  sigma <= 0, not finite, or n above the per-chunk limit give
+ * ZIPCCL_ERR_INVALID_ARG.
+ *
+ * zipccl_choose_compressed: with link, compress and decompress throughputs
+ * in GB/s of their input, sending n values raw takes 2n / link; compressed,
+ * 2n / compress + bytes / link + 2n / decompress (stages in sequence, bytes
+ * as predicted above).  *use_compressed = 1 when raw time / compressed time
+ * > 1 + margin; predicted_speedup (nullable) receives that ratio.
+ * Non-positive throughputs or a negative margin give ZIPCCL_ERR_INVALID_ARG.
+ */
+zipccl_status zipccl_predict_chunk_bytes(uint64_t n, float sigma, uint64_t *out_bytes, double *out_bits_per_value);
+zipccl_status zipccl_choose_compressed(uint64_t n, float sigma, double link_gbs, double compress_gbs,
+                                       double decompress_gbs, double margin, int *use_compressed,
+                                       double *predicted_speedup);
+
+/*
  * The code this library builds for scale phase r = q mod 16 (0..15): the
  * window start relative to floor(q/16) + 127 and the 16 code lengths
  * (symbols 0..14 = window exponents, 15 = escape).  Host only.

@@ -27,8 +27,9 @@ __all__ = [
     "ZipcclError", "load", "library_path", "zipccl_format_version", "zipccl_status_string",
     "zipccl_max_compressed_bytes", "zipccl_compress_workspace_bytes", "zipccl_decompress_workspace_bytes",
     "zipccl_reduce_workspace_bytes", "zipccl_compress", "zipccl_decompress", "zipccl_decompress_reduce",
-    "zipccl_get_device_status", "zipccl_codebook_phase", "zipccl_decompress_reduce_noalloc", "compress",
-    "decompress", "decompress_reduce", "Compressed", "EXPORTED_SYMBOLS",
+    "zipccl_get_device_status", "zipccl_codebook_phase", "zipccl_decompress_reduce_noalloc",
+    "zipccl_predict_chunk_bytes", "zipccl_choose_compressed", "compress", "decompress", "decompress_reduce",
+    "Compressed", "EXPORTED_SYMBOLS",
 ]
 
 OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_CORRUPT, ERR_VERSION, ERR_TIMEOUT, ERR_CUDA = range(7)
@@ -36,7 +37,8 @@ EXPORTED_SYMBOLS = [
     "zipccl_format_version", "zipccl_status_string", "zipccl_max_compressed_bytes",
     "zipccl_compress_workspace_bytes", "zipccl_decompress_workspace_bytes", "zipccl_reduce_workspace_bytes",
     "zipccl_compress", "zipccl_decompress", "zipccl_decompress_reduce", "zipccl_get_device_status",
-    "zipccl_codebook_phase", "zipccl_decompress_reduce_noalloc",
+    "zipccl_codebook_phase", "zipccl_decompress_reduce_noalloc", "zipccl_predict_chunk_bytes",
+    "zipccl_choose_compressed",
 ]
 
 _lock = threading.Lock()
@@ -99,6 +101,12 @@ def load(build_if_missing: bool = True):
                                                        ctypes.POINTER(vp), vp]
         L.zipccl_codebook_phase.restype = ctypes.c_int
         L.zipccl_codebook_phase.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_uint8)]
+        dbl = ctypes.c_double
+        L.zipccl_predict_chunk_bytes.restype = ctypes.c_int
+        L.zipccl_predict_chunk_bytes.argtypes = [u64, ctypes.c_float, u64p, ctypes.POINTER(dbl)]
+        L.zipccl_choose_compressed.restype = ctypes.c_int
+        L.zipccl_choose_compressed.argtypes = [u64, ctypes.c_float, dbl, dbl, dbl, dbl, ctypes.POINTER(ctypes.c_int),
+                                               ctypes.POINTER(dbl)]
         _lib = L
         return L
 
@@ -189,6 +197,27 @@ def zipccl_codebook_phase(phase: int) -> tuple[int, list[int]]:
     lens = (ctypes.c_uint8 * 16)()
     _check(load().zipccl_codebook_phase(int(phase), ctypes.byref(off), lens), "zipccl_codebook_phase")
     return off.value, list(lens)
+
+
+def zipccl_predict_chunk_bytes(n: int, sigma: float) -> tuple[int, float]:
+    """Predicted stream bytes of one chunk of n values from N(0, sigma^2), and bits per value."""
+    out = ctypes.c_uint64()
+    bits = ctypes.c_double()
+    _check(load().zipccl_predict_chunk_bytes(ctypes.c_uint64(int(n)), ctypes.c_float(sigma), ctypes.byref(out),
+                                             ctypes.byref(bits)), "zipccl_predict_chunk_bytes")
+    return int(out.value), float(bits.value)
+
+
+def zipccl_choose_compressed(n: int, sigma: float, link_gbs: float, compress_gbs: float, decompress_gbs: float,
+                             margin: float = 0.1) -> tuple[bool, float]:
+    """(compress?, predicted speedup of the compressed exchange) under the sequential cost model."""
+    use = ctypes.c_int()
+    sp = ctypes.c_double()
+    _check(load().zipccl_choose_compressed(ctypes.c_uint64(int(n)), ctypes.c_float(sigma), ctypes.c_double(link_gbs),
+                                           ctypes.c_double(compress_gbs), ctypes.c_double(decompress_gbs),
+                                           ctypes.c_double(margin), ctypes.byref(use), ctypes.byref(sp)),
+           "zipccl_choose_compressed")
+    return bool(use.value), float(sp.value)
 
 
 # ------------------------------------------------------------------ torch level

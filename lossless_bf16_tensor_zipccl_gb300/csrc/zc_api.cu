@@ -274,6 +274,44 @@ zipccl_status zipccl_get_device_status(const void* d_ws, void* stream) {
   return static_cast<zipccl_status>(st);
 }
 
+zipccl_status zipccl_predict_chunk_bytes(uint64_t n, float sigma, uint64_t* out_bytes, double* out_bits_per_value) {
+  if (!out_bytes || !(sigma > 0.0f) || !(sigma < INFINITY) || n > kMaxChunkElems) return ZIPCCL_ERR_INVALID_ARG;
+  // the scale a hint of sigma selects (as in zipccl_compress)
+  double v = floor(16.0 * log2((double)sigma) + 0.5);
+  v = v < -32768.0 ? -32768.0 : (v > 32767.0 ? 32767.0 : v);
+  const double bits = expected_exponent_bits((double)sigma, (int)v);
+  // format sizes: header and tile table, then per tile its header, the
+  // sign/mantissa plane and the exponent region, coded only when smaller
+  auto tile_bytes = [&](uint64_t nt) -> uint64_t {
+    const uint64_t words = (uint64_t)ceil((double)nt * bits / 32.0);
+    const uint64_t coded = kSegTab + 4 * words;
+    return kTileHdr + pad16(nt) + pad16(coded < nt ? coded : nt);
+  };
+  const uint64_t T = tiles_of(n);
+  uint64_t total = chunk_hdr_bytes(T);
+  if (T) total += (T - 1) * tile_bytes(kTile) + tile_bytes(n - (T - 1) * kTile);
+  *out_bytes = total;
+  if (out_bits_per_value) *out_bits_per_value = n ? 8.0 * (double)total / (double)n : 0.0;
+  return ZIPCCL_OK;
+}
+
+zipccl_status zipccl_choose_compressed(uint64_t n, float sigma, double link_gbs, double compress_gbs,
+                                       double decompress_gbs, double margin, int* use_compressed,
+                                       double* predicted_speedup) {
+  if (!use_compressed || !(link_gbs > 0.0) || !(compress_gbs > 0.0) || !(decompress_gbs > 0.0) || !(margin >= 0.0))
+    return ZIPCCL_ERR_INVALID_ARG;
+  uint64_t bytes = 0;
+  const zipccl_status st = zipccl_predict_chunk_bytes(n, sigma, &bytes, nullptr);
+  if (st != ZIPCCL_OK) return st;
+  const double raw = 2.0 * (double)n;
+  const double t_raw = raw / link_gbs;
+  const double t_zip = raw / compress_gbs + (double)bytes / link_gbs + raw / decompress_gbs;
+  const double speedup = t_zip > 0.0 ? t_raw / t_zip : 0.0;
+  *use_compressed = speedup > 1.0 + margin ? 1 : 0;
+  if (predicted_speedup) *predicted_speedup = speedup;
+  return ZIPCCL_OK;
+}
+
 zipccl_status zipccl_codebook_phase(int phase, int* base_offset, uint8_t* lens16) {
   if (phase < 0 || phase > 15 || !base_offset || !lens16) return ZIPCCL_ERR_INVALID_ARG;
   const PhaseTable& t = phase_tables()[phase];

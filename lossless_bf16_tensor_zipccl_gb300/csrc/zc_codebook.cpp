@@ -114,4 +114,24 @@ const PhaseTable* phase_tables() {
   return g_tables;
 }
 
+int base_for_q(int q) {
+  const int k = q >= 0 ? q / 16 : -((15 - q) / 16);  // floor(q / 16)
+  int b = k + 127 + phase_tables()[q - 16 * k].base_offset;
+  return b < 0 ? 0 : (b > 240 ? 240 : b);
+}
+
+double expected_exponent_bits(double sigma, int q) {
+  double p[256];
+  exponent_masses(sigma, p);
+  const int k = q >= 0 ? q / 16 : -((15 - q) / 16);
+  const PhaseTable& t = phase_tables()[q - 16 * k];
+  const int base = base_for_q(q);
+  double bits = 0.0;
+  for (int e = 0; e < 256; ++e) {
+    const int x = e - base;
+    bits += p[e] * (x >= 0 && x < kWindow ? (double)t.lens[x] : (double)(t.lens[kEsc] + 8));
+  }
+  return bits;
+}
+
 }  // namespace zc

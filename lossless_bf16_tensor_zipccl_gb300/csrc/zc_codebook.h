@@ -13,4 +13,13 @@ struct PhaseTable {
 // The 16 phase tables, built on first use (thread-safe).
 const PhaseTable* phase_tables();
 
+// Window start for scale q: floor(q/16) + 127 + the phase's offset, clamped
+// to [0, 240] so that the window stays inside [0, 254].
+int base_for_q(int q);
+
+// Expected code bits of one exponent of X ~ N(0, sigma^2) under the code for
+// scale q (window and lengths of phase q mod 16; an escape costs its
+// codeword and 8 raw bits).
+double expected_exponent_bits(double sigma, int q);
+
 }  // namespace zc

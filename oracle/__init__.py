@@ -90,6 +90,10 @@ def lib():
             L.zo_float_to_bf16_rne.restype = ctypes.c_uint16
             L.zo_format_version.argtypes = []
             L.zo_format_version.restype = ctypes.c_int
+            L.zo_expected_exponent_bits.argtypes = [ctypes.c_double, ctypes.c_int]
+            L.zo_expected_exponent_bits.restype = ctypes.c_double
+            L.zo_predict_chunk_bytes.argtypes = [ctypes.c_uint64, ctypes.c_double, ctypes.POINTER(ctypes.c_double)]
+            L.zo_predict_chunk_bytes.restype = ctypes.c_uint64
             _lib = L
     return _lib
 
@@ -160,6 +164,17 @@ def base_for_q(q: int) -> int:
     offs, _ = phase_tables()
     arr = (ctypes.c_int * 16)(*offs)
     return int(lib().zo_base_for_q(int(q), arr))
+
+
+def expected_exponent_bits(sigma: float, q: int) -> float:
+    """Expected code bits of one exponent of N(0, sigma^2) under the code for scale q."""
+    return float(lib().zo_expected_exponent_bits(float(sigma), int(q)))
+
+
+def predict_chunk_bytes(n: int, sigma: float) -> tuple[int, float]:
+    """Predicted stream bytes of one chunk of n values from N(0, sigma^2) (sigma hint), and bits per value."""
+    bits = ctypes.c_double()
+    return int(lib().zo_predict_chunk_bytes(int(n), float(sigma), ctypes.byref(bits))), float(bits.value)
 
 
 def float_to_bf16_rne(f: float) -> int:

@@ -379,6 +379,50 @@ uint64_t zo_max_compressed_bytes(const uint64_t *chunk_elems, uint32_t n_chunks)
 }
 
 /* ------------------------------------------------------------------------ */
+/* Predicted size: the cost model behind the compressed / plain switch       */
+/* ------------------------------------------------------------------------ */
+/*
+ * The abstract's technique (3) switches collectives between compressed and
+ * uncompressed operation; the pages give no model.  Reading: predict the
+ * stream size of a chunk of n values drawn from N(0, sigma^2), compressed
+ * with a sigma hint, from the closed-form masses: the expected code bits of
+ * one exponent are E = sum_e p(e) L(e), L(e) = lens[e - base] inside the
+ * window and lens[ESC] + 8 outside; a tile's exponent region then takes
+ * ceil(n_t E / 32) words after its segment table, unless raw bytes are not
+ * larger.
+ */
+double zo_expected_exponent_bits(double sigma, int q)
+{
+    double p[256], bits = 0.0;
+    int offs[16], lens_r[ZO_NSYM], r, e, base, k;
+    for (r = 0; r < 16; r++)
+        zo_phase_table(r, &offs[r], lens_r);
+    k = (int)floor_div(q, 16);
+    zo_phase_table(q - 16 * k, &offs[q - 16 * k], lens_r);
+    base = zo_base_for_q(q, offs);
+    zo_exponent_pmf(sigma, p);
+    for (e = 0; e < 256; e++) {
+        int x = e - base;
+        bits += p[e] * (double)((x >= 0 && x < ZO_WINDOW) ? lens_r[x] : lens_r[ZO_ESC] + 8);
+    }
+    return bits;
+}
+
+uint64_t zo_predict_chunk_bytes(uint64_t n, double sigma, double *bits_per_value)
+{
+    double E = zo_expected_exponent_bits(sigma, zo_q_from_sigma(sigma));
+    uint64_t T = n_tiles_of(n), total = ZO_CHUNK_HDR + pad16(4 * T), t;
+    for (t = 0; t < T; t++) {
+        uint64_t nt = (t + 1 < T) ? ZO_TILE : n - t * ZO_TILE;
+        uint64_t coded = ZO_SEGTAB + 4 * (uint64_t)ceil((double)nt * E / 32.0);
+        total += ZO_TILE_HDR + pad16(nt) + pad16(coded < nt ? coded : nt);
+    }
+    if (bits_per_value)
+        *bits_per_value = n ? 8.0 * (double)total / (double)n : 0.0;
+    return total;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Compression                                                               */
 /* ------------------------------------------------------------------------ */
 /* Encode one tile of nt elements at out; returns its size in bytes. */

@@ -109,3 +109,37 @@ def test_product_does_not_touch_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src and "zipccl_oracle" not in src, f
+
+
+# ----------------------------------------------------------------- size prediction / switch
+@pytest.mark.parametrize("n", [0, 1, 1000, 32768, 32769, 70001, 1 << 20, 8388608])
+@pytest.mark.parametrize("sigma", [1e-6, 1e-3, 0.02, 1.0, 100.0, 1e-39])
+def test_predicted_chunk_bytes_match_oracle(n, sigma):
+    s = float(np.float32(sigma))
+    assert zc.zipccl_predict_chunk_bytes(n, s) == oracle.predict_chunk_bytes(n, s)
+
+
+def test_choose_compressed_follows_the_cost_model():
+    n, sigma = 1 << 26, 1e-3
+    pred, _ = zc.zipccl_predict_chunk_bytes(n, sigma)
+    for link in [10.0, 100.0, 900.0, 5000.0]:
+        use, sp = zc.zipccl_choose_compressed(n, sigma, link, 1700.0, 2200.0, 0.1)
+        t_raw = 2 * n / link
+        t_zip = 2 * n / 1700.0 + pred / link + 2 * n / 2200.0
+        assert sp == pytest.approx(t_raw / t_zip, rel=1e-12)
+        assert use == (t_raw / t_zip > 1.1)
+    assert zc.zipccl_choose_compressed(n, sigma, 10.0, 1700.0, 2200.0)[0]
+    assert not zc.zipccl_choose_compressed(n, sigma, 5000.0, 1700.0, 2200.0)[0]
+    # a margin larger than the predicted gain keeps the plain exchange
+    sp = zc.zipccl_choose_compressed(n, sigma, 100.0, 1700.0, 2200.0, 0.0)[1]
+    assert not zc.zipccl_choose_compressed(n, sigma, 100.0, 1700.0, 2200.0, sp)[0]
+
+
+@pytest.mark.parametrize("args", [(1000, 0.0, 10.0, 1.0, 1.0, 0.1), (1000, -1.0, 10.0, 1.0, 1.0, 0.1),
+                                  (1000, float("inf"), 10.0, 1.0, 1.0, 0.1), (1000, 1.0, 0.0, 1.0, 1.0, 0.1),
+                                  (1000, 1.0, 10.0, 0.0, 1.0, 0.1), (1000, 1.0, 10.0, 1.0, -1.0, 0.1),
+                                  (1000, 1.0, 10.0, 1.0, 1.0, -0.5), (1 << 40, 1.0, 10.0, 1.0, 1.0, 0.1)])
+def test_switch_argument_errors(args):
+    with pytest.raises(zc.ZipcclError) as ei:
+        zc.zipccl_choose_compressed(*args)
+    assert ei.value.status == zc.ERR_INVALID_ARG

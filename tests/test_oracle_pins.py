@@ -362,3 +362,37 @@ def test_reduce_k1_is_decode_and_negation_cancels():
     s2, _ = oracle.compress(neg)
     y = oracle.decompress_reduce([s, s2], x.size)
     assert np.all(y == 0)
+
+
+# ----------------------------------------------------------------- size prediction
+@pytest.mark.parametrize("sigma", [1e-3, 0.02, 1.0, 37.0])
+def test_expected_exponent_bits_from_scipy_masses(sigma):
+    # the predictor's E = sum_e p(e) L(e) with scipy's masses, the phase
+    # table's lengths and window, an escape costing its codeword + 8 bits
+    q = oracle.q_from_sigma(sigma)
+    offs, lens = oracle.phase_tables()
+    base = oracle.base_for_q(q)
+    p = scipy_pmf(sigma)
+    L = np.array([lens[q % 16][e - base] if 0 <= e - base < 15 else lens[q % 16][15] + 8 for e in range(256)])
+    assert oracle.expected_exponent_bits(sigma, q) == pytest.approx(float((p * L).sum()), rel=1e-9)
+
+
+@pytest.mark.parametrize("sigma,seed", [(0.02, 1), (1e-3, 2), (1.0, 3)])
+def test_predicted_size_matches_compressed_gaussian(sigma, seed):
+    # the model's size against a stream compressed from N(0, sigma^2) data:
+    # sampling noise in the code lengths of 2^20 values is ~0.03%
+    n = 1 << 20
+    x = workloads.gaussian_bf16(n, sigma, 500 + seed)
+    s, _ = oracle.compress(x, [n], [sigma])
+    pred, bits = oracle.predict_chunk_bytes(n, sigma)
+    assert abs(pred - len(s)) / len(s) < 2e-3
+    assert bits == pytest.approx(8.0 * pred / n)
+
+
+def test_predicted_bits_bounded_by_entropy():
+    # 8 raw bits + the code's expected length: at least 8 + H(sigma), and
+    # within the measured redundancy of the 10-bit-limited code (+ metadata)
+    for sigma in [1e-5, 3e-3, 0.5, 20.0]:
+        _, bits = oracle.predict_chunk_bytes(1 << 24, sigma)
+        H = float(-(lambda p: (p[p > 0] * np.log2(p[p > 0])).sum())(scipy_pmf(sigma)))
+        assert 8.0 + H <= bits <= 8.0 + H + 0.1
