@@ -122,7 +122,27 @@ class ClockSampler:
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+        # nvidia-smi takes a moment to start: the timed region begins once it samples
+        self.wait_samples(1, 5.0)
         return self
+
+    def lines(self) -> int:
+        try:
+            with open(self.path) as f:
+                return sum(1 for line in f if line.count(",") >= 8)
+        except OSError:
+            return 0
+
+    def wait_samples(self, n: int, limit_s: float, work=None) -> None:
+        """Until the record holds n samples (or limit_s passes), calling work() meanwhile."""
+        if self.proc is None:
+            return
+        t0 = time.time()
+        while self.lines() < n and time.time() - t0 < limit_s:
+            if work is not None:
+                work()
+            else:
+                time.sleep(0.01)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -298,6 +318,7 @@ def run_ours(args, rank: int, world: int):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index) as clk:
+        n0 = clk.lines()
         for i in range(args.steps):
             flush.fill_(i & 0xFF)          # untimed: L2 flush
             ev[i][0].record(stream)
@@ -305,6 +326,15 @@ def run_ours(args, rank: int, world: int):
                 f()
                 ev[i][j + 1].record(stream)
         torch.cuda.synchronize(dev)
+
+        def more_steps():  # untimed, the same work: the clock record brackets the timed region under load
+            for _ in range(50):
+                flush.fill_(0)
+                for _, f in stages:
+                    f()
+            torch.cuda.synchronize(dev)
+
+        clk.wait_samples(n0 + 2, 3.0, more_steps)
     if world > 1:
         torch.distributed.barrier()
     stage_ms = {name: [ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)]
