@@ -165,6 +165,17 @@ zipccl_status zipccl_decompress_reduce_noalloc(const void *const *d_peer_chunks,
 zipccl_status zipccl_get_device_status(const void *d_ws, void *stream);
 
 /*
+ * Self-test of the bounded device waits: which = 0 runs the compressor's
+ * look-back for a tile whose predecessor never publishes its state; which =
+ * 1 waits for an mbarrier phase that never completes (the wait used for the
+ * decoders' payload copies).  The wait gives up after its limit (2 s) and
+ * the kernel records ZIPCCL_ERR_TIMEOUT in the workspace status, read with
+ * zipccl_get_device_status; nothing faults and the context stays usable.
+ * d_ws: at least 272 bytes, 256-byte aligned.  Asynchronous on `stream`.
+ */
+zipccl_status zipccl_selftest_bounded_wait(int which, void *d_ws, uint64_t ws_bytes, void *stream);
+
+/*
  * Cost model of the switch between compressed and plain exchange ("ZipCCL:
  * Efficient Lossless Data Compression of Communication Collectives for
  * Accelerating LLM Training", abstract, technique (3): collectives switch

@@ -28,7 +28,7 @@ __all__ = [
     "zipccl_max_compressed_bytes", "zipccl_compress_workspace_bytes", "zipccl_decompress_workspace_bytes",
     "zipccl_reduce_workspace_bytes", "zipccl_compress", "zipccl_decompress", "zipccl_decompress_reduce",
     "zipccl_get_device_status", "zipccl_codebook_phase", "zipccl_decompress_reduce_noalloc",
-    "zipccl_predict_chunk_bytes", "zipccl_choose_compressed", "compress", "decompress", "decompress_reduce",
+    "zipccl_predict_chunk_bytes", "zipccl_choose_compressed", "zipccl_selftest_bounded_wait", "compress", "decompress", "decompress_reduce",
     "Compressed", "EXPORTED_SYMBOLS",
 ]
 
@@ -38,7 +38,7 @@ EXPORTED_SYMBOLS = [
     "zipccl_compress_workspace_bytes", "zipccl_decompress_workspace_bytes", "zipccl_reduce_workspace_bytes",
     "zipccl_compress", "zipccl_decompress", "zipccl_decompress_reduce", "zipccl_get_device_status",
     "zipccl_codebook_phase", "zipccl_decompress_reduce_noalloc", "zipccl_predict_chunk_bytes",
-    "zipccl_choose_compressed",
+    "zipccl_choose_compressed", "zipccl_selftest_bounded_wait",
 ]
 
 _lock = threading.Lock()
@@ -104,6 +104,8 @@ def load(build_if_missing: bool = True):
         dbl = ctypes.c_double
         L.zipccl_predict_chunk_bytes.restype = ctypes.c_int
         L.zipccl_predict_chunk_bytes.argtypes = [u64, ctypes.c_float, u64p, ctypes.POINTER(dbl)]
+        L.zipccl_selftest_bounded_wait.restype = ctypes.c_int
+        L.zipccl_selftest_bounded_wait.argtypes = [ctypes.c_int, vp, u64, vp]
         L.zipccl_choose_compressed.restype = ctypes.c_int
         L.zipccl_choose_compressed.argtypes = [u64, ctypes.c_float, dbl, dbl, dbl, dbl, ctypes.POINTER(ctypes.c_int),
                                                ctypes.POINTER(dbl)]
@@ -197,6 +199,11 @@ def zipccl_codebook_phase(phase: int) -> tuple[int, list[int]]:
     lens = (ctypes.c_uint8 * 16)()
     _check(load().zipccl_codebook_phase(int(phase), ctypes.byref(off), lens), "zipccl_codebook_phase")
     return off.value, list(lens)
+
+
+def zipccl_selftest_bounded_wait(which: int, ws_ptr: int, ws_bytes: int, stream_ptr: int) -> int:
+    """Run one bounded wait that must give up (0: look-back, 1: mbarrier); returns the call's status."""
+    return int(load().zipccl_selftest_bounded_wait(int(which), ws_ptr, int(ws_bytes), stream_ptr))
 
 
 def zipccl_predict_chunk_bytes(n: int, sigma: float) -> tuple[int, float]:

@@ -312,6 +312,16 @@ zipccl_status zipccl_choose_compressed(uint64_t n, float sigma, double link_gbs,
   return ZIPCCL_OK;
 }
 
+zipccl_status zipccl_selftest_bounded_wait(int which, void* d_ws, uint64_t ws_bytes, void* stream) {
+  if ((which != 0 && which != 1) || !d_ws || !aligned(d_ws, 256) || ws_bytes < sizeof(WsHeader) + 16)
+    return ZIPCCL_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(d_ws);
+  if (cudaMemsetAsync(ws, 0, sizeof(WsHeader) + 16, s) != cudaSuccess) return ZIPCCL_ERR_CUDA;
+  return cuda_status(launch_selftest_wait(reinterpret_cast<WsHeader*>(ws), reinterpret_cast<uint64_t*>(ws + sizeof(WsHeader)),
+                                          which, s));
+}
+
 zipccl_status zipccl_codebook_phase(int phase, int* base_offset, uint8_t* lens16) {
   if (phase < 0 || phase > 15 || !base_offset || !lens16) return ZIPCCL_ERR_INVALID_ARG;
   const PhaseTable& t = phase_tables()[phase];

@@ -924,7 +924,34 @@ __global__ void __launch_bounds__(kEncThreads, 1) zc_encode_kernel(EncodeArgs a)
   }
 }
 
+// ---------------------------------------------------------------- bounded-wait self-test
+// One warp waits, through the encoder's and the decoders' own code, on
+// something no one completes: the look-back state of a predecessor tile
+// (which = 0: tile 1 waits on tile 0, whose state stays 0) or the phase of an
+// mbarrier no one arrives on (which = 1).  The wait gives up at its limit and
+// the kernel records the timeout in the workspace status.
+__global__ void zc_selftest_wait_kernel(WsHeader* hdr, uint64_t* state, int which) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t lane = threadIdx.x & 31;
+  bool timed_out;
+  if (which == 0) {
+    bool err = false;
+    (void)lookback(state, 1, lane, err);
+    timed_out = err;
+  } else {
+    if (lane == 0) mbar_init(&bar, 1);
+    __syncwarp();
+    timed_out = __any_sync(kFull, !mbar_wait(&bar, 0));
+  }
+  if (lane == 0 && timed_out) set_status(hdr, kStTimeout);
+}
+
 // ---------------------------------------------------------------- launchers
+cudaError_t launch_selftest_wait(WsHeader* hdr, uint64_t* state, int which, cudaStream_t s) {
+  zc_selftest_wait_kernel<<<1, 32, 0, s>>>(hdr, state, which);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_select(const SelectArgs& args, cudaStream_t s) {
   if (args.count == 0) return cudaSuccess;
   zc_select_kernel<<<args.count, 256, 0, s>>>(args);

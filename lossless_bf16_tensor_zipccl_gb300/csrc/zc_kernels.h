@@ -104,6 +104,7 @@ inline cudaLaunchConfig_t follow_config(dim3 grid, dim3 block, size_t smem, cuda
 }
 
 cudaError_t launch_select(const SelectArgs& args, cudaStream_t s);
+cudaError_t launch_selftest_wait(WsHeader* hdr, uint64_t* state, int which, cudaStream_t s);
 cudaError_t launch_encode(const EncodeArgs& args, uint32_t n_items, cudaStream_t s);
 cudaError_t launch_decode(const DprepArgs& prep, const DecodeArgs& args, uint32_t max_items, cudaStream_t s);
 cudaError_t launch_reduce(const ReduceArgs& args, cudaStream_t s);

@@ -86,6 +86,14 @@ def test_compress_argument_errors_return_before_launch():
         zc.ERR_INVALID_ARG
 
 
+def test_selftest_argument_errors_return_before_launch():
+    assert zc.zipccl_selftest_bounded_wait(2, FAKE, 512, 0) == zc.ERR_INVALID_ARG
+    assert zc.zipccl_selftest_bounded_wait(-1, FAKE, 512, 0) == zc.ERR_INVALID_ARG
+    assert zc.zipccl_selftest_bounded_wait(0, 0, 512, 0) == zc.ERR_INVALID_ARG
+    assert zc.zipccl_selftest_bounded_wait(0, FAKE + 16, 512, 0) == zc.ERR_INVALID_ARG
+    assert zc.zipccl_selftest_bounded_wait(1, FAKE, 271, 0) == zc.ERR_INVALID_ARG
+
+
 def test_decompress_and_reduce_argument_errors():
     ws = zc.zipccl_decompress_workspace_bytes(100, 1)
     assert zc.zipccl_decompress(FAKE, FAKE, 0, FAKE, 100, FAKE, ws, 0) == zc.ERR_INVALID_ARG

@@ -231,6 +231,22 @@ def test_corrupt_streams_report_status():
     assert corrupt_status(s[: int(short[-1])], short, n) == zc.ERR_CORRUPT  # truncated
 
 
+@pytest.mark.parametrize("which", [0, 1])
+def test_bounded_wait_gives_up_and_context_stays_usable(which):
+    # 0: the compressor's look-back on a predecessor that never publishes;
+    # 1: an mbarrier phase that never completes.  Each wait has a 2 s limit.
+    import time
+    ws = torch.empty(512, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    assert zc.zipccl_selftest_bounded_wait(which, ws.data_ptr(), ws.numel(), s) == zc.OK
+    assert zc.zipccl_get_device_status(ws.data_ptr(), s) == zc.ERR_TIMEOUT
+    dt = time.perf_counter() - t0
+    assert 1.5 < dt < 30.0, f"wait took {dt:.2f} s"
+    gpu_roundtrip(workloads.gaussian_bf16(70000, 0.02, 11))
+
+
 # ------------------------------------------------------------------ full-size workloads
 def sampled_chunk_parity(w: workloads.Workload, c: zc.Compressed, chunks_to_check):
     s, offs = stream_bytes(c)
