@@ -213,13 +213,15 @@ __device__ __forceinline__ void build_lut(uint64_t lens, uint32_t* lut, uint32_t
 }
 
 // ---------------------------------------------------------------- merge
-// 4 exponent bytes + 4 sign/mantissa bytes -> 4 BF16 words (2 x u32).
+// 4 exponent bytes + 4 sign/mantissa bytes (sign in bit 7) -> 4 BF16 words
+// (2 x u32).  All four high bytes (sign, exponent bits 7..1) and all four low
+// bytes (exponent bit 0, mantissa) are formed at once, then interleaved.
 __device__ __forceinline__ uint2 merge4(uint32_t e4, uint32_t sm4) {
-  const uint32_t e01 = __byte_perm(e4, 0, 0x4140), e23 = __byte_perm(e4, 0, 0x4342);
-  const uint32_t s01 = __byte_perm(sm4, 0, 0x4140), s23 = __byte_perm(sm4, 0, 0x4342);
+  const uint32_t hi = (sm4 & 0x80808080u) | ((e4 >> 1) & 0x7F7F7F7Fu);
+  const uint32_t lo = ((e4 << 7) & 0x80808080u) | (sm4 & 0x7F7F7F7Fu);
   uint2 r;
-  r.x = ((s01 & 0x00800080u) << 8) | (e01 << 7) | (s01 & 0x007F007Fu);
-  r.y = ((s23 & 0x00800080u) << 8) | (e23 << 7) | (s23 & 0x007F007Fu);
+  r.x = __byte_perm(lo, hi, 0x5140);
+  r.y = __byte_perm(lo, hi, 0x7362);
   return r;
 }
 
@@ -312,9 +314,11 @@ struct LaneDecoder {
 
   // Warp-wide: decode until every lane holds at least `need` symbols (need
   // <= 8); lanes that are there already keep decoding while they have room,
-  // so the next row starts ahead.  All 32 lanes must call this together.
+  // so the next row starts ahead.  All 32 lanes must call this together,
+  // after init or take8, which leave at most 8 symbols pending: the first
+  // step always has room.
   __device__ __forceinline__ void fill_warp(uint32_t need) {
-    if (cnt4 <= 44) step();
+    step();
     if (cnt4 <= 44) step();
     while (__any_sync(kFull, cnt4 < 4 * need)) {
       if (cnt4 <= 44) step();
