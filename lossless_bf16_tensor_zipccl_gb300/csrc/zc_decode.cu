@@ -147,7 +147,7 @@ struct RowSource {
     uint32_t lo = 0, hi = 0;
     if (tv.mode == 0) {
       dec.fill_warp(cnt);
-      dec.take8(lo, hi);
+      dec.template take8<false>(lo, hi);
     } else {
       const uint2 e = load_bytes8(tv.tile + tv.exp_off + r * kRow + col, cnt);
       lo = e.x;
@@ -307,7 +307,7 @@ __device__ __forceinline__ void decode_rows(RowSource<kStaged>& src, bool full, 
       if (r + kSmAhead < kRows) sq[r % kSmAhead] = ld_stream_v2(smp + (r + kSmAhead) * kRow);
       uint32_t elo, ehi;
       src.dec.fill_warp(8);
-      src.dec.take8(elo, ehi);
+      src.dec.template take8<true>(elo, ehi);
       const uint2 u = merge4(elo, sm.x), v = merge4(ehi, sm.y);
       *reinterpret_cast<uint4*>(y + r * kRow) = make_uint4(u.x, u.y, v.x, v.y);
     }
@@ -584,7 +584,7 @@ __device__ __forceinline__ bool reduce_rows(RowSource<kStaged>& src, const uint8
     for (uint32_t r = 0; r < kRows; ++r) {
       uint32_t elo, ehi;
       src.dec.fill_warp(8);
-      src.dec.take8(elo, ehi);
+      src.dec.template take8<true>(elo, ehi);
       const uint2 sm = sq[r % kSmAhead];
       if (r + kSmAhead < kRows) sq[r % kSmAhead] = ld_stream_v2(smp + (r + kSmAhead) * kRow);
       const uint2 u = merge4(elo, sm.x), w = merge4(ehi, sm.y);

@@ -326,27 +326,35 @@ struct LaneDecoder {
   }
 
   // Pop 8 pending symbols as exponent bytes (e0..e3, e4..e7); with fewer
-  // pending (a segment's last row) the missing ones are garbage.
+  // pending (a segment's last row) the missing ones are garbage.  kRow8: at
+  // least 8 are pending (every row of a full tile).  Escape bytes are kept
+  // per queue position; bytes whose escm bit is clear are never read, so the
+  // escape registers move only while an escape is pending.
+  template <bool kRow8>
   __device__ __forceinline__ void take8(uint32_t& e_lo, uint32_t& e_hi) {
     // the oldest 8 symbols, oldest in the top nibble
-    const uint32_t e32 = cnt4 >= 32 ? __funnelshift_rc(qlo, qhi, cnt4 - 32) : __funnelshift_lc(0u, qlo, 32 - cnt4);
+    uint32_t e32;
+    if constexpr (kRow8) e32 = __funnelshift_rc(qlo, qhi, cnt4 - 32);
+    else e32 = cnt4 >= 32 ? __funnelshift_rc(qlo, qhi, cnt4 - 32) : __funnelshift_lc(0u, qlo, 32 - cnt4);
     const uint32_t ev = e32 & 0x0F0F0F0Fu, od = (e32 >> 4) & 0x0F0F0F0Fu;
     e_lo = __byte_perm(ev, od, 0x2637) + base4;
     e_hi = __byte_perm(ev, od, 0x0415) + base4;
-    if (__builtin_expect((escm & 0xFFu) != 0, 0)) {  // substitute the raw exponents of escapes
+    if (__builtin_expect(escm != 0, 0)) {
       const uint32_t m = escm;
-      const uint32_t m0 = (m & 1 ? 0xFFu : 0u) | (m & 2 ? 0xFF00u : 0u) | (m & 4 ? 0xFF0000u : 0u) |
-                          (m & 8 ? 0xFF000000u : 0u);
-      const uint32_t m1 = (m & 16 ? 0xFFu : 0u) | (m & 32 ? 0xFF00u : 0u) | (m & 64 ? 0xFF0000u : 0u) |
-                          (m & 128 ? 0xFF000000u : 0u);
-      e_lo = (e_lo & ~m0) | (esc0 & m0);
-      e_hi = (e_hi & ~m1) | (esc1 & m1);
+      if (m & 0xFFu) {  // substitute the raw exponents of escapes
+        const uint32_t m0 = (m & 1 ? 0xFFu : 0u) | (m & 2 ? 0xFF00u : 0u) | (m & 4 ? 0xFF0000u : 0u) |
+                            (m & 8 ? 0xFF000000u : 0u);
+        const uint32_t m1 = (m & 16 ? 0xFFu : 0u) | (m & 32 ? 0xFF00u : 0u) | (m & 64 ? 0xFF0000u : 0u) |
+                            (m & 128 ? 0xFF000000u : 0u);
+        e_lo = (e_lo & ~m0) | (esc0 & m0);
+        e_hi = (e_hi & ~m1) | (esc1 & m1);
+      }
+      esc0 = esc2;
+      esc1 = esc3;
+      escm = m >> 8;
     }
-    cnt4 = cnt4 > 32 ? cnt4 - 32 : 0;  // fewer than 8 only on a segment's last row
-    esc0 = esc2;
-    esc1 = esc3;
-    esc2 = esc3 = 0;
-    escm >>= 8;
+    if constexpr (kRow8) cnt4 -= 32;
+    else cnt4 = cnt4 > 32 ? cnt4 - 32 : 0;  // fewer than 8 only on a segment's last row
   }
 };
 
