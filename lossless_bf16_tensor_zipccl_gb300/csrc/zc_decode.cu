@@ -510,6 +510,14 @@ __device__ __forceinline__ uint32_t f32_to_bf16_rne(float f) {
   return u >> 16;
 }
 
+// Two values as packed BF16 words (a low, b high), round to nearest even,
+// subnormals kept; a NaN input gives a NaN whose payload the caller fixes.
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2_rn(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+
 // One block per half tile, one warp per peer.  Each warp stages the payload
 // bits of its peer's half tile in shared memory with one TMA bulk copy and
 // decodes its half rows with the sign/mantissa bytes read straight from
@@ -573,7 +581,14 @@ __device__ __forceinline__ bool reduce_rows(RowSource<kStaged>& src, const uint8
       const uint32_t cnt = src.count(r);
       uint32_t o[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) o[q] = f32_to_bf16_rne(f[2 * q]) | (f32_to_bf16_rne(f[2 * q + 1]) << 16);
+      for (int q = 0; q < 4; ++q) o[q] = f32x2_to_bf16x2_rn(f[2 * q], f[2 * q + 1]);
+      // the sum of the 8 values is NaN when any of them is (or when infinities
+      // cancel): only then are the words formed one by one, NaN as 0x7FC0
+      const float any = ((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7]));
+      if (__builtin_expect(any != any, 0)) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) o[q] = f32_to_bf16_rne(f[2 * q]) | (f32_to_bf16_rne(f[2 * q + 1]) << 16);
+      }
       if (cnt) store_row(y + r * kRow + col, cnt, (reinterpret_cast<uintptr_t>(y) & 15) == 0, make_uint4(o[0], o[1], o[2], o[3]));
     }
     mbar_arrive(done + kRedBufs * p + j);
