@@ -317,6 +317,23 @@ def test_pr1_entropy_and_bits_per_value():
     assert 100.0 * (1.0 - len(s) / (2 * w.n)) > g["size_reduction_percent"]
 
 
+def test_moe_dispatch_within_one_percent_of_chunk_entropy():
+    # Outlier-heavy activations routed to 64 expert chunks: the code built
+    # from the Gaussian pmf of each chunk's sampled scale still comes within
+    # 1% of 8 + the chunk's empirical exponent entropy (outliers escape).
+    w = workloads.moe(tokens=1024)
+    e = ((w.x >> 7) & 0xFF).astype(np.int64)
+    bound, st = 0.0, 0
+    for n in w.chunk_elems:
+        if n:
+            c = np.bincount(e[st:st + n], minlength=256)
+            p = c[c > 0] / n
+            bound += n * (8.0 - np.sum(p * np.log2(p)))
+        st += n
+    s, _ = oracle.compress(w.x, w.chunk_elems)
+    assert 8.0 * len(s) <= 1.01 * bound
+
+
 # ------------------------------------------------------------ decompress_reduce
 def torch_bf16_rne(f32: np.ndarray) -> np.ndarray:
     import torch
