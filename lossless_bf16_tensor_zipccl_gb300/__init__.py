@@ -272,11 +272,21 @@ def _words(x):
     return x.reshape(-1)
 
 
-def _ws(nbytes: int, device, ws=None):
+def _ws(nbytes: int, device, ws=None, stream=None):
     torch = _torch()
     if ws is not None and ws.numel() >= nbytes:
         return ws
-    return torch.empty(max(256, nbytes), dtype=torch.uint8, device=device)
+    return _keep(torch.empty(max(256, nbytes), dtype=torch.uint8, device=device), stream)
+
+
+def _keep(t, stream):
+    """A tensor allocated here and used by work on `stream`: when that is not
+    the current stream, the caching allocator must not hand its memory out
+    again before the work on `stream` is done."""
+    torch = _torch()
+    if stream is not None and stream != torch.cuda.current_stream(t.device):
+        t.record_stream(stream)
+    return t
 
 
 def compress(x, chunk_elems=None, sigma_hint=None, out=None, offsets=None, ws=None, stream=None) -> Compressed:
@@ -287,11 +297,11 @@ def compress(x, chunk_elems=None, sigma_hint=None, out=None, offsets=None, ws=No
     chunk_elems = [n] if chunk_elems is None else [int(c) for c in chunk_elems]
     cap = zipccl_max_compressed_bytes(chunk_elems)
     if out is None or out.numel() < cap:
-        out = torch.empty(max(16, cap), dtype=torch.uint8, device=w.device)
+        out = _keep(torch.empty(max(16, cap), dtype=torch.uint8, device=w.device), stream)
     if offsets is None:
-        offsets = torch.empty(len(chunk_elems) + 1, dtype=torch.int64, device=w.device)
+        offsets = _keep(torch.empty(len(chunk_elems) + 1, dtype=torch.int64, device=w.device), stream)
     wsb = zipccl_compress_workspace_bytes(chunk_elems)
-    ws = _ws(wsb, w.device, ws)
+    ws = _ws(wsb, w.device, ws, stream)
     st = zipccl_compress(w.data_ptr(), n, chunk_elems, sigma_hint, out.data_ptr(), out.numel(),
                          offsets.data_ptr(), ws.data_ptr(), ws.numel(), _stream_ptr(stream))
     _check(st, "zipccl_compress")
@@ -302,9 +312,9 @@ def decompress(c: Compressed, out=None, ws=None, stream=None):
     """Decompress into a bfloat16 tensor of c.n elements (bit-identical)."""
     torch = _torch()
     if out is None:
-        out = torch.empty(max(1, c.n), dtype=torch.bfloat16, device=c.data.device)[: c.n]
+        out = _keep(torch.empty(max(1, c.n), dtype=torch.bfloat16, device=c.data.device), stream)[: c.n]
     wsb = zipccl_decompress_workspace_bytes(c.n, c.n_chunks)
-    ws = _ws(wsb, c.data.device, ws)
+    ws = _ws(wsb, c.data.device, ws, stream)
     st = zipccl_decompress(c.data.data_ptr(), c.offsets.data_ptr(), c.n_chunks, out.data_ptr(), c.n,
                            ws.data_ptr(), ws.numel(), _stream_ptr(stream))
     _check(st, "zipccl_decompress")
@@ -318,9 +328,9 @@ def decompress_reduce(peer_chunks, n: int, out=None, ws=None, stream=None):
     k = len(peer_chunks)
     dev = peer_chunks[0].device
     if out is None:
-        out = torch.empty(max(1, n), dtype=torch.bfloat16, device=dev)[:n]
+        out = _keep(torch.empty(max(1, n), dtype=torch.bfloat16, device=dev), stream)[:n]
     wsb = zipccl_reduce_workspace_bytes(k)
-    ws = _ws(wsb, dev, ws)
+    ws = _ws(wsb, dev, ws, stream)
     st = zipccl_decompress_reduce([p.data_ptr() for p in peer_chunks], [p.numel() for p in peer_chunks], k, n,
                                   out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_ptr(stream))
     _check(st, "zipccl_decompress_reduce")

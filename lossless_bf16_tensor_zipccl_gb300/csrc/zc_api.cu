@@ -100,7 +100,7 @@ zipccl_status zipccl_max_compressed_bytes(const uint64_t* chunk_elems, uint32_t 
   uint64_t total = 0;
   for (uint32_t c = 0; c < n_chunks; ++c) {
     uint64_t b;
-    if (!chunk_bound(chunk_elems[c], &b)) return ZIPCCL_ERR_INVALID_ARG;
+    if (!chunk_bound(chunk_elems[c], &b) || total + b < total) return ZIPCCL_ERR_INVALID_ARG;
     total += b;
   }
   *out_bytes = total;
@@ -138,7 +138,7 @@ zipccl_status zipccl_compress(const uint16_t* d_in, uint64_t n, const uint64_t* 
   uint64_t sum = 0, bound = 0;
   for (uint32_t c = 0; c < n_chunks; ++c) {
     uint64_t b;
-    if (!chunk_bound(chunk_elems[c], &b)) return ZIPCCL_ERR_INVALID_ARG;
+    if (!chunk_bound(chunk_elems[c], &b) || bound + b < bound) return ZIPCCL_ERR_INVALID_ARG;
     sum += chunk_elems[c];
     bound += b;
   }

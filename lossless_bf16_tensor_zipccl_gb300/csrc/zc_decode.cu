@@ -20,6 +20,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "zc_device.cuh"
 #include "zc_kernels.h"
 
@@ -718,7 +720,9 @@ __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
 }
 
 // ---------------------------------------------------------------- launchers
-static int g_red_attr_done[64];
+// Per device: the reduce kernels' shared-memory limits are set.  Calls from
+// several host threads may both do the set-up; each stores the same value.
+static std::atomic<int> g_red_attr_done[64];
 
 cudaError_t launch_decode(const DprepArgs& prep, const DecodeArgs& args, uint32_t max_items, cudaStream_t s) {
   zc_dprep_kernel<<<prep.n_chunks * kLutParts + 1, 256, 0, s>>>(prep);
@@ -747,14 +751,14 @@ cudaError_t launch_reduce(const ReduceArgs& args, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!g_red_attr_done[dev]) {
+  if (!g_red_attr_done[dev].load(std::memory_order_acquire)) {
     const cudaError_t es[kMaxPeers] = {reduce_setup<1>(),  reduce_setup<2>(),  reduce_setup<3>(),  reduce_setup<4>(),
                                        reduce_setup<5>(),  reduce_setup<6>(),  reduce_setup<7>(),  reduce_setup<8>(),
                                        reduce_setup<9>(),  reduce_setup<10>(), reduce_setup<11>(), reduce_setup<12>(),
                                        reduce_setup<13>(), reduce_setup<14>(), reduce_setup<15>(), reduce_setup<16>()};
     for (const cudaError_t x : es)
       if (x != cudaSuccess) return x;
-    g_red_attr_done[dev] = 1;
+    g_red_attr_done[dev].store(1, std::memory_order_release);
   }
   zc_rprep_kernel<<<args.k * kLutParts, 256, 0, s>>>(args);
   e = cudaGetLastError();

@@ -17,6 +17,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "zc_device.cuh"
 #include "zc_kernels.h"
 
@@ -958,14 +960,17 @@ cudaError_t launch_select(const SelectArgs& args, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-static int g_enc_ctas[64];  // co-resident encode CTAs per device (0: not set up)
+// Co-resident encode CTAs per device (0: not set up).  Calls from several
+// host threads may both do the set-up; each stores the same value.
+static std::atomic<int> g_enc_ctas[64];
 
 cudaError_t launch_encode(const EncodeArgs& args, uint32_t n_items, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!g_enc_ctas[dev]) {
+  int ctas = g_enc_ctas[dev].load(std::memory_order_acquire);
+  if (!ctas) {
     e = cudaFuncSetAttribute(zc_encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEncSmem);
     if (e != cudaSuccess) return e;
     int sms = 0, per_sm = 0;
@@ -974,11 +979,12 @@ cudaError_t launch_encode(const EncodeArgs& args, uint32_t n_items, cudaStream_t
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, zc_encode_kernel, kEncThreads, kEncSmem);
     if (e != cudaSuccess) return e;
     if (sms <= 0 || per_sm <= 0) return cudaErrorInvalidConfiguration;
-    g_enc_ctas[dev] = sms * per_sm;
+    ctas = sms * per_sm;
+    g_enc_ctas[dev].store(ctas, std::memory_order_release);
   }
   // Every CTA must be resident for the look-back order to make progress:
   // the cooperative launch guarantees it (or fails).
-  const uint32_t grid = min(n_items, (uint32_t)g_enc_ctas[dev]);
+  const uint32_t grid = min(n_items, (uint32_t)ctas);
   cudaLaunchAttribute at[2];
   const cudaLaunchConfig_t cfg = follow_config(dim3(grid), dim3(kEncThreads), kEncSmem, s, true, at);
   return cudaLaunchKernelEx(&cfg, zc_encode_kernel, args);

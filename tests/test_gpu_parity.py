@@ -231,6 +231,26 @@ def test_corrupt_streams_report_status():
     assert corrupt_status(s[: int(short[-1])], short, n) == zc.ERR_CORRUPT  # truncated
 
 
+def test_side_stream_calls_with_library_allocated_buffers():
+    # Every buffer the helpers allocate is recorded on the call's stream, so
+    # work queued on the current stream meanwhile cannot take its memory.
+    x = workloads.gaussian_bf16(300000, 0.05, 21)
+    d = to_dev(x)
+    peers = [workloads.gaussian_bf16(100000, 0.05, 22, p) for p in range(3)]
+    pc = [torch.from_numpy(np.frombuffer(oracle.compress(p)[0], np.uint8).copy()).cuda() for p in peers]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    c = zc.compress(d, stream=side)
+    y = zc.decompress(c, stream=side)
+    r = zc.decompress_reduce(pc, 100000, stream=side)
+    junk = [torch.full((1 << 20,), 7, dtype=torch.uint8, device="cuda") for _ in range(8)]
+    torch.cuda.synchronize()
+    del junk
+    assert torch.equal(y.view(torch.int16), d)
+    assert np.array_equal(r.view(torch.int16).cpu().numpy().view(np.uint16), oracle.decompress_reduce(
+        [oracle.compress(p)[0] for p in peers], 100000))
+
+
 @pytest.mark.parametrize("which", [0, 1])
 def test_bounded_wait_gives_up_and_context_stays_usable(which):
     # 0: the compressor's look-back on a predecessor that never publishes;
