@@ -1,5 +1,7 @@
 """Host logic of bench.py without a GPU: the reference arm's JSON line, the
-silent non-zero ranks, and the max-over-ranks timing on 2 gloo ranks."""
+silent non-zero ranks, the max-over-ranks timing on 2 gloo ranks, the DRAM
+traffic taken only for the sources it was measured on, and the clock record's
+summary."""
 from __future__ import annotations
 
 import json
@@ -64,3 +66,38 @@ def test_max_over_ranks_gloo_world2():
 
 def test_single_rank_identity():
     assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+def test_traffic_is_used_only_for_the_sources_it_was_taken_on(tmp_path, monkeypatch):
+    csrc = tmp_path / "lossless_bf16_tensor_zipccl_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text("__global__ void k() {}\n")
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sha = bench.sources_sha()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(
+        {"k": {"dram_bytes_per_launch": 1234, "sources_sha": sha}}))
+    assert bench.traffic_for("k") == 1234
+    assert bench.traffic_for("other") is None
+    (csrc / "k.cu").write_text("__global__ void k() { }\n")  # the kernel changed since the capture
+    assert bench.traffic_for("k") is None
+
+
+def test_clock_record_summary(tmp_path):
+    c = bench.ClockSampler(0)
+    c.path = str(tmp_path / "clocks.csv")
+    c.proc = object()  # a record exists
+    rows = [
+        "0, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2070, 1400.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+    ]
+    (tmp_path / "clocks.csv").write_text("\n".join(rows) + "\n")
+    s = c.summary()
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"]
+    rows[0] = "0, 1500, 2070, 900.5, 0x40, Not Active, Active, Not Active, Not Active"
+    (tmp_path / "clocks.csv").write_text("\n".join(rows) + "\n")
+    assert bench.ClockSampler.summary(c)["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert c.lines() == 3
