@@ -158,6 +158,19 @@ def test_reduce_parity(k, n):
     assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), ref)
 
 
+@pytest.mark.parametrize("k", [4, 6, 7, 9, 10, 11, 12, 13, 14, 15])
+def test_reduce_remaining_peer_counts(k):
+    # every peer count is its own kernel instantiation: two full tiles and a
+    # ragged tail, each peer at its own scale (several code tables)
+    n = 2 * 32768 + 4321
+    xs = [workloads.gaussian_bf16(n, 0.003 * 1.7 ** p, 66, k, p) for p in range(k)]
+    chunks = oracle_chunks(xs)
+    ref = oracle.decompress_reduce(chunks, n)
+    y = zc.decompress_reduce(dev_chunks(chunks), n)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), ref)
+
+
 def test_reduce_peers_with_one_table():
     # peers with the same values share peer 0's code lengths: the decode
     # table sits in shared memory
