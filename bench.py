@@ -15,6 +15,15 @@ resident in HBM when timing starts; L2 is flushed before every timed step.
 ``e2e`` times the same step through the public API with pinned host buffers
 and the host<->device copies inside the timed region.
 
+``configs`` (same JSON line) times each workload on its own, compress and
+decompress with L2 flushed before every call: PR1 (1,048,576 values from
+N(0, 0.02^2), plus the round trip of all 65,536 BF16 patterns), the gradient
+bucket, MoE dispatch (134,217,728 values in 64 expert chunks), the FSDP
+all-gather stack (872,415,232 values in 224 row chunks) and the stress mix
+(268,435,456 values in 256 chunks, every 16th incompressible).  Each entry
+gives GB/s of uncompressed BF16, the algorithmic HBM fraction, bits per
+value, the gap to the entropy bound and the oracle's rate on a stated prefix.
+
 ``--impl reference`` times the plain single-threaded CPU oracle on a bounded
 sample of the same workload instead.
 
@@ -47,6 +56,12 @@ PEER_N = 8_388_608
 K_PEERS = 8
 L2_FLUSH_BYTES = 2 * 129 * 1024 * 1024
 KERNELS_PER_STEP = 6  # select, encode, decode-prep, decode, reduce-prep, reduce
+# Every workload is also timed on its own (compress and decompress), after the headline step.
+CONFIG_NAMES = ["pr1", "gradient", "moe", "fsdp", "stress"]
+# Stage whose kernel the `roofline` object describes: the compress call, the largest HBM mover of
+# the step and the stage the 60% bandwidth bar is set on.  Fixed, so that the named kernel does
+# not change between runs with noise; every stage's own fraction is in `stages`.
+ROOFLINE_STAGE = "compress"
 
 
 def parse_args():
@@ -57,6 +72,8 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--configs", default=",".join(CONFIG_NAMES),
+                   help="comma-separated workloads timed after the headline step ('none' for none)")
     return p.parse_args()
 
 
@@ -206,12 +223,36 @@ SAMPLE_DESC = ("oracle compress + decompress of one 8,388,608-value chunk of the
                "of 8 peers x 1,048,576 values; same distribution, GB/s of uncompressed bf16")
 
 
+def host_info() -> dict:
+    """The host's logical CPU count and CPU model (lscpu's model name, else /proc/cpuinfo)."""
+    model = None
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    import platform
+    return {"host_cpus": os.cpu_count(), "cpu_model": model or "unknown", "machine": platform.machine()}
+
+
 def cpu_baseline(repeats: int = 3) -> dict:
     x, pc = oracle_sample()
     ts = [oracle_step(x, pc) for _ in range(repeats)]
     t = statistics.median(ts)
     return {"value": oracle_sample_bytes() / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": SAMPLE_DESC + f"; median of {repeats}"}
+            "sample": SAMPLE_DESC + f"; median of {repeats}", **host_info()}
 
 
 def run_reference(args, rank: int, world: int):
@@ -228,7 +269,8 @@ def run_reference(args, rank: int, world: int):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16/u8 (integer coding), f32 reduce",
         "data": "synthetic (seeded numpy PCG64)", "config": workload_config(args.gpus),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": SAMPLE_DESC},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": SAMPLE_DESC,
+                         **host_info()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -354,7 +396,7 @@ def run_ours(args, rank: int, world: int):
         stage_info[name] = {"ms": ms, "gbs_uncompressed": unc[name] / (ms * 1e-3) / 1e9,
                             "hbm_gbs_algorithmic": algo[name] / (ms * 1e-3) / 1e9,
                             "hbm_frac_of_measured": algo[name] / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
-    dom = max(stage_info, key=lambda k: stage_info[k]["ms"])
+    dom = ROOFLINE_STAGE
     kernel_of = {"compress": "zc_encode_kernel", "decompress": "zc_decode_kernel", "decompress_reduce": "zc_reduce_kernel"}
     ach = stage_info[dom]["hbm_gbs_algorithmic"]
 
@@ -378,8 +420,179 @@ def run_ours(args, rank: int, world: int):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
+    names = [c for c in args.configs.split(",") if c and c != "none"]
+    if rank == 0 and names:
+        line["configs"] = measure_configs(args, zc, torch, dev, pk, names, cpu=world == 1 and not args.no_cpu_baseline,
+                                         gradient_wl=wl)
+    if world > 1:
+        torch.distributed.barrier()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def gaussian_exponent_entropy(sigma: float) -> float:
+    """Entropy (bits) of the biased BF16 exponent of X ~ N(0, sigma^2): binade e >= 1 holds
+    2^(e-127) <= |X| < 2^(e-126), e = 0 holds |X| < 2^-126.  The bound the coded size is set
+    against (8 raw sign/mantissa bits + this per value)."""
+    import math
+    s = sigma * math.sqrt(2.0)
+
+    def mass(lo, hi):  # P(lo <= |X| < hi), from the side of the distribution with more precision
+        a, b = lo / s, hi / s
+        return math.erfc(a) - math.erfc(b) if a > 0.5 else math.erf(b) - math.erf(a)
+
+    ps = [mass(0.0, 2.0 ** -126)] + [mass(2.0 ** (e - 127), 2.0 ** (e - 126)) for e in range(1, 255)]
+    return -sum(p * math.log2(p) for p in ps if p > 0)
+
+
+def empirical_bound_bits(x: np.ndarray, chunk_elems) -> float:
+    """Sum over chunks of n_c * (8 + empirical entropy of the chunk's exponents), per value."""
+    total, pos = 0.0, 0
+    for m in chunk_elems:
+        if m:
+            cnt = np.bincount(((x[pos:pos + m] >> 7) & 0xFF).astype(np.uint8), minlength=256).astype(np.float64)
+            p = cnt[cnt > 0] / m
+            total += m * (8.0 - float((p * np.log2(p)).sum()))
+        pos += m
+    return total / max(1, pos)
+
+
+CONFIG_SIGMA = {"pr1": 0.02, "gradient": 1e-3, "fsdp": 0.02}  # Gaussian workloads with one sigma
+CPU_PREFIX_VALUES = 8 << 20
+
+
+def config_workload(name: str, gradient_wl):
+    import workloads
+    if name == "gradient" and gradient_wl is not None:
+        return gradient_wl
+    return workloads.WORKLOADS[name]()
+
+
+def chunk_prefix(wl, min_values: int, must_hold=None):
+    """Leading whole chunks of a workload holding at least min_values values (and chunk must_hold)."""
+    tot, k = 0, 0
+    for k, m in enumerate(wl.chunk_elems, 1):
+        tot += m
+        if tot >= min_values and (must_hold is None or k > must_hold):
+            break
+    return wl.x[:tot], wl.chunk_elems[:k]
+
+
+def cpu_config_baseline(name: str, wl, repeats: int = 3) -> dict:
+    """The oracle's compress + decompress on a stated prefix of the workload."""
+    import oracle
+    oracle.lib()
+    x, ce = chunk_prefix(wl, CPU_PREFIX_VALUES, must_hold=15 if name == "stress" else None)
+    ts = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        s, offs = oracle.compress(x, ce)
+        oracle.decompress(s, offs, x.size)
+        ts.append(time.perf_counter() - t0)
+    t = statistics.median(ts)
+    return {"value": 4 * x.size / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"oracle compress + decompress of the first {len(ce)} chunks ({x.size:,} values); "
+                      f"GB/s of uncompressed bf16 in and out; median of {repeats}"}
+
+
+def measure_configs(args, zc, torch, dev, pk, names, cpu: bool, gradient_wl=None) -> dict:
+    """Each workload compressed and decompressed on its own: median CUDA-event time of each call over
+    the timed steps, L2 flushed before every call; GB/s of uncompressed BF16 (2 bytes a value),
+    algorithmic HBM bytes (2 a value + the stream) over the measured copy bandwidth, bits per value,
+    and the gap to the entropy bound."""
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    res = {}
+    for name in names:
+        wl = config_workload(name, gradient_wl)
+        n, ce = wl.n, wl.chunk_elems
+        x = torch.from_numpy(wl.x.view(np.int16)).to(dev)
+        cap = zc.zipccl_max_compressed_bytes(ce)
+        out = torch.empty(cap, dtype=torch.uint8, device=dev)
+        offs = torch.empty(len(ce) + 1, dtype=torch.int64, device=dev)
+        ws_c = torch.empty(zc.zipccl_compress_workspace_bytes(ce), dtype=torch.uint8, device=dev)
+        ws_d = torch.empty(zc.zipccl_decompress_workspace_bytes(n, len(ce)), dtype=torch.uint8, device=dev)
+        dec = torch.empty(max(1, n), dtype=torch.int16, device=dev)
+
+        def comp():
+            st = zc.zipccl_compress(x.data_ptr(), n, ce, None, out.data_ptr(), cap, offs.data_ptr(),
+                                    ws_c.data_ptr(), ws_c.numel(), sp)
+            if st != zc.OK:
+                raise zc.ZipcclError(st, f"{name} compress")
+
+        def decomp():
+            st = zc.zipccl_decompress(out.data_ptr(), offs.data_ptr(), len(ce), dec.data_ptr(), n,
+                                      ws_d.data_ptr(), ws_d.numel(), sp)
+            if st != zc.OK:
+                raise zc.ZipcclError(st, f"{name} decompress")
+
+        for _ in range(max(3, args.warmup)):
+            comp()
+            decomp()
+        torch.cuda.synchronize(dev)
+        for ws in (ws_c, ws_d):
+            st = zc.zipccl_get_device_status(ws.data_ptr(), sp)
+            if st != zc.OK:
+                raise zc.ZipcclError(st, f"{name} device status")
+        if not torch.equal(dec[:n], x):
+            raise RuntimeError(f"{name}: round trip mismatch")
+        comp_bytes = int(offs[-1].item())
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            comp()
+            ev[i][1].record(stream)
+            flush.fill_((i + 1) & 0xFF)
+            ev[i][2].record(stream)
+            decomp()
+            ev[i][3].record(stream)
+        torch.cuda.synchronize(dev)
+        tc = statistics.median(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps))
+        td = statistics.median(ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps))
+        algo = 2 * n + comp_bytes
+        bits = 8.0 * comp_bytes / max(1, n)
+        emp = empirical_bound_bits(wl.x, ce)
+        e = {
+            "workload": wl.note, "n_elems": n, "chunks": len(ce),
+            "compress_us": 1e3 * tc, "decompress_us": 1e3 * td,
+            "compress_gbs": 2 * n / (tc * 1e-3) / 1e9, "decompress_gbs": 2 * n / (td * 1e-3) / 1e9,
+            "compress_hbm_frac_of_measured": algo / (tc * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "decompress_hbm_frac_of_measured": algo / (td * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "compressed_bytes": comp_bytes, "bits_per_value": bits, "compression_ratio": comp_bytes / max(1, 2 * n),
+            "empirical_bound_bits": emp, "gap_to_empirical_bound": bits / emp - 1.0,
+            "round_trip": "bit-exact",
+            "l2": "flushed before every call" + (" (input smaller than L2)" if 2 * n < (129 << 20) else ""),
+        }
+        if name in CONFIG_SIGMA:
+            hb = 8.0 + gaussian_exponent_entropy(CONFIG_SIGMA[name])
+            e["closed_form_bound_bits"] = hb
+            e["gap_to_closed_form_bound"] = bits / hb - 1.0
+        if name == "stress":
+            o = offs.cpu().numpy().view(np.uint64)
+            raw = [c for c in range(len(ce)) if c % 16 == 15]
+            e["incompressible_chunk_expansion_max"] = max(float(o[c + 1] - o[c]) / (2 * ce[c]) for c in raw)
+            e["worst_case_bound_ratio"] = cap / (2 * n)
+        if name == "pr1":
+            e["all_patterns_round_trip"] = all_patterns_round_trip(zc, torch, dev)
+        if cpu:
+            e["cpu_baseline"] = {**cpu_config_baseline(name, wl), **host_info()}
+        res[name] = e
+        del x, out, offs, ws_c, ws_d, dec
+        torch.cuda.empty_cache()
+    return res
+
+
+def all_patterns_round_trip(zc, torch, dev) -> str:
+    import workloads
+    w = workloads.all_patterns()
+    x = torch.from_numpy(w.x.view(np.int16)).to(dev)
+    y = zc.decompress(zc.compress(x))
+    torch.cuda.synchronize(dev)
+    if not torch.equal(y.view(torch.int16), x):
+        raise RuntimeError("all 65,536 BF16 patterns: round trip mismatch")
+    return "bit-exact (all 65,536 patterns)"
 
 
 def measure_e2e(args, zc, torch, dev, wl, peer_chunks, peer_bytes, comp_bytes):

@@ -173,8 +173,15 @@ def zipccl_decompress(d_stream: int, d_chunk_offsets: int, n_chunks: int, d_out:
     return int(load().zipccl_decompress(d_stream, d_chunk_offsets, n_chunks, d_out, n, d_ws, ws_bytes, stream))
 
 
+def _peer_arrays_match(d_peer_chunks, peer_chunk_bytes, k: int) -> bool:
+    """The C call reads k entries of each host array: both must hold exactly k."""
+    return int(k) == len(d_peer_chunks) == len(peer_chunk_bytes)
+
+
 def zipccl_decompress_reduce(d_peer_chunks, peer_chunk_bytes, k: int, n: int, d_out: int, d_ws: int,
                              ws_bytes: int, stream: int) -> int:
+    if not _peer_arrays_match(d_peer_chunks, peer_chunk_bytes, k):
+        return ERR_INVALID_ARG
     ptrs = (ctypes.c_void_p * max(1, len(d_peer_chunks)))(*[int(p) for p in d_peer_chunks])
     return int(load().zipccl_decompress_reduce(ptrs, _u64_array(peer_chunk_bytes), k, n, d_out, d_ws, ws_bytes,
                                                stream))
@@ -187,6 +194,8 @@ def zipccl_get_device_status(d_ws: int, stream: int) -> int:
 def zipccl_decompress_reduce_noalloc(d_peer_chunks, peer_chunk_bytes, k: int, n: int, d_out: int,
                                      stream: int) -> tuple[int, int]:
     """The no-allocation reduce call; returns (status, device address of its scratch)."""
+    if not _peer_arrays_match(d_peer_chunks, peer_chunk_bytes, k):
+        return ERR_INVALID_ARG, 0
     ptrs = (ctypes.c_void_p * max(1, len(d_peer_chunks)))(*[int(p) for p in d_peer_chunks])
     scratch = ctypes.c_void_p()
     st = load().zipccl_decompress_reduce_noalloc(ptrs, _u64_array(peer_chunk_bytes), k, n, d_out,

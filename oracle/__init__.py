@@ -35,8 +35,8 @@ _lib = None
 
 OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_CORRUPT, ERR_VERSION = 0, 1, 2, 3, 4
 TILE = 32768
-SEGS = 32
-ROW = 256
+SEGS = 64
+ROW = 512
 LANE_ELEMS = 8
 NSYM = 16
 ESC = 15

@@ -151,3 +151,12 @@ def test_switch_argument_errors(args):
     with pytest.raises(zc.ZipcclError) as ei:
         zc.zipccl_choose_compressed(*args)
     assert ei.value.status == zc.ERR_INVALID_ARG
+
+
+def test_reduce_wrappers_reject_mismatched_peer_arrays():
+    # k must equal the length of both host arrays, or the C call would read past them
+    for call in (lambda p, b, k: zc.zipccl_decompress_reduce(p, b, k, 10, 16, 32, 4096, 0),
+                 lambda p, b, k: zc.zipccl_decompress_reduce_noalloc(p, b, k, 10, 16, 0)[0]):
+        assert call([16, 32], [100, 100], 3) == zc.ERR_INVALID_ARG
+        assert call([16, 32], [100], 2) == zc.ERR_INVALID_ARG
+        assert call([16], [100, 100], 1) == zc.ERR_INVALID_ARG

@@ -204,6 +204,62 @@ def test_select_q_small_and_special_chunks():
     assert oracle.select_q(x) == 23
 
 
+def _large_chunk_sample_input(n=100_003, a=120, e_other=200, shift_block=None, shift=0):
+    """A chunk of n > 4096 values whose 64 sample blocks (64 values at floor(b n / 64), the
+    rule of the scale select) hold exponents a and a + 1 and every other value exponent
+    e_other.  214 sampled values hold a + 1: the first and last of every block and 86 more
+    inside the blocks.  shift_block / shift: move that block's pattern by `shift` positions
+    (the rule then reads one e_other value)."""
+    x = np.full(n, e_other << 7, np.uint16)
+    hi = set()
+    for b in range(64):
+        hi.update({(b, 0), (b, 63)})
+    extra = 214 - len(hi)
+    for b in range(64):
+        for t in range(1, 63):
+            if extra and (b, t) not in hi and t % 9 == 4:
+                hi.add((b, t))
+                extra -= 1
+    assert len(hi) == 214
+    for b in range(64):
+        start = (b * n) // 64 + (shift if b == shift_block else 0)
+        for t in range(64):
+            x[start + t] = (a + ((b, t) in hi)) << 7
+    return x
+
+
+def test_select_q_large_chunk_samples_exactly_the_stated_blocks():
+    # 4096 sampled exponents: 3882 x 120 and 214 x 121.  By hand:
+    #   16 (mean - 127) + 16 c0 + 1/2 = 16 (120 - 127) + 16 * 214 / 4096 + 22.6624 + 0.5
+    #                                 = -112 + 0.8359375 + 23.1624 = -88.0016625  ->  q = -89.
+    # One value from outside the blocks (exponent 200) anywhere in the sample adds at least
+    # 16 * 79 / 4096 = 0.31 and gives q >= -88.
+    assert oracle.select_q(_large_chunk_sample_input()) == -89
+
+
+@pytest.mark.parametrize("b", [0, 1, 17, 31, 32, 50, 62, 63])
+@pytest.mark.parametrize("shift", [-1, 1])
+def test_select_q_large_chunk_block_shift_changes_q(b, shift):
+    # a block placed one position off the rule's start: the sample takes one exponent-200 value
+    # in place of a 121 (and the sum rises by at least 79), so q leaves -89.
+    if b == 0 and shift == -1:
+        pytest.skip("block 0 starts at the first value")
+    x = _large_chunk_sample_input(shift_block=b, shift=shift)
+    assert oracle.select_q(x) != -89
+
+
+def test_select_q_large_chunk_reads_the_whole_block():
+    # the last value of every block becomes exponent 200 (was 121): by hand, the sample is
+    # 64 x 200, 150 x 121 and 3882 x 120, so mean = 120 + (64 * 80 + 150) / 4096 = 121.28662 and
+    #   16 (121.28662 - 127) + 23.1624 = -68.2517  ->  q = -69.
+    # A block length of 63 would not see those values (q = -89); 65 would add more (q > -69).
+    x = _large_chunk_sample_input()
+    n = x.size
+    for b in range(64):
+        x[(b * n) // 64 + 63] = 200 << 7
+    assert oracle.select_q(x) == -69
+
+
 def test_base_clamped_to_valid_window():
     assert oracle.base_for_q(-32768) == 0
     assert oracle.base_for_q(32767) == 240
