@@ -56,6 +56,8 @@ int zipccl_format_version(void);
 const char *zipccl_status_string(int status);
 
 /*
+ * Passage: abstract, technique (3) (collectives fall back to uncompressed
+ * operation) -- read as a per-tile raw fallback, so the expansion is bounded.
  * Exact worst-case compressed size of a chunk layout: every tile stored with
  * raw exponents (bounded expansion).  chunk_elems: host array of n_chunks
  * element counts.  *out_bytes receives the bound.  Host only.
@@ -63,7 +65,12 @@ const char *zipccl_status_string(int status);
 zipccl_status zipccl_max_compressed_bytes(const uint64_t *chunk_elems, uint32_t n_chunks,
                                           uint64_t *out_bytes);
 
-/* Workspace bytes needed by zipccl_compress for this chunk layout. Host only. */
+/*
+ * Workspace sizes, one call per operation (each sizes only what its kernels
+ * use): compress needs per-chunk code tables and per-tile records, the
+ * decoders per-chunk decode tables.  Host only.
+ */
+/* Workspace bytes needed by zipccl_compress for this chunk layout. */
 zipccl_status zipccl_compress_workspace_bytes(const uint64_t *chunk_elems, uint32_t n_chunks,
                                               uint64_t *out_bytes);
 
@@ -74,6 +81,11 @@ zipccl_status zipccl_decompress_workspace_bytes(uint64_t n, uint32_t n_chunks, u
 zipccl_status zipccl_reduce_workspace_bytes(uint32_t k, uint64_t *out_bytes);
 
 /*
+ * Passages: abstract, technique (1) (exponent coding from the Gaussian law,
+ * no expensive online statistics) and technique (2) (GPU compressor with a
+ * communication-aware data layout); shd-paper key-design paragraph
+ * (frequent exponents get short codes); Fig. 6 caption (about 11 bits per
+ * value: sign and mantissa raw).
  * Compress n BF16 words (d_in, bit patterns as uint16) split into n_chunks
  * per-destination chunks: chunk c is the next chunk_elems[c] words (host
  * array, sum == n, n_chunks >= 1, each chunk < 2^31 words; empty chunks are
@@ -98,6 +110,9 @@ zipccl_status zipccl_compress(const uint16_t *d_in, uint64_t n, const uint64_t *
                               uint64_t ws_bytes, void *stream);
 
 /*
+ * Passages: Fig. 6 caption (the decompressor restores each value from its
+ * raw sign/mantissa byte and its decoded exponent); pith summary (lossless:
+ * every byte restored).
  * Decompress n_chunks chunks from d_stream into n BF16 words at d_out,
  * bit-identical to the compressed input.  d_chunk_offsets (device,
  * n_chunks + 1) are the offsets compress wrote; the stream must hold
@@ -110,9 +125,13 @@ zipccl_status zipccl_decompress(const void *d_stream, const uint64_t *d_chunk_of
                                 uint64_t ws_bytes, void *stream);
 
 /*
+ * Passages: Fig. 3 and Fig. 5 captions (zipcclReduceScatter: the receiver
+ * decompresses the peers' chunks and reduces them).
  * Receive side of a reduce-scatter: d_peer_chunks is a host array of k
  * (1 <= k <= 16) device pointers, in rank order, each to one compressed
- * chunk of n elements and peer_chunk_bytes[p] bytes (host array).
+ * chunk of n elements and peer_chunk_bytes[p] bytes (host array; every read
+ * of peer p stays inside those bytes, so a truncated or corrupt chunk gives
+ * ZIPCCL_ERR_CORRUPT instead of a read past it).
  * d_out[i] = bf16_rne(((x0[i] + x1[i]) + x2[i]) ... + x_{k-1}[i]) with every
  * addition in fp32 (round to nearest even, subnormals kept); a NaN result is
  * written as 0x7FC0.  d_ws: at least zipccl_reduce_workspace_bytes bytes.
@@ -123,6 +142,7 @@ zipccl_status zipccl_decompress_reduce(const void *const *d_peer_chunks,
                                        void *stream);
 
 /*
+ * Passages: none; this call has no counterpart in the paper.
  * zipccl_decompress_reduce for callers that may not allocate device memory
  * at the point of the call: code that runs inside a device allocator's own
  * hook or callback (allocating there would re-enter the allocator), and
@@ -139,7 +159,10 @@ zipccl_status zipccl_decompress_reduce(const void *const *d_peer_chunks,
  *     one-time set-up: it looks up the scratch's device address, which may
  *     load this library's kernels onto the device.  Make that first call
  *     before any stream capture begins.  A failed lookup returns
- *     ZIPCCL_ERR_CUDA.
+ *     ZIPCCL_ERR_CUDA.  The address is kept for the life of the process:
+ *     do not call this after cudaDeviceReset on that device, or from a
+ *     context other than the device's primary context; the library's module,
+ *     and the scratch with it, may then sit at another address.
  *   - Each call first clears the scratch's 256-byte status header on
  *     `stream` (cudaMemsetAsync); the rest of the scratch is written before
  *     it is read, so nothing else must start at zero.
@@ -205,11 +228,22 @@ zipccl_status zipccl_choose_compressed(uint64_t n, float sigma, double link_gbs,
                                        double *predicted_speedup);
 
 /*
- * The code this library builds for scale phase r = q mod 16 (0..15): the
- * window start relative to floor(q/16) + 127 and the 16 code lengths
- * (symbols 0..14 = window exponents, 15 = escape).  Host only.
+ * The code this library uses for scale phase r = q mod 16 (0..15), frozen
+ * in format v1: the window start relative to floor(q/16) + 127 and the 16
+ * code lengths (symbols 0..14 = window exponents, 15 = escape).  Host only.
  */
 zipccl_status zipccl_codebook_phase(int phase, int *base_offset, uint8_t *lens16);
+
+/*
+ * Passages: abstract, technique (1); shd-paper key-design paragraph (the
+ * code comes from the Gaussian density).
+ * The same table as zipccl_codebook_phase, derived again from the
+ * closed-form masses at sigma = 2^(phase/16) (exact dynamic program over
+ * Kraft sums, libm erf/erfc).  The library codes only with the frozen
+ * tables of format v1; this call lets a test check that they still equal
+ * their derivation.  Host only.
+ */
+zipccl_status zipccl_codebook_rebuild_phase(int phase, int *base_offset, uint8_t *lens16);
 
 #ifdef __cplusplus
 }

@@ -27,7 +27,8 @@ __all__ = [
     "ZipcclError", "load", "library_path", "zipccl_format_version", "zipccl_status_string",
     "zipccl_max_compressed_bytes", "zipccl_compress_workspace_bytes", "zipccl_decompress_workspace_bytes",
     "zipccl_reduce_workspace_bytes", "zipccl_compress", "zipccl_decompress", "zipccl_decompress_reduce",
-    "zipccl_get_device_status", "zipccl_codebook_phase", "zipccl_decompress_reduce_noalloc",
+    "zipccl_get_device_status", "zipccl_codebook_phase", "zipccl_codebook_rebuild_phase",
+    "zipccl_decompress_reduce_noalloc",
     "zipccl_predict_chunk_bytes", "zipccl_choose_compressed", "zipccl_selftest_bounded_wait", "compress", "decompress", "decompress_reduce",
     "Compressed", "EXPORTED_SYMBOLS",
 ]
@@ -37,7 +38,8 @@ EXPORTED_SYMBOLS = [
     "zipccl_format_version", "zipccl_status_string", "zipccl_max_compressed_bytes",
     "zipccl_compress_workspace_bytes", "zipccl_decompress_workspace_bytes", "zipccl_reduce_workspace_bytes",
     "zipccl_compress", "zipccl_decompress", "zipccl_decompress_reduce", "zipccl_get_device_status",
-    "zipccl_codebook_phase", "zipccl_decompress_reduce_noalloc", "zipccl_predict_chunk_bytes",
+    "zipccl_codebook_phase", "zipccl_codebook_rebuild_phase", "zipccl_decompress_reduce_noalloc",
+    "zipccl_predict_chunk_bytes",
     "zipccl_choose_compressed", "zipccl_selftest_bounded_wait",
 ]
 
@@ -99,8 +101,10 @@ def load(build_if_missing: bool = True):
         L.zipccl_decompress_reduce_noalloc.restype = ctypes.c_int
         L.zipccl_decompress_reduce_noalloc.argtypes = [ctypes.POINTER(vp), u64p, u32, u64, vp,
                                                        ctypes.POINTER(vp), vp]
-        L.zipccl_codebook_phase.restype = ctypes.c_int
-        L.zipccl_codebook_phase.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_uint8)]
+        for name in ("zipccl_codebook_phase", "zipccl_codebook_rebuild_phase"):
+            f = getattr(L, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_uint8)]
         dbl = ctypes.c_double
         L.zipccl_predict_chunk_bytes.restype = ctypes.c_int
         L.zipccl_predict_chunk_bytes.argtypes = [u64, ctypes.c_float, u64p, ctypes.POINTER(dbl)]
@@ -207,6 +211,14 @@ def zipccl_codebook_phase(phase: int) -> tuple[int, list[int]]:
     off = ctypes.c_int()
     lens = (ctypes.c_uint8 * 16)()
     _check(load().zipccl_codebook_phase(int(phase), ctypes.byref(off), lens), "zipccl_codebook_phase")
+    return off.value, list(lens)
+
+
+def zipccl_codebook_rebuild_phase(phase: int) -> tuple[int, list[int]]:
+    """The phase table derived again from the closed form (for checking the frozen one)."""
+    off = ctypes.c_int()
+    lens = (ctypes.c_uint8 * 16)()
+    _check(load().zipccl_codebook_rebuild_phase(int(phase), ctypes.byref(off), lens), "zipccl_codebook_rebuild_phase")
     return off.value, list(lens)
 
 

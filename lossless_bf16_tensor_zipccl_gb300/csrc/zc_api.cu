@@ -330,4 +330,13 @@ zipccl_status zipccl_codebook_phase(int phase, int* base_offset, uint8_t* lens16
   return ZIPCCL_OK;
 }
 
+zipccl_status zipccl_codebook_rebuild_phase(int phase, int* base_offset, uint8_t* lens16) {
+  if (phase < 0 || phase > 15 || !base_offset || !lens16) return ZIPCCL_ERR_INVALID_ARG;
+  PhaseTable t;
+  rebuild_phase_table(phase, &t);
+  *base_offset = t.base_offset;
+  for (int s = 0; s < kNsym; ++s) lens16[s] = t.lens[s];
+  return ZIPCCL_OK;
+}
+
 }  // extern "C"

@@ -5,6 +5,10 @@
 // summary's key design: the exponent code comes from the Gaussian density, so
 // frequent exponents get short codewords and no histogram is taken online.
 //
+// The tables the library codes with are the frozen integers of format v1
+// (zc_format.h); rebuild_phase_table derives them again from the closed form,
+// for the tests that check the frozen copy.
+//
 // For X ~ N(0, sigma^2) the biased BF16 exponent e has
 //   P(e) = P(2^(e-127) <= |X| < 2^(e-126)),  1 <= e <= 254,
 //   P(0) = P(|X| < 2^-126).
@@ -78,39 +82,46 @@ void optimal_limited_lengths(const double* w, int n, int lmax, uint8_t* lens) {
 PhaseTable g_tables[16];
 std::once_flag g_once;
 
-void build_all() {
+// The frozen tables of format v1 (zc_format.h), unpacked once.
+void load_frozen() {
   for (int r = 0; r < 16; ++r) {
-    double p[256];
-    exponent_masses(pow(2.0, r / 16.0), p);
-    int best = 0;
-    double best_mass = -1.0;
-    for (int b = 0; b + kWindow <= 255; ++b) {
-      double m = 0.0;
-      for (int i = 0; i < kWindow; ++i) m += p[b + i];
-      if (m > best_mass) {
-        best_mass = m;
-        best = b;
-      }
-    }
-    double w[kNsym];
-    double in_window = 0.0;
-    for (int i = 0; i < kWindow; ++i) {
-      w[i] = p[best + i];
-      in_window += w[i];
-    }
-    w[kEsc] = 1.0 - in_window;
-    g_tables[r].base_offset = best - 127;
-    optimal_limited_lengths(w, kNsym, kLmax, g_tables[r].lens);
-    uint64_t packed = 0;
-    for (int s = 0; s < kNsym; ++s) packed |= (uint64_t)g_tables[r].lens[s] << (4 * s);
-    g_tables[r].lens_packed = packed;
+    g_tables[r].base_offset = kPhaseBaseOffset[r];
+    g_tables[r].lens_packed = kPhaseLens[r];
+    for (int s = 0; s < kNsym; ++s) g_tables[r].lens[s] = (uint8_t)((kPhaseLens[r] >> (4 * s)) & 15);
   }
 }
 
 }  // namespace
 
+void rebuild_phase_table(int r, PhaseTable* out) {
+  double p[256];
+  exponent_masses(pow(2.0, r / 16.0), p);
+  int best = 0;
+  double best_mass = -1.0;
+  for (int b = 0; b + kWindow <= 255; ++b) {
+    double m = 0.0;
+    for (int i = 0; i < kWindow; ++i) m += p[b + i];
+    if (m > best_mass) {
+      best_mass = m;
+      best = b;
+    }
+  }
+  double w[kNsym];
+  double in_window = 0.0;
+  for (int i = 0; i < kWindow; ++i) {
+    w[i] = p[best + i];
+    in_window += w[i];
+  }
+  w[kEsc] = 1.0 - in_window;
+  out->base_offset = best - 127;
+  optimal_limited_lengths(w, kNsym, kLmax, out->lens);
+  uint64_t packed = 0;
+  for (int s = 0; s < kNsym; ++s) packed |= (uint64_t)out->lens[s] << (4 * s);
+  out->lens_packed = packed;
+}
+
 const PhaseTable* phase_tables() {
-  std::call_once(g_once, build_all);
+  std::call_once(g_once, load_frozen);
   return g_tables;
 }
 

@@ -10,8 +10,13 @@ struct PhaseTable {
   uint64_t lens_packed; // lens[s] at bits 4s..4s+3
 };
 
-// The 16 phase tables, built on first use (thread-safe).
+// The 16 phase tables of format v1 (the frozen integers, unpacked on first
+// use; thread-safe).
 const PhaseTable* phase_tables();
+
+// Phase r rebuilt from the closed-form masses by the exact dynamic program
+// (double precision, libm erf/erfc): for checking the frozen tables.
+void rebuild_phase_table(int r, PhaseTable* out);
 
 // Window start for scale q: floor(q/16) + 127 + the phase's offset, clamped
 // to [0, 240] so that the window stays inside [0, 254].

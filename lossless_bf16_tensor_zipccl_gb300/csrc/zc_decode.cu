@@ -483,10 +483,13 @@ __global__ void __launch_bounds__(256) zc_rprep_kernel(ReduceArgs a) {
     }
     return;
   }
-  // peers with the same code lengths share the first such peer's table
+  // Peers with the same code lengths share the first such peer's table.  The
+  // owner's header is validated here too, so that a table is only ever
+  // shared with a peer whose own block builds it.
   uint32_t owner = p;
   for (uint32_t j = 0; j < p; ++j) {
-    if (a.bytes[j] >= kChunkHdr && ld_u64(a.peers[j] + 24) == h.lens) {
+    HeaderInfo hj;
+    if (check_header(a.peers[j], a.bytes[j], hj) == 0 && hj.n == a.n && hj.lens == h.lens) {
       owner = j;
       break;
     }

@@ -61,6 +61,22 @@ __host__ __device__ constexpr inline uint64_t chunk_hdr_bytes(uint64_t n_tiles) 
   return kChunkHdr + pad16(4 * n_tiles);
 }
 
+// Code tables of format v1, frozen: for scale phase r = q mod 16, the window
+// start relative to floor(q/16) + 127 and the 16 code lengths (symbol s at
+// bits 4s..4s+3; symbols 0..14 are the window exponents, 15 the escape).
+// They are the optimal 10-bit-limited prefix code over the closed-form
+// Gaussian exponent masses at sigma = 2^(r/16) (window: the 15 consecutive
+// exponents of largest mass).  The host builder in zc_codebook.cpp
+// regenerates them for the tests; the library itself uses only these
+// integers, so its streams do not depend on the host's erf.
+constexpr int kPhaseBaseOffset[16] = {-13, -12, -12, -12, -12, -12, -12, -12,
+                                      -12, -12, -12, -12, -12, -12, -12, -12};
+constexpr uint64_t kPhaseLens[16] = {
+    0xa5222355679aaaaaull, 0xaa4222445679aaaaull, 0xaa4222445679aaaaull, 0xaa4222445679aaaaull,
+    0xaa3223345679aaaaull, 0xa932233456889aaaull, 0xa932233456889aaaull, 0xa832233456899aaaull,
+    0xa8222345689aaaaaull, 0xa8222345689aaaaaull, 0xa7222345779aaaaaull, 0xa7222345779aaaaaull,
+    0xa6222346679aaaaaull, 0xa6222346679aaaaaull, 0xa5222355679aaaaaull, 0xa5222355679aaaaaull};
+
 // Look-back state word: 2-bit flag | 62-bit byte count.
 constexpr uint64_t kFlagShift = 62;
 constexpr uint64_t kFlagAgg = 1ull << kFlagShift;

@@ -46,7 +46,9 @@ LMAX = 10
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc into oracle/_build (plain -O2, no fast-math)."""
     os.makedirs(_BUILD, exist_ok=True)
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+    deps = [_SRC, os.path.join(_HERE, "zo_frozen_tables.h")]
+    if force or not os.path.exists(_LIB_PATH) or any(
+            os.path.exists(d) and os.path.getmtime(_LIB_PATH) < os.path.getmtime(d) for d in deps):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.check_call(
             ["gcc", "-O2", "-std=c99", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared",
@@ -70,6 +72,9 @@ def lib():
             L.zo_package_merge.restype = ctypes.c_int
             L.zo_phase_table.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
             L.zo_phase_table.restype = None
+            L.zo_frozen_phase_table.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                                ctypes.POINTER(ctypes.c_int)]
+            L.zo_frozen_phase_table.restype = None
             L.zo_select_q.argtypes = [ctypes.c_void_p, ctypes.c_uint64]
             L.zo_select_q.restype = ctypes.c_int
             L.zo_q_from_sigma.argtypes = [ctypes.c_double]
@@ -134,11 +139,29 @@ def package_merge(weights, limit: int) -> list[int]:
     return list(lens)
 
 
-def phase_table(r: int) -> tuple[int, list[int]]:
-    """(window start - 127, code lengths of symbols 0..15) for phase r = q mod 16."""
+def rebuilt_phase_table(r: int) -> tuple[int, list[int]]:
+    """Phase r = q mod 16 rebuilt from the closed form: (window start - 127,
+    code lengths of symbols 0..15), by the oracle's package-merge."""
     off = ctypes.c_int()
     lens = (ctypes.c_int * NSYM)()
     lib().zo_phase_table(int(r), ctypes.byref(off), lens)
+    return off.value, list(lens)
+
+
+def rebuilt_phase_tables() -> tuple[list[int], list[list[int]]]:
+    offs, lens = [], []
+    for r in range(16):
+        o, l = rebuilt_phase_table(r)
+        offs.append(o)
+        lens.append(l)
+    return offs, lens
+
+
+def phase_table(r: int) -> tuple[int, list[int]]:
+    """The frozen table of format v1 that the oracle's encoder uses for phase r."""
+    off = ctypes.c_int()
+    lens = (ctypes.c_int * NSYM)()
+    lib().zo_frozen_phase_table(int(r), ctypes.byref(off), lens)
     return off.value, list(lens)
 
 

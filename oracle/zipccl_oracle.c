@@ -41,6 +41,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include "zo_frozen_tables.h"
 
 #define ZO_MAGIC 0x4C43435Au
 #define ZO_VERSION 1
@@ -192,6 +193,19 @@ void zo_phase_table(int r, int *base_off, int *lens)
     w[ZO_ESC] = 1.0 - sum;
     *base_off = bb - 127;
     zo_package_merge(w, ZO_NSYM, ZO_LMAX, lens);
+}
+
+/*
+ * The table of phase r as stream format v1 freezes it (zo_frozen_tables.h,
+ * written from zo_phase_table by freeze_tables.py).  The encoder and the
+ * predictor use this copy, so streams do not depend on the host's erf.
+ */
+void zo_frozen_phase_table(int r, int *base_off, int *lens)
+{
+    int i;
+    *base_off = zo_frozen_base_off[r];
+    for (i = 0; i < ZO_NSYM; i++)
+        lens[i] = zo_frozen_lens[r][i];
 }
 
 /* ------------------------------------------------------------------------ */
@@ -396,9 +410,9 @@ double zo_expected_exponent_bits(double sigma, int q)
     double p[256], bits = 0.0;
     int offs[16], lens_r[ZO_NSYM], r, e, base, k;
     for (r = 0; r < 16; r++)
-        zo_phase_table(r, &offs[r], lens_r);
+        zo_frozen_phase_table(r, &offs[r], lens_r);
     k = (int)floor_div(q, 16);
-    zo_phase_table(q - 16 * k, &offs[q - 16 * k], lens_r);
+    zo_frozen_phase_table(q - 16 * k, &offs[q - 16 * k], lens_r);
     base = zo_base_for_q(q, offs);
     zo_exponent_pmf(sigma, p);
     for (e = 0; e < 256; e++) {
@@ -513,7 +527,7 @@ int zo_compress(const uint16_t *in, uint64_t n, const uint64_t *chunk_elems, uin
     if (cap < zo_max_compressed_bytes(chunk_elems, n_chunks))
         return ZO_ERR_CAPACITY;
     for (r = 0; r < 16; r++)
-        zo_phase_table(r, &base_off[r], lens_tab[r]);
+        zo_frozen_phase_table(r, &base_off[r], lens_tab[r]);
 
     for (c = 0; c < n_chunks; c++) {
         uint64_t nc = chunk_elems[c], T = n_tiles_of(nc), t, tpos;

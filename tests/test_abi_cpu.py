@@ -39,12 +39,25 @@ def test_format_version_and_status_strings():
 
 
 def test_codebook_tables_match_oracle():
+    # the frozen tables of format v1: the library's copy equals the oracle's copy
     offs, lens = oracle.phase_tables()
     for r in range(16):
         o, l = zc.zipccl_codebook_phase(r)
         assert o == offs[r] and l == lens[r], r
     with pytest.raises(zc.ZipcclError):
         zc.zipccl_codebook_phase(16)
+
+
+def test_frozen_tables_equal_their_derivation():
+    # each side's frozen copy still equals what its own builder derives from the
+    # closed form: the library's exact dynamic program, the oracle's package-merge
+    roffs, rlens = oracle.rebuilt_phase_tables()
+    offs, lens = oracle.phase_tables()
+    assert (roffs, rlens) == (offs, lens)
+    for r in range(16):
+        assert zc.zipccl_codebook_rebuild_phase(r) == zc.zipccl_codebook_phase(r), r
+    with pytest.raises(zc.ZipcclError):
+        zc.zipccl_codebook_rebuild_phase(-1)
 
 
 @pytest.mark.parametrize("chunks", [[1], [0], [0, 5, 0], [32768], [32769, 1, 65536], [1 << 20] * 3,
