@@ -11,7 +11,8 @@ Metric: GB/s of uncompressed BF16 through the step (2 bytes per value
 compressed + 2 per value decompressed + 2 per peer value reduced) per second
 of device time; the per-stage rates, the compression ratio and the dominant
 kernel's fraction of the measured HBM bandwidth ride along.  Inputs are
-resident in HBM when timing starts; L2 is flushed before every timed step.
+resident in HBM when timing starts; L2 is flushed before every timed step
+(a buffer twice its size written, then another read).
 ``e2e`` times the same step through the public API with pinned host buffers
 and the host<->device copies inside the timed region.
 
@@ -83,8 +84,28 @@ def workload_config(n_gpus: int) -> dict:
                     "(compress + decompress) + decompress_reduce of 8 peer chunks x 8,388,608 (fp32 sum, rank order)",
         "n_elems": N_BUCKET, "chunks": RANKS, "reduce_peers": K_PEERS, "reduce_elems": PEER_N,
         "parallelism": f"replicas x{n_gpus} (independent buckets, no collective)",
-        "l2": "flushed before every timed step (256 MiB write)",
+        "l2": L2_NOTE,
     }
+
+
+class L2Flush:
+    """Untimed, before each timed call: write a buffer twice the L2's size, then read
+    another of the same size.  The L2 then holds none of the call's data, and the
+    written lines are already back in HBM, so the timed call does not pay for
+    writing back the flush's own dirty lines."""
+
+    def __init__(self, torch, dev):
+        self.torch = torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+        self.sink = torch.empty(1, dtype=torch.int64, device=dev)
+
+    def __call__(self, i: int = 0) -> None:
+        self.w.fill_(i & 0xFF)
+        self.torch.sum(self.r, dim=0, keepdim=True, out=self.sink)
+
+
+L2_NOTE = "flushed before every timed call: 258 MiB written, then 258 MiB read (no dirty lines left)"
 
 
 def peaks() -> dict:
@@ -324,7 +345,7 @@ def run_ours(args, rank: int, world: int):
     ws_r = torch.empty(zc.zipccl_reduce_workspace_bytes(K_PEERS), dtype=torch.uint8, device=dev)
     dec = torch.empty(N_BUCKET, dtype=torch.int16, device=dev)
     red = torch.empty(PEER_N, dtype=torch.int16, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
 
     def check(st, what):
         if st != zc.OK:
@@ -362,7 +383,7 @@ def run_ours(args, rank: int, world: int):
     with ClockSampler(dev.index) as clk:
         n0 = clk.lines()
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)          # untimed: L2 flush
+            flush(i)                       # untimed: L2 flush
             ev[i][0].record(stream)
             for j, (_, f) in enumerate(stages):
                 f()
@@ -371,7 +392,7 @@ def run_ours(args, rank: int, world: int):
 
         def more_steps():  # untimed, the same work: the clock record brackets the timed region under load
             for _ in range(50):
-                flush.fill_(0)
+                flush(0)
                 for _, f in stages:
                     f()
             torch.cuda.synchronize(dev)
@@ -420,6 +441,8 @@ def run_ours(args, rank: int, world: int):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        line["send_pipeline"] = measure_send_overlap(args, zc, torch, dev, wl)
     names = [c for c in args.configs.split(",") if c and c != "none"]
     if rank == 0 and names:
         line["configs"] = measure_configs(args, zc, torch, dev, pk, names, cpu=world == 1 and not args.no_cpu_baseline,
@@ -502,7 +525,7 @@ def measure_configs(args, zc, torch, dev, pk, names, cpu: bool, gradient_wl=None
     and the gap to the entropy bound."""
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     res = {}
     for name in names:
         wl = config_workload(name, gradient_wl)
@@ -540,11 +563,11 @@ def measure_configs(args, zc, torch, dev, pk, names, cpu: bool, gradient_wl=None
         comp_bytes = int(offs[-1].item())
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush(i)
             ev[i][0].record(stream)
             comp()
             ev[i][1].record(stream)
-            flush.fill_((i + 1) & 0xFF)
+            flush(i + 1)
             ev[i][2].record(stream)
             decomp()
             ev[i][3].record(stream)
@@ -563,7 +586,7 @@ def measure_configs(args, zc, torch, dev, pk, names, cpu: bool, gradient_wl=None
             "compressed_bytes": comp_bytes, "bits_per_value": bits, "compression_ratio": comp_bytes / max(1, 2 * n),
             "empirical_bound_bits": emp, "gap_to_empirical_bound": bits / emp - 1.0,
             "round_trip": "bit-exact",
-            "l2": "flushed before every call" + (" (input smaller than L2)" if 2 * n < (129 << 20) else ""),
+            "l2": L2_NOTE + ("; the input is smaller than L2" if 2 * n < (129 << 20) else ""),
         }
         if name in CONFIG_SIGMA:
             hb = 8.0 + gaussian_exponent_entropy(CONFIG_SIGMA[name])
@@ -582,6 +605,79 @@ def measure_configs(args, zc, torch, dev, pk, names, cpu: bool, gradient_wl=None
         del x, out, offs, ws_c, ws_d, dec
         torch.cuda.empty_cache()
     return res
+
+
+def measure_send_overlap(args, zc, torch, dev, wl) -> dict:
+    """Compress-and-send on the gradient bucket: the fused call (every tile stored to the
+    output and to a send buffer from shared memory, each chunk posted as soon as its tiles
+    are stored) against the compress call followed by a device-to-device copy of the whole
+    stream into the send buffer.  Median CUDA-event times over the timed steps, L2 flushed
+    before each; plus, from one more call, when each chunk was posted after the kernel began."""
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    ce = wl.chunk_elems
+    x = torch.from_numpy(wl.x.view(np.int16)).to(dev)
+    cap = zc.zipccl_max_compressed_bytes(ce)
+    out = torch.empty(cap, dtype=torch.uint8, device=dev)
+    send = torch.empty(cap, dtype=torch.uint8, device=dev)
+    offs = torch.empty(len(ce) + 1, dtype=torch.int64, device=dev)
+    ws = torch.empty(zc.zipccl_compress_workspace_bytes(ce), dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
+
+    def comp():
+        st = zc.zipccl_compress(x.data_ptr(), x.numel(), ce, None, out.data_ptr(), cap, offs.data_ptr(),
+                                ws.data_ptr(), ws.numel(), sp)
+        if st != zc.OK:
+            raise zc.ZipcclError(st, "compress")
+
+    ready = torch.zeros(len(ce) + 1, dtype=torch.int64, device=dev)
+
+    def comp_send():
+        st = zc.zipccl_compress_send(x.data_ptr(), x.numel(), ce, None, out.data_ptr(), cap, offs.data_ptr(),
+                                     send.data_ptr(), cap, ready.data_ptr(), ws.data_ptr(), ws.numel(), sp)
+        if st != zc.OK:
+            raise zc.ZipcclError(st, "compress_send")
+
+    comp()
+    torch.cuda.synchronize(dev)
+    total = int(offs[-1].item())
+
+    def copy():
+        send[:total].copy_(out[:total])
+
+    variants = {"compress_then_copy": lambda: (comp(), copy()), "compress_send": comp_send, "copy_alone": copy}
+    for _ in range(max(3, args.warmup)):
+        for f in variants.values():
+            f()
+    torch.cuda.synchronize(dev)
+    if zc.zipccl_get_device_status(ws.data_ptr(), sp) != zc.OK:
+        raise RuntimeError("compress_send: device status")
+    send.zero_()
+    flush(0)
+    comp_send()
+    torch.cuda.synchronize(dev)
+    if not torch.equal(send[:total], out[:total]):
+        raise RuntimeError("compress_send: the send buffer differs from the stream")
+    r = ready.cpu().numpy()
+    posted_us = [round((int(v) - int(r[-1])) / 1e3, 2) for v in r[:-1]]
+    times = {k: [] for k in variants}
+    for i in range(args.steps):
+        for k, f in variants.items():
+            flush(i)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            f()
+            e1.record(stream)
+            times[k].append((e0, e1))
+    torch.cuda.synchronize(dev)
+    med = {k: statistics.median(a.elapsed_time(b) for a, b in v) * 1e3 for k, v in times.items()}
+    return {"workload": "gradient bucket, 8 chunks", "stream_bytes": total,
+            "compress_then_copy_us": med["compress_then_copy"], "compress_send_us": med["compress_send"],
+            "copy_alone_us": med["copy_alone"],
+            "saved_us": med["compress_then_copy"] - med["compress_send"],
+            "copy_hidden_fraction": (med["compress_then_copy"] - med["compress_send"]) / med["copy_alone"],
+            "chunk_posted_us_after_kernel_start": posted_us,
+            "l2": L2_NOTE}
 
 
 def all_patterns_round_trip(zc, torch, dev) -> str:

@@ -110,6 +110,37 @@ zipccl_status zipccl_compress(const uint16_t *d_in, uint64_t n, const uint64_t *
                               uint64_t ws_bytes, void *stream);
 
 /*
+ * Passages: abstract (the compressor and decompressor kernels overlap
+ * compression with memory access through a pipeline); Fig. 5 caption
+ * (minimize kernel launch overhead, overlap compression with memory access);
+ * abstract, technique (2) (communication-aware layout: one chunk per
+ * destination rank).
+ * zipccl_compress that also writes every chunk into d_send, the buffer a
+ * transport would send from, and posts each chunk as soon as it is complete
+ * while later chunks are still being coded.  In the same kernel: each tile's
+ * image leaves shared memory by two TMA stores, one to d_out and one to the
+ * same offset in d_send (the send costs HBM writes, no reads); the store
+ * warps count the stored tiles of each chunk (release at GPU scope); one
+ * warp in the first CTA, the stand-in for the proxy that hands chunks to
+ * the network, waits for each chunk's count in chunk order (acquire, bounded
+ * by 2 s) and posts it: it writes %globaltimer into d_chunk_ready[c].
+ * d_chunk_ready[n_chunks] receives the kernel's start on the same clock.
+ * The exchange itself is outside this library.
+ *   d_send: device, 16-byte aligned, not d_out, send_capacity >=
+ *     zipccl_max_compressed_bytes; afterwards d_send[0, offsets[n_chunks])
+ *     equals d_out over the same range.
+ *   d_chunk_ready: device, n_chunks + 1 uint64, 8-byte aligned, or NULL.
+ * A wait that gives up records ZIPCCL_ERR_TIMEOUT; an error of the coding
+ * warps ends the posting; read either with zipccl_get_device_status.  Other
+ * arguments as zipccl_compress.
+ */
+zipccl_status zipccl_compress_send(const uint16_t *d_in, uint64_t n, const uint64_t *chunk_elems,
+                                   uint32_t n_chunks, const float *sigma_hint, void *d_out,
+                                   uint64_t out_capacity, uint64_t *d_chunk_offsets, void *d_send,
+                                   uint64_t send_capacity, uint64_t *d_chunk_ready, void *d_ws,
+                                   uint64_t ws_bytes, void *stream);
+
+/*
  * Passages: Fig. 6 caption (the decompressor restores each value from its
  * raw sign/mantissa byte and its decoded exponent); pith summary (lossless:
  * every byte restored).
@@ -191,10 +222,12 @@ zipccl_status zipccl_get_device_status(const void *d_ws, void *stream);
  * Self-test of the bounded device waits: which = 0 runs the compressor's
  * look-back for a tile whose predecessor never publishes its state; which =
  * 1 waits for an mbarrier phase that never completes (the wait used for the
- * decoders' payload copies).  The wait gives up after its limit (2 s) and
- * the kernel records ZIPCCL_ERR_TIMEOUT in the workspace status, read with
- * zipccl_get_device_status; nothing faults and the context stays usable.
- * d_ws: at least 272 bytes, 256-byte aligned.  Asynchronous on `stream`.
+ * decoders' payload copies); which = 2 runs the compress-and-send sender's
+ * wait for a chunk whose tiles are never stored (no encoder runs).  The wait
+ * gives up after its limit (2 s) and the kernel records ZIPCCL_ERR_TIMEOUT
+ * in the workspace status, read with zipccl_get_device_status; nothing
+ * faults and the context stays usable.  d_ws: 256-byte aligned, at least
+ * 272 bytes (which 0, 1) or 336 bytes (which 2).  Asynchronous on `stream`.
  */
 zipccl_status zipccl_selftest_bounded_wait(int which, void *d_ws, uint64_t ws_bytes, void *stream);
 

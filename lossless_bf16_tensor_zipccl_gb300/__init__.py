@@ -26,7 +26,8 @@ from . import build as _build
 __all__ = [
     "ZipcclError", "load", "library_path", "zipccl_format_version", "zipccl_status_string",
     "zipccl_max_compressed_bytes", "zipccl_compress_workspace_bytes", "zipccl_decompress_workspace_bytes",
-    "zipccl_reduce_workspace_bytes", "zipccl_compress", "zipccl_decompress", "zipccl_decompress_reduce",
+    "zipccl_reduce_workspace_bytes", "zipccl_compress", "zipccl_compress_send", "zipccl_decompress",
+    "zipccl_decompress_reduce",
     "zipccl_get_device_status", "zipccl_codebook_phase", "zipccl_codebook_rebuild_phase",
     "zipccl_decompress_reduce_noalloc",
     "zipccl_predict_chunk_bytes", "zipccl_choose_compressed", "zipccl_selftest_bounded_wait", "compress", "decompress", "decompress_reduce",
@@ -37,8 +38,9 @@ OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_CORRUPT, ERR_VERSION, ERR_TIMEOUT, ERR_CU
 EXPORTED_SYMBOLS = [
     "zipccl_format_version", "zipccl_status_string", "zipccl_max_compressed_bytes",
     "zipccl_compress_workspace_bytes", "zipccl_decompress_workspace_bytes", "zipccl_reduce_workspace_bytes",
-    "zipccl_compress", "zipccl_decompress", "zipccl_decompress_reduce", "zipccl_get_device_status",
-    "zipccl_codebook_phase", "zipccl_codebook_rebuild_phase", "zipccl_decompress_reduce_noalloc",
+    "zipccl_compress", "zipccl_compress_send", "zipccl_decompress", "zipccl_decompress_reduce",
+    "zipccl_get_device_status", "zipccl_codebook_phase", "zipccl_codebook_rebuild_phase",
+    "zipccl_decompress_reduce_noalloc",
     "zipccl_predict_chunk_bytes",
     "zipccl_choose_compressed", "zipccl_selftest_bounded_wait",
 ]
@@ -92,6 +94,9 @@ def load(build_if_missing: bool = True):
         L.zipccl_reduce_workspace_bytes.argtypes = [u32, u64p]
         L.zipccl_compress.restype = ctypes.c_int
         L.zipccl_compress.argtypes = [vp, u64, u64p, u32, ctypes.POINTER(ctypes.c_float), vp, u64, vp, vp, u64, vp]
+        L.zipccl_compress_send.restype = ctypes.c_int
+        L.zipccl_compress_send.argtypes = [vp, u64, u64p, u32, ctypes.POINTER(ctypes.c_float), vp, u64, vp, vp, u64,
+                                           vp, vp, u64, vp]
         L.zipccl_decompress.restype = ctypes.c_int
         L.zipccl_decompress.argtypes = [vp, vp, u32, vp, u64, vp, u64, vp]
         L.zipccl_decompress_reduce.restype = ctypes.c_int
@@ -170,6 +175,17 @@ def zipccl_compress(d_in: int, n: int, chunk_elems, sigma_hint, d_out: int, out_
         hint = (ctypes.c_float * len(sigma_hint))(*[float(v) for v in sigma_hint])
     return int(load().zipccl_compress(d_in, n, _u64_array(chunk_elems), len(chunk_elems), hint, d_out,
                                       out_capacity, d_chunk_offsets, d_ws, ws_bytes, stream))
+
+
+def zipccl_compress_send(d_in: int, n: int, chunk_elems, sigma_hint, d_out: int, out_capacity: int,
+                         d_chunk_offsets: int, d_send: int, send_capacity: int, d_chunk_ready: int, d_ws: int,
+                         ws_bytes: int, stream: int) -> int:
+    hint = None
+    if sigma_hint is not None:
+        hint = (ctypes.c_float * len(sigma_hint))(*[float(v) for v in sigma_hint])
+    return int(load().zipccl_compress_send(d_in, n, _u64_array(chunk_elems), len(chunk_elems), hint, d_out,
+                                           out_capacity, d_chunk_offsets, d_send, send_capacity, d_chunk_ready,
+                                           d_ws, ws_bytes, stream))
 
 
 def zipccl_decompress(d_stream: int, d_chunk_offsets: int, n_chunks: int, d_out: int, n: int, d_ws: int,
@@ -310,8 +326,13 @@ def _keep(t, stream):
     return t
 
 
-def compress(x, chunk_elems=None, sigma_hint=None, out=None, offsets=None, ws=None, stream=None) -> Compressed:
-    """Compress a BF16 CUDA tensor into per-chunk self-contained streams."""
+def compress(x, chunk_elems=None, sigma_hint=None, out=None, offsets=None, ws=None, stream=None,
+             send=None, ready=None) -> Compressed:
+    """Compress a BF16 CUDA tensor into per-chunk self-contained streams.  With
+    ``send`` (a uint8 CUDA tensor of at least the worst-case size), the same
+    kernel writes every chunk there too and posts each one as it completes;
+    ``ready`` (int64 CUDA tensor of n_chunks + 1, optional) receives the post
+    times (see zipccl_compress_send)."""
     torch = _torch()
     w = _words(x)
     n = w.numel()
@@ -323,9 +344,16 @@ def compress(x, chunk_elems=None, sigma_hint=None, out=None, offsets=None, ws=No
         offsets = _keep(torch.empty(len(chunk_elems) + 1, dtype=torch.int64, device=w.device), stream)
     wsb = zipccl_compress_workspace_bytes(chunk_elems)
     ws = _ws(wsb, w.device, ws, stream)
-    st = zipccl_compress(w.data_ptr(), n, chunk_elems, sigma_hint, out.data_ptr(), out.numel(),
-                         offsets.data_ptr(), ws.data_ptr(), ws.numel(), _stream_ptr(stream))
-    _check(st, "zipccl_compress")
+    if send is None:
+        st = zipccl_compress(w.data_ptr(), n, chunk_elems, sigma_hint, out.data_ptr(), out.numel(),
+                             offsets.data_ptr(), ws.data_ptr(), ws.numel(), _stream_ptr(stream))
+        _check(st, "zipccl_compress")
+    else:
+        st = zipccl_compress_send(w.data_ptr(), n, chunk_elems, sigma_hint, out.data_ptr(), out.numel(),
+                                  offsets.data_ptr(), send.data_ptr(), send.numel(),
+                                  0 if ready is None else ready.data_ptr(), ws.data_ptr(), ws.numel(),
+                                  _stream_ptr(stream))
+        _check(st, "zipccl_compress_send")
     return Compressed(out, offsets, n, chunk_elems)
 
 

@@ -128,10 +128,19 @@ zipccl_status zipccl_reduce_workspace_bytes(uint32_t k, uint64_t* out_bytes) {
   return ZIPCCL_OK;
 }
 
-zipccl_status zipccl_compress(const uint16_t* d_in, uint64_t n, const uint64_t* chunk_elems, uint32_t n_chunks,
-                              const float* sigma_hint, void* d_out, uint64_t out_capacity,
-                              uint64_t* d_chunk_offsets, void* d_ws, uint64_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// zipccl_compress and zipccl_compress_send: the same kernels; with a send
+// buffer the encoder also runs its sender warps.
+zipccl_status compress_impl(const uint16_t* d_in, uint64_t n, const uint64_t* chunk_elems, uint32_t n_chunks,
+                            const float* sigma_hint, void* d_out, uint64_t out_capacity, uint64_t* d_chunk_offsets,
+                            void* d_send, uint64_t send_capacity, uint64_t* d_chunk_ready, void* d_ws,
+                            uint64_t ws_bytes, void* stream) {
   if (!chunk_elems || n_chunks == 0 || !d_out || !d_chunk_offsets || !d_ws) return ZIPCCL_ERR_INVALID_ARG;
+  if (d_send && (!aligned(d_send, 16) || d_send == d_out)) return ZIPCCL_ERR_INVALID_ARG;
+  if (d_chunk_ready && !aligned(d_chunk_ready, 8)) return ZIPCCL_ERR_INVALID_ARG;
   if ((n > 0 && !d_in) || !aligned(d_in, 16) || !aligned(d_out, 16) || !aligned(d_chunk_offsets, 8) ||
       !aligned(d_ws, 256))
     return ZIPCCL_ERR_INVALID_ARG;
@@ -145,7 +154,7 @@ zipccl_status zipccl_compress(const uint16_t* d_in, uint64_t n, const uint64_t* 
   if (sum != n) return ZIPCCL_ERR_INVALID_ARG;
   const EncLayout L = enc_layout(chunk_elems, n_chunks);
   if (L.n_items >= (1ull << 31)) return ZIPCCL_ERR_INVALID_ARG;
-  if (out_capacity < bound || ws_bytes < L.total) return ZIPCCL_ERR_CAPACITY;
+  if (out_capacity < bound || ws_bytes < L.total || (d_send && send_capacity < bound)) return ZIPCCL_ERR_CAPACITY;
 
   const PhaseTable* tabs = phase_tables();
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
@@ -193,6 +202,9 @@ zipccl_status zipccl_compress(const uint16_t* d_in, uint64_t n, const uint64_t* 
   ea.in = d_in;
   ea.out = static_cast<uint8_t*>(d_out);
   ea.cap = out_capacity;
+  ea.send = static_cast<uint8_t*>(d_send);
+  ea.send_cap = d_send ? send_capacity : 0;
+  ea.ready = d_send ? d_chunk_ready : nullptr;
   ea.offsets = d_chunk_offsets;
   ea.chunks = sa->chunks;
   ea.tables = sa->tables;
@@ -202,6 +214,26 @@ zipccl_status zipccl_compress(const uint16_t* d_in, uint64_t n, const uint64_t* 
   ea.n_chunks = n_chunks;
   ea.n_items = (uint32_t)L.n_items;
   return cuda_status(launch_encode(ea, (uint32_t)L.n_items, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+zipccl_status zipccl_compress(const uint16_t* d_in, uint64_t n, const uint64_t* chunk_elems, uint32_t n_chunks,
+                              const float* sigma_hint, void* d_out, uint64_t out_capacity,
+                              uint64_t* d_chunk_offsets, void* d_ws, uint64_t ws_bytes, void* stream) {
+  return compress_impl(d_in, n, chunk_elems, n_chunks, sigma_hint, d_out, out_capacity, d_chunk_offsets, nullptr, 0,
+                       nullptr, d_ws, ws_bytes, stream);
+}
+
+zipccl_status zipccl_compress_send(const uint16_t* d_in, uint64_t n, const uint64_t* chunk_elems, uint32_t n_chunks,
+                                   const float* sigma_hint, void* d_out, uint64_t out_capacity,
+                                   uint64_t* d_chunk_offsets, void* d_send, uint64_t send_capacity,
+                                   uint64_t* d_chunk_ready, void* d_ws, uint64_t ws_bytes, void* stream) {
+  if (!d_send) return ZIPCCL_ERR_INVALID_ARG;
+  return compress_impl(d_in, n, chunk_elems, n_chunks, sigma_hint, d_out, out_capacity, d_chunk_offsets, d_send,
+                       send_capacity, d_chunk_ready, d_ws, ws_bytes, stream);
 }
 
 zipccl_status zipccl_decompress(const void* d_stream, const uint64_t* d_chunk_offsets, uint32_t n_chunks,
@@ -313,11 +345,12 @@ zipccl_status zipccl_choose_compressed(uint64_t n, float sigma, double link_gbs,
 }
 
 zipccl_status zipccl_selftest_bounded_wait(int which, void* d_ws, uint64_t ws_bytes, void* stream) {
-  if ((which != 0 && which != 1) || !d_ws || !aligned(d_ws, 256) || ws_bytes < sizeof(WsHeader) + 16)
-    return ZIPCCL_ERR_INVALID_ARG;
+  // which 2 reads one chunk record and one offset after the status header
+  const uint64_t need = sizeof(WsHeader) + (which == 2 ? sizeof(EncChunk) + 16 : 16);
+  if (which < 0 || which > 2 || !d_ws || !aligned(d_ws, 256) || ws_bytes < need) return ZIPCCL_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
-  if (cudaMemsetAsync(ws, 0, sizeof(WsHeader) + 16, s) != cudaSuccess) return ZIPCCL_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, need, s) != cudaSuccess) return ZIPCCL_ERR_CUDA;
   return cuda_status(launch_selftest_wait(reinterpret_cast<WsHeader*>(ws), reinterpret_cast<uint64_t*>(ws + sizeof(WsHeader)),
                                           which, s));
 }

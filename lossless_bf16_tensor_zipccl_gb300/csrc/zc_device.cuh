@@ -32,6 +32,20 @@ __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// Acquire load and release add at GPU scope: the per-chunk completion count
+// of the compress-and-send call.  A writer's earlier stores (its own, and
+// those ordered before by a fence) are visible to a reader whose acquire
+// load sees the count.
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add_u64(uint64_t* p, uint64_t v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 __device__ __forceinline__ void set_status(WsHeader* h, uint32_t code) {
   atomicCAS(&h->status, 0u, code);
 }
@@ -80,6 +94,19 @@ __device__ __forceinline__ void bulk_store_issue(void* gdst, const void* ssrc, u
 __device__ __forceinline__ void bulk_commit_and_wait_read() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until at most one (all_but_last) or none (all) of this thread's bulk
+// groups is still writing global memory, then order those writes (made by
+// the async proxy) before this thread's later generic-proxy operations.
+__device__ __forceinline__ void bulk_wait_written_all_but_last() {
+  asm volatile("cp.async.bulk.wait_group 1;" ::: "memory");
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_written_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // ---- mbarrier-tracked TMA bulk loads global -> shared

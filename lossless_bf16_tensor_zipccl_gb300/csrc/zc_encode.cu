@@ -100,7 +100,8 @@ __global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ 
     ec.base = (uint32_t)base;
     ec.lens = lens;
     ec.start_slot = 0;
-    ec.pad[0] = ec.pad[1] = 0;
+    ec.done = 0;
+    ec.end = 0;
     a.chunks[ci] = ec;
   }
   // Code tables of the chunk.  tab[e]: reversed codeword | length << 24 (an
@@ -192,8 +193,11 @@ __global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ 
 constexpr int kRowWarpsPerHalf = 8;
 constexpr int kRowWarps = 2 * kRowWarpsPerHalf;
 constexpr int kLayoutWarp = kRowWarps;
+constexpr int kStoreWarp = kRowWarps + 1;
+constexpr int kSendWarp = kRowWarps + 2;  // compress-and-send only
 constexpr int kRowThreads = 32 * kRowWarps;
 constexpr int kEncThreads = 32 * (kRowWarps + 2);
+constexpr int kEncThreadsSend = kEncThreads + 32;
 constexpr uint32_t kBarThreads = kRowThreads + 32;      // row warps + one role warp
 constexpr int kRowsPerWarp = kRows / kRowWarpsPerHalf;   // 8
 constexpr uint32_t kPrivWords = 8;                        // 256 bits per lane part (4 bits per value)
@@ -750,10 +754,31 @@ __device__ __forceinline__ void layout_tile(const EncodeArgs& a, const EncShared
   bar_arrive(kBarB0 + b, 64);
 }
 
+// What the compress-and-send path publishes about a stored tile once its
+// bytes are in global memory: its chunk, and the chunk's end offset when it
+// is the chunk's last tile.
+struct StoredTile {
+  uint32_t c;
+  uint32_t last;
+  uint64_t end;
+};
+
+// Compress-and-send: the tile's stored bytes (and the headers and offsets its
+// store warp wrote) become visible to the sender warps of every CTA.  Called
+// by all lanes of the store warp after bulk_wait_written_*.
+__device__ __forceinline__ void publish_stored(const EncodeArgs& a, const StoredTile& t) {
+  __syncwarp();  // the other lanes' header and table stores come before the release
+  if ((threadIdx.x & 31) == 0) {
+    if (t.last) st_relaxed_u64(&a.chunks[t.c].end, t.end);
+    red_release_add_u64(&a.chunks[t.c].done, 1);
+  }
+}
+
 // Store warp, one tile: phases C and E.  `reuse`: the row warps will pack a
 // later tile into this tile's image, so announce when its store has read it.
+// `stored` receives what the compress-and-send path publishes later.
 __device__ __forceinline__ void store_tile(const EncodeArgs& a, const EncShared& S, uint32_t buf, uint32_t item,
-                                           const EncItem& rec, const EncChunk& ci, bool reuse) {
+                                           const EncItem& rec, const EncChunk& ci, bool reuse, StoredTile& stored) {
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t c = rec.c, k = rec.k, nt = rec.nt;
   const uint64_t hdr = chunk_hdr_bytes(ci.n_tiles);
@@ -796,14 +821,17 @@ __device__ __forceinline__ void store_tile(const EncodeArgs& a, const EncShared&
     }
   }
   const uint64_t goff = excl + (k == 0 ? hdr : 0);
-  if (!err && (goff + size > a.cap || cs + hdr > a.cap)) {
+  const uint64_t lim = a.send && a.send_cap < a.cap ? a.send_cap : a.cap;  // both copies must fit
+  if (!err && (goff + size > lim || cs + hdr > lim)) {
     err = true;
     if (lane == 0) set_status(a.hdr, kStCapacity);
   } else if (err && lane == 0) {
     set_status(a.hdr, kStTimeout);
   }
-  if (!err) {
-    uint8_t* cp = a.out + cs;
+  // the chunk header and tile table go to the output and, with a send
+  // buffer, to the same offsets there
+  for (uint32_t copy = 0; !err && copy < (a.send ? 2u : 1u); ++copy) {
+    uint8_t* cp = (copy ? a.send : a.out) + cs;
     if (k == 0) {
       if (lane < 8) {
         uint32_t v;
@@ -824,20 +852,62 @@ __device__ __forceinline__ void store_tile(const EncodeArgs& a, const EncShared&
       if (tail0 + 4 * lane < tail1) reinterpret_cast<uint32_t*>(cp + kChunkHdr + tail0)[lane] = 0;
     }
     if (nt && lane == 0) reinterpret_cast<uint32_t*>(cp + kChunkHdr)[k] = (uint32_t)(goff - cs);
-    if (item == a.n_items - 1 && lane == 0) a.offsets[a.n_chunks] = excl + agg;
   }
+  if (!err && item == a.n_items - 1 && lane == 0) a.offsets[a.n_chunks] = excl + agg;
+
+  stored.c = c;
+  stored.last = k + 1 >= ci.n_tiles ? 1u : 0u;  // an empty chunk's header-only item is its last
+  stored.end = err ? 0 : goff + size;
 
   bar_wait(kBarImg0 + buf, kBarThreads);
-  // Phase E: one TMA bulk store of the finished tile image.
-  if (lane == 0 && !err && size) {
-    bulk_store_issue(a.out + goff, S.img(buf), size);
-    bulk_commit_and_wait_read();
+  // Phase E: one TMA bulk store of the finished tile image, and with a send
+  // buffer a second one of the same image there (the send costs HBM writes
+  // only).  With a send buffer every tile commits one bulk group (empty when
+  // nothing is stored), so that the group before last is always the
+  // previous tile's.
+  if (lane == 0) {
+    if (!err && size) {
+      bulk_store_issue(a.out + goff, S.img(buf), size);
+      if (a.send) bulk_store_issue(a.send + goff, S.img(buf), size);
+    }
+    if (a.send || (!err && size)) bulk_commit_and_wait_read();
   }
   __syncwarp();
   if (reuse) bar_arrive(kBarFree0 + buf, kBarThreads);
 }
 
-__global__ void __launch_bounds__(kEncThreads, 1) zc_encode_kernel(EncodeArgs a) {
+// Sender warp of the compress-and-send path (CTA 0 only): the stand-in for
+// the proxy that posts each chunk to its destination rank.  For chunks 0, 1,
+// ... in order it waits until every tile of the chunk is stored in both
+// buffers (the count published with release semantics by the store warps),
+// then posts the chunk: here, it records %globaltimer in ready[c], so the
+// caller sees how early each chunk could have left.  Waits are bounded; a
+// wait that gives up records ZIPCCL_ERR_TIMEOUT and ends the posting, as does
+// an error already recorded by the coding warps.
+__device__ void send_chunks(const EncodeArgs& a) {
+  const uint32_t lane = threadIdx.x & 31;
+  for (uint32_t c = 0; c < a.n_chunks; ++c) {
+    const uint32_t nt = a.chunks[c].n_tiles;
+    const uint64_t want = nt ? nt : 1u;
+    uint32_t ok = 1;
+    if (lane == 0) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_u64(&a.chunks[c].done) < want) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          ok = 0;
+          break;
+        }
+        __nanosleep(128);
+      }
+      if (!ok) set_status(a.hdr, kStTimeout);
+      else if (*reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0) ok = 0;
+      if (ok && a.ready) a.ready[c] = globaltimer_ns();
+    }
+    if (!__shfl_sync(kFull, ok, 0)) return;
+  }
+}
+
+__global__ void __launch_bounds__(kEncThreadsSend, 1) zc_encode_kernel(EncodeArgs a) {
   pdl_wait();  // records and tables come from the select kernel
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t s_segstart[kImgBufs * kSegs], s_mode[kImgBufs], s_over[kImgBufs], s_size[kImgBufs];
@@ -910,18 +980,35 @@ __global__ void __launch_bounds__(kEncThreads, 1) zc_encode_kernel(EncodeArgs a)
       layout_tile(a, S, b, i, t, t + 2 * G);
       b = b + 1 == kImgBufs ? 0 : b + 1;
     }
-  } else {
+  } else if (warp == kStoreWarp) {
     __syncthreads();
     // records are loaded one tile ahead
     EncItem rec = load_item(a, t0);
     EncChunk ch = a.chunks[rec.c];
+    StoredTile prev = {0, 0, 0};
     for (uint32_t i = 0; i < count; ++i) {
       const uint32_t t = t0 + i * G;
       const EncItem rn = load_item(a, t + G);
       const EncChunk chn = a.chunks[rn.c];
-      store_tile(a, S, i % kImgBufs, t, rec, ch, i + kImgBufs < count);
+      StoredTile cur;
+      store_tile(a, S, i % kImgBufs, t, rec, ch, i + kImgBufs < count, cur);
+      if (a.send && i > 0) {  // the previous tile's bulk group has written its bytes
+        if (lane == 0) bulk_wait_written_all_but_last();
+        publish_stored(a, prev);
+      }
+      prev = cur;
       rec = rn;
       ch = chn;
+    }
+    if (a.send && count > 0) {
+      if (lane == 0) bulk_wait_written_all();
+      publish_stored(a, prev);
+    }
+  } else {
+    __syncthreads();
+    if (a.send && blockIdx.x == 0) {
+      if (lane == 0 && a.ready) a.ready[a.n_chunks] = globaltimer_ns();
+      send_chunks(a);
     }
   }
 }
@@ -929,8 +1016,9 @@ __global__ void __launch_bounds__(kEncThreads, 1) zc_encode_kernel(EncodeArgs a)
 // ---------------------------------------------------------------- bounded-wait self-test
 // One warp waits, through the encoder's and the decoders' own code, on
 // something no one completes: the look-back state of a predecessor tile
-// (which = 0: tile 1 waits on tile 0, whose state stays 0) or the phase of an
-// mbarrier no one arrives on (which = 1).  The wait gives up at its limit and
+// (which = 0: tile 1 waits on tile 0, whose state stays 0), the phase of an
+// mbarrier no one arrives on (which = 1), or the compress-and-send sender's
+// wait for a chunk whose tiles are never stored (which = 2).  The wait gives up at its limit and
 // the kernel records the timeout in the workspace status.
 __global__ void zc_selftest_wait_kernel(WsHeader* hdr, uint64_t* state, int which) {
   __shared__ __align__(8) uint64_t bar;
@@ -940,6 +1028,18 @@ __global__ void zc_selftest_wait_kernel(WsHeader* hdr, uint64_t* state, int whic
     bool err = false;
     (void)lookback(state, 1, lane, err);
     timed_out = err;
+  } else if (which == 2) {
+    // the compress-and-send sender's wait: one chunk of one tile whose
+    // completion count stays 0 (the encoder never runs)
+    EncodeArgs a = {};
+    a.chunks = reinterpret_cast<EncChunk*>(state);
+    a.offsets = state + sizeof(EncChunk) / 8;
+    a.hdr = hdr;
+    a.n_chunks = 1;
+    a.send = reinterpret_cast<uint8_t*>(state);
+    a.ready = nullptr;
+    send_chunks(a);
+    timed_out = false;  // send_chunks records the timeout itself
   } else {
     if (lane == 0) mbar_init(&bar, 1);
     __syncwarp();
@@ -976,7 +1076,7 @@ cudaError_t launch_encode(const EncodeArgs& args, uint32_t n_items, cudaStream_t
     int sms = 0, per_sm = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, zc_encode_kernel, kEncThreads, kEncSmem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, zc_encode_kernel, kEncThreadsSend, kEncSmem);
     if (e != cudaSuccess) return e;
     if (sms <= 0 || per_sm <= 0) return cudaErrorInvalidConfiguration;
     ctas = sms * per_sm;
@@ -986,7 +1086,8 @@ cudaError_t launch_encode(const EncodeArgs& args, uint32_t n_items, cudaStream_t
   // the cooperative launch guarantees it (or fails).
   const uint32_t grid = min(n_items, (uint32_t)ctas);
   cudaLaunchAttribute at[2];
-  const cudaLaunchConfig_t cfg = follow_config(dim3(grid), dim3(kEncThreads), kEncSmem, s, true, at);
+  const int threads = args.send ? kEncThreadsSend : kEncThreads;  // the sender warp only with a send buffer
+  const cudaLaunchConfig_t cfg = follow_config(dim3(grid), dim3(threads), kEncSmem, s, true, at);
   return cudaLaunchKernelEx(&cfg, zc_encode_kernel, args);
 }
 

@@ -108,7 +108,8 @@ struct alignas(64) EncChunk {
   uint32_t base;        // window start exponent
   uint64_t lens;        // 16 x 4-bit code lengths, symbol s at bits 4s..4s+3
   uint64_t start_slot;  // kSlotValid | chunk byte offset, published by tile 0
-  uint64_t pad[2];
+  uint64_t done;        // compress-and-send: tiles whose stores have completed
+  uint64_t end;         // compress-and-send: chunk end offset, from its last tile
 };
 static_assert(sizeof(EncChunk) == 64, "enc chunk");
 

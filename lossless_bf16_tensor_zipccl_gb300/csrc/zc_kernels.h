@@ -40,6 +40,9 @@ struct EncodeArgs {
   const uint16_t* in;
   uint8_t* out;
   uint64_t cap;
+  uint8_t* send;       // compress-and-send: second copy of every tile (null: none)
+  uint64_t send_cap;
+  uint64_t* ready;     // compress-and-send: %globaltimer when chunk c was complete (nullable)
   uint64_t* offsets;
   EncChunk* chunks;
   const uint32_t* tables;

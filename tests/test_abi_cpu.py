@@ -99,8 +99,24 @@ def test_compress_argument_errors_return_before_launch():
         zc.ERR_INVALID_ARG
 
 
+def test_compress_send_argument_errors_return_before_launch():
+    cap = zc.zipccl_max_compressed_bytes([100])
+    ws = zc.zipccl_compress_workspace_bytes([100])
+    SEND = FAKE + (1 << 20)
+
+    def call(send, send_cap, out=FAKE):
+        return zc.zipccl_compress_send(FAKE, 100, [100], None, out, cap, FAKE, send, send_cap, 0, FAKE, ws, 0)
+    assert call(0, cap) == zc.ERR_INVALID_ARG              # no send buffer
+    assert call(SEND + 8, cap) == zc.ERR_INVALID_ARG       # misaligned
+    assert call(FAKE, cap) == zc.ERR_INVALID_ARG           # the output itself
+    assert call(SEND, cap - 1) == zc.ERR_CAPACITY          # below the worst-case size
+    assert zc.zipccl_compress_send(FAKE, 100, [100], None, FAKE, cap, FAKE, SEND, cap, FAKE + 4, FAKE, ws, 0) == \
+        zc.ERR_INVALID_ARG                                   # misaligned ready array
+
+
 def test_selftest_argument_errors_return_before_launch():
-    assert zc.zipccl_selftest_bounded_wait(2, FAKE, 512, 0) == zc.ERR_INVALID_ARG
+    assert zc.zipccl_selftest_bounded_wait(3, FAKE, 512, 0) == zc.ERR_INVALID_ARG
+    assert zc.zipccl_selftest_bounded_wait(2, FAKE, 335, 0) == zc.ERR_INVALID_ARG
     assert zc.zipccl_selftest_bounded_wait(-1, FAKE, 512, 0) == zc.ERR_INVALID_ARG
     assert zc.zipccl_selftest_bounded_wait(0, 0, 512, 0) == zc.ERR_INVALID_ARG
     assert zc.zipccl_selftest_bounded_wait(0, FAKE + 16, 512, 0) == zc.ERR_INVALID_ARG

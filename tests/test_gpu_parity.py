@@ -264,10 +264,77 @@ def test_side_stream_calls_with_library_allocated_buffers():
         [oracle.compress(p)[0] for p in peers], 100000))
 
 
-@pytest.mark.parametrize("which", [0, 1])
+def compress_send_check(x: np.ndarray, chunk_elems, hint=None):
+    """zipccl_compress_send through the C ABI: the stream equals the oracle's, the
+    send buffer holds the same bytes over the stream's extent and nothing past it,
+    and every chunk is posted in order."""
+    d = to_dev(x)
+    cap = zc.zipccl_max_compressed_bytes(chunk_elems)
+    out = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    send = torch.full((cap + 64,), 0xAB, dtype=torch.uint8, device="cuda")
+    offs = torch.empty(len(chunk_elems) + 1, dtype=torch.int64, device="cuda")
+    ws = torch.empty(zc.zipccl_compress_workspace_bytes(chunk_elems), dtype=torch.uint8, device="cuda")
+    sp = torch.cuda.current_stream().cuda_stream
+    ready = torch.zeros(len(chunk_elems) + 1, dtype=torch.int64, device="cuda")
+    st = zc.zipccl_compress_send(d.data_ptr(), x.size, chunk_elems, hint, out.data_ptr(), cap, offs.data_ptr(),
+                                 send.data_ptr(), cap, ready.data_ptr(), ws.data_ptr(), ws.numel(), sp)
+    assert st == zc.OK
+    assert zc.zipccl_get_device_status(ws.data_ptr(), sp) == zc.OK
+    # every chunk was posted, in chunk order, after the kernel started
+    r = ready.cpu().numpy()
+    assert (r[:-1] >= r[-1]).all() and (np.diff(r[:-1]) >= 0).all() and r[-1] > 0
+    o = offs.cpu().numpy().view(np.uint64)
+    total = int(o[-1])
+    so, oo = oracle.compress(x, chunk_elems, hint)
+    assert np.array_equal(o, oo), "chunk offsets differ from the oracle"
+    assert out[:total].cpu().numpy().tobytes() == so, "stream differs from the oracle"
+    assert torch.equal(send[:total], out[:total]), "send buffer differs from the stream"
+    assert bool((send[total:] == 0xAB).all()), "send buffer written past the stream"
+    return total
+
+
+@pytest.mark.parametrize("case", ["one_chunk", "eight_chunks", "ragged_empty", "many_small", "raw_tiles"])
+def test_compress_send_parity(case):
+    # compress-and-send: each chunk is written to the send buffer and posted as soon as its tiles are stored
+    if case == "one_chunk":
+        w = workloads.gaussian_bf16(300000, 0.02, 21)
+        compress_send_check(w, [w.size])
+    elif case == "eight_chunks":
+        x = np.concatenate([workloads.gaussian_bf16(131072 + 777 * r, 1e-3, 22, r) for r in range(8)])
+        compress_send_check(x, [131072 + 777 * r for r in range(8)])
+    elif case == "ragged_empty":
+        w = workloads.random_chunks(23, n_chunks=40, max_elems=90000, empty_prob=0.2)
+        compress_send_check(w.x, w.chunk_elems, [0.0 if i % 3 else 0.01 for i in range(40)])
+    elif case == "many_small":
+        # more chunks than CTAs, many of them a fraction of a tile
+        w = workloads.random_chunks(24, n_chunks=400, max_elems=9000, empty_prob=0.1)
+        compress_send_check(w.x, w.chunk_elems)
+    else:
+        rng = np.random.default_rng(25)
+        x = np.concatenate([workloads.gaussian_bf16(70000, 1.0, 25),
+                            rng.integers(0, 65536, size=100000, dtype=np.uint16)])
+        compress_send_check(x, [70000, 100000])
+
+
+def test_compress_send_gradient_bucket():
+    # the full 67,108,864-value bucket in 8 chunks: send == out byte for byte, and the
+    # sampled chunks equal the oracle's
+    w = workloads.gradient()
+    d = to_dev(w.x)
+    cap = zc.zipccl_max_compressed_bytes(w.chunk_elems)
+    send = torch.zeros(cap, dtype=torch.uint8, device="cuda")
+    c = zc.compress(d, w.chunk_elems, send=send)
+    torch.cuda.synchronize()
+    s, offs = sampled_chunk_parity(w, c, [0, 7])
+    assert torch.equal(send[: len(s)], c.data[: len(s)])
+
+
+@pytest.mark.parametrize("which", [0, 1, 2])
 def test_bounded_wait_gives_up_and_context_stays_usable(which):
     # 0: the compressor's look-back on a predecessor that never publishes;
-    # 1: an mbarrier phase that never completes.  Each wait has a 2 s limit.
+    # 1: an mbarrier phase that never completes; 2: the compress-and-send
+    # sender's wait for a chunk whose tiles are never stored (no encoder is
+    # launched).  Each wait has a 2 s limit.
     import time
     ws = torch.empty(512, dtype=torch.uint8, device="cuda")
     s = torch.cuda.current_stream().cuda_stream
