@@ -540,6 +540,16 @@ constexpr uint32_t kRedSlot = 5696;  // staged half payload per peer (~2.78 bits
 constexpr uint32_t kRedBufs = 2;     // fp32 half-row accumulators in the ring
 constexpr uint32_t kRedAcc = kRedBufs * kHalf * 4;
 
+// Up to this many peers, the hand-off from warp p to warp p + 1 of buffer j
+// is a hardware named barrier (ids 1 .. 2 (K - 1), two warps each: one
+// arrives, one waits): cheaper than an mbarrier phase.  Every warp folds the
+// same rows, so each barrier sees one arrival per wait; warp p arrives for
+// row r + kRedBufs only after warp p + 1 has waited for row r, since warp 0
+// reuses a buffer only after the last warp has finished with it.
+constexpr uint32_t kNamedFoldPeers = 8;
+static_assert(1 + 2 * (kNamedFoldPeers - 1) <= 15, "named barrier ids");
+__device__ __forceinline__ uint32_t fold_barrier(uint32_t p, uint32_t j) { return 1 + kRedBufs * p + j; }
+
 __host__ __device__ constexpr size_t reduce_smem_bytes(uint32_t k) {
   return 2 * kLutEntries * 4 + kRedAcc + (size_t)k * (kRedSlot + 16 + 8 * kRedBufs) + kStagePad;
 }
@@ -561,7 +571,12 @@ __device__ __forceinline__ bool reduce_rows(RowSource<kStaged>& src, const uint8
     const uint32_t j = r % kRedBufs, use = r / kRedBufs;  // buffer, and its use count before row r
     // wait for the previous warp's row r, or (warp 0) for the last warp to
     // have finished the previous row in this buffer
-    if (live) {
+    if (K <= kNamedFoldPeers) {
+      // warp p - 1 -> p through a named barrier per (pair, buffer); the last
+      // warp -> warp 0 (the buffer is free again) through its mbarrier
+      if (p > 0) asm volatile("bar.sync %0, 64;" ::"r"(fold_barrier(p - 1, j)) : "memory");
+      else if (K > 1 && use > 0 && live) live = mbar_wait(done + kRedBufs * (K - 1) + j, (use - 1) & 1);
+    } else if (live) {
       if (p > 0) live = mbar_wait(done + kRedBufs * (p - 1) + j, use & 1);
       else if (K > 1 && use > 0) live = mbar_wait(done + kRedBufs * (K - 1) + j, (use - 1) & 1);
     }
@@ -596,7 +611,8 @@ __device__ __forceinline__ bool reduce_rows(RowSource<kStaged>& src, const uint8
       }
       if (cnt) store_row(y + r * kRow + col, cnt, (reinterpret_cast<uintptr_t>(y) & 15) == 0, make_uint4(o[0], o[1], o[2], o[3]));
     }
-    mbar_arrive(done + kRedBufs * p + j);
+    if (K <= kNamedFoldPeers && p + 1 < K) asm volatile("bar.arrive %0, 64;" ::"r"(fold_barrier(p, j)) : "memory");
+    else mbar_arrive(done + kRedBufs * p + j);
   };
   if (fast) {
     // full coded tile: 8 values per lane in every row

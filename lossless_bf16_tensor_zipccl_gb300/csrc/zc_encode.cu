@@ -1004,7 +1004,7 @@ __global__ void __launch_bounds__(kEncThreadsSend, 1) zc_encode_kernel(EncodeArg
       if (lane == 0) bulk_wait_written_all();
       publish_stored(a, prev);
     }
-  } else {
+  } else if (warp == kSendWarp) {
     __syncthreads();
     if (a.send && blockIdx.x == 0) {
       if (lane == 0 && a.ready) a.ready[a.n_chunks] = globaltimer_ns();
