@@ -323,12 +323,57 @@ __device__ __forceinline__ void decode_rows(RowSource<kStaged>& src, bool full, 
   }
 }
 
+// The same rows with the tile's whole sign/mantissa plane already in shared
+// memory (pl: this lane's bytes of row 0 there; plain loads, never the
+// global-only streaming loads).
+__device__ __forceinline__ uint2 plane_bytes8(const uint8_t* p, uint32_t cnt) {
+  if (cnt == 8) return *reinterpret_cast<const uint2*>(p);
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    if (t < (int)cnt) {
+      const uint32_t b = p[t];
+      if (t < 4) lo |= b << (8 * t);
+      else hi |= b << (8 * (t - 4));
+    }
+  }
+  return make_uint2(lo, hi);
+}
+
+template <bool kStaged>
+__device__ __forceinline__ void decode_rows_plane(RowSource<kStaged>& src, bool full, const uint8_t* pl, uint16_t* y,
+                                                  bool vec) {
+  if (full) {
+#pragma unroll 4
+    for (uint32_t r = 0; r < kRows; ++r) {
+      const uint2 sm = *reinterpret_cast<const uint2*>(pl + r * kRow);
+      uint32_t elo, ehi;
+      src.dec.fill_warp(8);
+      src.dec.template take8<true>(elo, ehi);
+      const uint2 u = merge4(elo, sm.x), v = merge4(ehi, sm.y);
+      *reinterpret_cast<uint4*>(y + r * kRow) = make_uint4(u.x, u.y, v.x, v.y);
+    }
+  } else {
+    const uint32_t rows = (src.nt + kRow - 1) / kRow;
+    for (uint32_t r = 0; r < rows; ++r) {
+      const uint32_t cnt = src.count(r);
+      const uint4 v = src.row(r, plane_bytes8(pl + r * kRow, cnt));
+      if (cnt) store_row(y + r * kRow, cnt, vec, v);
+    }
+  }
+}
+
 // Chunks up to this count are found by each decode CTA itself while the prep
 // kernel runs (one offset and one header per thread of the 64-thread CTA).
 constexpr uint32_t kEarlyChunks = 64;
 
+// kPlane: the tile's sign/mantissa plane also comes into shared memory by
+// TMA (dynamic shared memory, 32 KB), for grids of a few tiles per SM, where
+// each CTA's rows would otherwise wait on their own global loads.
+template <bool kPlane>
 __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
   __shared__ __align__(128) uint8_t s_exp[kExpSlot + kStagePad];
+  extern __shared__ __align__(128) uint8_t s_plane[];  // kPlane only
   __shared__ __align__(16) uint32_t s_lut[kLutEntries];
   __shared__ __align__(8) uint64_t s_xbar;
   __shared__ uint32_t s_flag[3];
@@ -342,7 +387,7 @@ __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
 
   // This tile's chunk c and index k in it; its tile view, payload copy and
   // first sign/mantissa loads.
-  uint32_t c = 0, k = 0, nt = 0, n_tiles = 0, sbytes = 0;
+  uint32_t c = 0, k = 0, nt = 0, n_tiles = 0, sbytes = 0, pbytes = 0;
   const uint8_t* ch = nullptr;
   TileView tv = {};
   bool located = false;
@@ -353,12 +398,14 @@ __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
               open_tile(ch, chunk_bytes, n_tiles, k, nt, half, lane, tv);
     uint32_t slo = 0;
     sbytes = located && tv.mode == 0 ? stage_span(tv, 0, tv.bits, kExpSlot, slo) : 0u;  // the same in both warps
-    if (tid == 0 && sbytes) {
+    pbytes = kPlane && located ? (uint32_t)pad16(nt) : 0u;  // within the chunk: open_tile checked the region after it
+    if (tid == 0 && (sbytes || pbytes)) {
       mbar_init(&s_xbar, 1);
-      mbar_arrive_expect_tx(&s_xbar, sbytes);
-      bulk_copy_g2s(s_exp, tv.tile + tv.exp_off + kSegTab, sbytes, &s_xbar);
+      mbar_arrive_expect_tx(&s_xbar, sbytes + pbytes);
+      if (sbytes) bulk_copy_g2s(s_exp, tv.tile + tv.exp_off + kSegTab, sbytes, &s_xbar);
+      if (pbytes) bulk_copy_g2s(s_plane, tv.tile + kTileHdr, pbytes, &s_xbar);
     }
-    if (located && nt == kTile && tv.mode == 0) {
+    if (!kPlane && located && nt == kTile && tv.mode == 0) {
       const uint8_t* smp = tv.tile + kTileHdr + col;
 #pragma unroll
       for (uint32_t r = 0; r < kSmAhead; ++r) sq[r] = ld_stream_v2(smp + r * kRow);
@@ -413,7 +460,7 @@ __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
   if (tid == 0) s_flag[0] = *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0 || item >= a.hdr->total_items;
   __syncthreads();
   if (s_flag[0]) {
-    if (tid == 0 && sbytes) mbar_wait(&s_xbar, 0);  // nothing left in flight
+    if (tid == 0 && (sbytes || pbytes)) mbar_wait(&s_xbar, 0);  // nothing left in flight
     return;
   }
   if (!early) {
@@ -443,7 +490,7 @@ __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
   load_lut(s_lut, a.luts + (size_t)(d.ok ? c : 0) * kLutEntries, tid, 64);
   __syncthreads();  // the table is in place; the payload barrier is initialised
   const bool bad = s_flag[1] | s_flag[2];
-  const bool timeout = sbytes && __any_sync(kFull, !mbar_wait(&s_xbar, 0));
+  const bool timeout = (sbytes || pbytes) && __any_sync(kFull, !mbar_wait(&s_xbar, 0));
   if (bad || timeout) {
     // the copy has arrived or was given up on; the status tells the caller
     if (lane == 0) set_status(a.hdr, bad ? kStCorrupt : kStTimeout);
@@ -454,17 +501,20 @@ __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
   const bool vec = (e0 & 7) == 0;
   const uint8_t* smp = tv.tile + kTileHdr + col;  // this lane's sign/mantissa bytes of row 0
   const bool full = nt == kTile && vec && tv.mode == 0;
+  const uint8_t* pl = s_plane + col;  // kPlane: this lane's bytes of row 0 in the staged plane
   if (sbytes) {
     RowSource<true> src;
     const ExpSource xs{reinterpret_cast<const uint32_t*>(s_exp), 0u, nullptr};
     src.start(tv, nt, col, s_lut, d.base, xs);
-    decode_rows(src, full, smp, y, vec, sq);
+    if constexpr (kPlane) decode_rows_plane(src, full, pl, y, vec);
+    else decode_rows(src, full, smp, y, vec, sq);
   } else {
     RowSource<false> src;
     const ExpSource xs{reinterpret_cast<const uint32_t*>(tv.tile + tv.exp_off + kSegTab), 0u,
                        reinterpret_cast<const uint32_t*>(tv.tile + tv.exp_off + pad16(tv.exp_bytes))};
     src.start(tv, nt, col, s_lut, d.base, xs);
-    decode_rows(src, full, smp, y, vec, sq);
+    if constexpr (kPlane) decode_rows_plane(src, full, pl, y, vec);
+    else decode_rows(src, full, smp, y, vec, sq);
   }
 }
 
@@ -743,13 +793,35 @@ __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
 // several host threads may both do the set-up; each stores the same value.
 static std::atomic<int> g_red_attr_done[64];
 
+// Per device: SM count for the choice of decode kernel (0: not read yet).
+static std::atomic<int> g_dec_sms[64];
+constexpr uint32_t kPlaneCtasPerSm = 4;  // the plane-staging decoder fits 4 CTAs per SM
+
 cudaError_t launch_decode(const DprepArgs& prep, const DecodeArgs& args, uint32_t max_items, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int sms = g_dec_sms[dev].load(std::memory_order_acquire);
+  if (!sms) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(zc_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTile);
+    if (e != cudaSuccess) return e;
+    g_dec_sms[dev].store(sms, std::memory_order_release);
+  }
   zc_dprep_kernel<<<prep.n_chunks * kLutParts + 1, 256, 0, s>>>(prep);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess || max_items == 0) return e;
   cudaLaunchAttribute at[2];
+  // A few tiles per SM: each CTA's latency is the time, so stage the plane
+  // too; more: the small CTA keeps 14 tiles per SM in flight.
+  if (max_items <= kPlaneCtasPerSm * (uint32_t)sms) {
+    const cudaLaunchConfig_t cfg = follow_config(dim3(max_items), dim3(64), kTile, s, false, at);
+    return cudaLaunchKernelEx(&cfg, zc_decode_kernel<true>, args);
+  }
   const cudaLaunchConfig_t cfg = follow_config(dim3(max_items), dim3(64), 0, s, false, at);
-  return cudaLaunchKernelEx(&cfg, zc_decode_kernel, args);
+  return cudaLaunchKernelEx(&cfg, zc_decode_kernel<false>, args);
 }
 
 template <uint32_t K>

@@ -782,15 +782,12 @@ __device__ __forceinline__ void store_tile(const EncodeArgs& a, const EncShared&
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t c = rec.c, k = rec.k, nt = rec.nt;
   const uint64_t hdr = chunk_hdr_bytes(ci.n_tiles);
-  bar_wait(kBarB0 + buf, 64);
-  const uint32_t size = S.size[buf];
-  const uint64_t agg = size + (k == 0 ? hdr : 0);
-
   // Phase C: look-back for this tile's byte offset, chunk header / tile
-  // table / chunk offsets.
+  // table / chunk offsets.  The look-back and the wait for the chunk's start
+  // need only earlier tiles, so they run before this tile's own size is
+  // known, while its rows are still being packed and laid out.
   bool err = false;
   const uint64_t excl = item == 0 ? 0 : lookback(a.item_state, item, lane, err);
-  if (item != 0 && lane == 0) st_relaxed_u64(a.item_state + item, err ? kFlagErr : (kFlagInc | (excl + agg)));
   uint64_t cs = 0;
   if (!err) {
     if (k == 0) {
@@ -820,6 +817,10 @@ __device__ __forceinline__ void store_tile(const EncodeArgs& a, const EncShared&
       cs = v & ~kSlotValid;
     }
   }
+  bar_wait(kBarB0 + buf, 64);
+  const uint32_t size = S.size[buf];
+  const uint64_t agg = size + (k == 0 ? hdr : 0);
+  if (item != 0 && lane == 0) st_relaxed_u64(a.item_state + item, err ? kFlagErr : (kFlagInc | (excl + agg)));
   const uint64_t goff = excl + (k == 0 ? hdr : 0);
   const uint64_t lim = a.send && a.send_cap < a.cap ? a.send_cap : a.cap;  // both copies must fit
   if (!err && (goff + size > lim || cs + hdr > lim)) {
