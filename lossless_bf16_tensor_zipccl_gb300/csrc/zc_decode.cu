@@ -600,6 +600,48 @@ constexpr uint32_t kNamedFoldPeers = 8;
 static_assert(1 + 2 * (kNamedFoldPeers - 1) <= 15, "named barrier ids");
 __device__ __forceinline__ uint32_t fold_barrier(uint32_t p, uint32_t j) { return 1 + kRedBufs * p + j; }
 
+// An SM holds 64 hardware named barriers, and a barrier instruction with a
+// register id makes ptxas reserve all 16 for the block, so at most 4 blocks
+// are resident.  For up to this many peers a second instantiation names each
+// hand-off barrier as an immediate (a warp-uniform switch): its blocks
+// reserve only the 2 (K - 1) + 1 ids they use and are limited by registers
+// and shared memory instead (K = 1..5: 13, 10, 8, 6, 5 blocks per SM).  It
+// is launched only when that takes fewer waves of blocks than the register
+// ids' 4 per SM (from the occupancy API at set-up); otherwise the register
+// ids, which cost no switch per row, keep the grid.  From 6 peers on,
+// registers allow at most 4 blocks anyway.
+constexpr uint32_t kImmFoldPeers = 5;
+
+template <uint32_t kMaxId, bool kArrive>
+__device__ __forceinline__ void fold_bar_imm(uint32_t id) {
+#define ZC_FOLD_BAR(n)                                                            \
+  case n:                                                                         \
+    if constexpr (kMaxId >= n) {                                                  \
+      if constexpr (kArrive) asm volatile("bar.arrive " #n ", 64;" ::: "memory"); \
+      else asm volatile("bar.sync " #n ", 64;" ::: "memory");                     \
+    }                                                                             \
+    break;
+  switch (id) {
+    ZC_FOLD_BAR(1) ZC_FOLD_BAR(2) ZC_FOLD_BAR(3) ZC_FOLD_BAR(4) ZC_FOLD_BAR(5)
+    ZC_FOLD_BAR(6) ZC_FOLD_BAR(7) ZC_FOLD_BAR(8) ZC_FOLD_BAR(9) ZC_FOLD_BAR(10)
+    default: break;
+  }
+#undef ZC_FOLD_BAR
+}
+
+// Hand-off barrier id of a K-peer block: wait (kArrive false) or arrive.
+template <uint32_t K, bool kImm, bool kArrive>
+__device__ __forceinline__ void fold_bar(uint32_t id) {
+  if constexpr (kImm) {
+    static_assert(K <= kImmFoldPeers, "immediate ids");
+    fold_bar_imm<kRedBufs * (K - 1), kArrive>(id);
+  } else if constexpr (kArrive) {
+    asm volatile("bar.arrive %0, 64;" ::"r"(id) : "memory");
+  } else {
+    asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+  }
+}
+
 __host__ __device__ constexpr size_t reduce_smem_bytes(uint32_t k) {
   return 2 * kLutEntries * 4 + kRedAcc + (size_t)k * (kRedSlot + 16 + 8 * kRedBufs) + kStagePad;
 }
@@ -608,7 +650,7 @@ __host__ __device__ constexpr size_t reduce_smem_bytes(uint32_t k) {
 // done: kRedBufs x K mbarriers (buffer j, warp q at done[kRedBufs q + j]),
 // 32 arrivals each.  sq: the first kSmAhead rows of this lane's sign/mantissa bytes,
 // already in flight.  Returns false if a hand-off wait gave up.
-template <uint32_t K, bool kStaged>
+template <uint32_t K, bool kImm, bool kStaged>
 __device__ __forceinline__ bool reduce_rows(RowSource<kStaged>& src, const uint8_t* smp, float* acc, uint64_t* done,
                                             uint16_t* y, uint2 (&sq)[kSmAhead]) {
   const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5;
@@ -624,7 +666,7 @@ __device__ __forceinline__ bool reduce_rows(RowSource<kStaged>& src, const uint8
     if (K <= kNamedFoldPeers) {
       // warp p - 1 -> p through a named barrier per (pair, buffer); the last
       // warp -> warp 0 (the buffer is free again) through its mbarrier
-      if (p > 0) asm volatile("bar.sync %0, 64;" ::"r"(fold_barrier(p - 1, j)) : "memory");
+      if (K > 1 && p > 0) fold_bar<K, kImm, false>(fold_barrier(p - 1, j));
       else if (K > 1 && use > 0 && live) live = mbar_wait(done + kRedBufs * (K - 1) + j, (use - 1) & 1);
     } else if (live) {
       if (p > 0) live = mbar_wait(done + kRedBufs * (p - 1) + j, use & 1);
@@ -661,7 +703,7 @@ __device__ __forceinline__ bool reduce_rows(RowSource<kStaged>& src, const uint8
       }
       if (cnt) store_row(y + r * kRow + col, cnt, (reinterpret_cast<uintptr_t>(y) & 15) == 0, make_uint4(o[0], o[1], o[2], o[3]));
     }
-    if (K <= kNamedFoldPeers && p + 1 < K) asm volatile("bar.arrive %0, 64;" ::"r"(fold_barrier(p, j)) : "memory");
+    if (K > 1 && K <= kNamedFoldPeers && p + 1 < K) fold_bar<K, kImm, true>(fold_barrier(p, j));
     else mbar_arrive(done + kRedBufs * p + j);
   };
   if (fast) {
@@ -689,8 +731,9 @@ __device__ __forceinline__ bool reduce_rows(RowSource<kStaged>& src, const uint8
   return live;
 }
 
-// Instantiated per peer count K (1..16), so the fold unrolls.
-template <uint32_t K>
+// Instantiated per peer count K (1..16), so the fold unrolls; kImm: the
+// hand-off barriers are immediates (K <= kImmFoldPeers).
+template <uint32_t K, bool kImm>
 __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
   extern __shared__ __align__(128) uint8_t rsm[];
   const uint32_t lane = threadIdx.x & 31, p = threadIdx.x >> 5, tid = threadIdx.x;
@@ -773,17 +816,17 @@ __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
   if (staged && two) {
     RowSource<true> src;
     src.start(tv, nt, col, d.item_start == 0 ? s_lut : s_lut + kLutEntries, d.base, sx);
-    live = reduce_rows<K>(src, smp, acc, done, y, sq);
+    live = reduce_rows<K, kImm>(src, smp, acc, done, y, sq);
   } else if (staged) {
     RowSource<true> src;
     src.start(tv, nt, col, a.luts + (size_t)d.item_start * kLutEntries, d.base, sx);
-    live = reduce_rows<K>(src, smp, acc, done, y, sq);
+    live = reduce_rows<K, kImm>(src, smp, acc, done, y, sq);
   } else {
     RowSource<false> src;
     const ExpSource xs{reinterpret_cast<const uint32_t*>(payload), 0u,
                        reinterpret_cast<const uint32_t*>(tv.tile + tv.exp_off + pad16(tv.exp_bytes))};
     src.start(tv, nt, col, a.luts + (size_t)d.item_start * kLutEntries, d.base, xs);
-    live = reduce_rows<K>(src, smp, acc, done, y, sq);
+    live = reduce_rows<K, kImm>(src, smp, acc, done, y, sq);
   }
   if (!live && lane == 0) set_status(a.hdr, kStTimeout);
 }
@@ -824,18 +867,38 @@ cudaError_t launch_decode(const DprepArgs& prep, const DecodeArgs& args, uint32_
   return cudaLaunchKernelEx(&cfg, zc_decode_kernel<false>, args);
 }
 
+// Per device and peer count: resident blocks per SM of the register-id
+// [0] and immediate-id [1] instantiations (0: none).
+static std::atomic<int> g_red_occ[64][kMaxPeers + 1][2];
+
 template <uint32_t K>
-static cudaError_t reduce_setup() {
-  return cudaFuncSetAttribute(zc_reduce_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)reduce_smem_bytes(K));
+static cudaError_t reduce_setup(int dev) {
+  const int smem = (int)reduce_smem_bytes(K);
+  cudaError_t e = cudaFuncSetAttribute(zc_reduce_kernel<K, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  int occ = 0;
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, zc_reduce_kernel<K, false>, 32 * K, smem);
+  g_red_occ[dev][K][0].store(occ, std::memory_order_relaxed);
+  occ = 0;
+  if constexpr (K <= kImmFoldPeers) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(zc_reduce_kernel<K, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, zc_reduce_kernel<K, true>, 32 * K, smem);
+  }
+  g_red_occ[dev][K][1].store(occ, std::memory_order_relaxed);
+  return e;
 }
 
 template <uint32_t K>
-static cudaError_t reduce_launch(const ReduceArgs& args, uint32_t blocks, cudaStream_t s) {
+static cudaError_t reduce_launch(const ReduceArgs& args, uint32_t blocks, bool imm, cudaStream_t s) {
   cudaLaunchAttribute at[2];
   const cudaLaunchConfig_t cfg = follow_config(dim3(blocks), dim3(32 * K), reduce_smem_bytes(K), s, false, at);
-  return cudaLaunchKernelEx(&cfg, zc_reduce_kernel<K>, args);
+  if constexpr (K <= kImmFoldPeers) {
+    if (imm) return cudaLaunchKernelEx(&cfg, zc_reduce_kernel<K, true>, args);
+  }
+  return cudaLaunchKernelEx(&cfg, zc_reduce_kernel<K, false>, args);
 }
+
+// Per device: SM count for the reduce's choice of instantiation (0: not read yet).
+static std::atomic<int> g_red_sms[64];
 
 cudaError_t launch_reduce(const ReduceArgs& args, cudaStream_t s) {
   int dev = 0;
@@ -843,35 +906,45 @@ cudaError_t launch_reduce(const ReduceArgs& args, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!g_red_attr_done[dev].load(std::memory_order_acquire)) {
-    const cudaError_t es[kMaxPeers] = {reduce_setup<1>(),  reduce_setup<2>(),  reduce_setup<3>(),  reduce_setup<4>(),
-                                       reduce_setup<5>(),  reduce_setup<6>(),  reduce_setup<7>(),  reduce_setup<8>(),
-                                       reduce_setup<9>(),  reduce_setup<10>(), reduce_setup<11>(), reduce_setup<12>(),
-                                       reduce_setup<13>(), reduce_setup<14>(), reduce_setup<15>(), reduce_setup<16>()};
+    const cudaError_t es[kMaxPeers] = {
+        reduce_setup<1>(dev),  reduce_setup<2>(dev),  reduce_setup<3>(dev),  reduce_setup<4>(dev),
+        reduce_setup<5>(dev),  reduce_setup<6>(dev),  reduce_setup<7>(dev),  reduce_setup<8>(dev),
+        reduce_setup<9>(dev),  reduce_setup<10>(dev), reduce_setup<11>(dev), reduce_setup<12>(dev),
+        reduce_setup<13>(dev), reduce_setup<14>(dev), reduce_setup<15>(dev), reduce_setup<16>(dev)};
     for (const cudaError_t x : es)
       if (x != cudaSuccess) return x;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_red_sms[dev].store(sms, std::memory_order_release);
     g_red_attr_done[dev].store(1, std::memory_order_release);
   }
   zc_rprep_kernel<<<args.k * kLutParts, 256, 0, s>>>(args);
   e = cudaGetLastError();
   if (e != cudaSuccess || args.n == 0) return e;
   const uint32_t blocks = 2 * (uint32_t)tiles_of(args.n);
+  // the immediate-id instantiation only where it takes fewer waves
+  const uint64_t sms = (uint64_t)g_red_sms[dev].load(std::memory_order_acquire);
+  const uint64_t r0 = sms * (uint64_t)g_red_occ[dev][args.k][0].load(std::memory_order_relaxed);
+  const uint64_t r1 = sms * (uint64_t)g_red_occ[dev][args.k][1].load(std::memory_order_relaxed);
+  const bool imm = r0 && r1 && (blocks + r1 - 1) / r1 < (blocks + r0 - 1) / r0;
   switch (args.k) {
-    case 1: return reduce_launch<1>(args, blocks, s);
-    case 2: return reduce_launch<2>(args, blocks, s);
-    case 3: return reduce_launch<3>(args, blocks, s);
-    case 4: return reduce_launch<4>(args, blocks, s);
-    case 5: return reduce_launch<5>(args, blocks, s);
-    case 6: return reduce_launch<6>(args, blocks, s);
-    case 7: return reduce_launch<7>(args, blocks, s);
-    case 8: return reduce_launch<8>(args, blocks, s);
-    case 9: return reduce_launch<9>(args, blocks, s);
-    case 10: return reduce_launch<10>(args, blocks, s);
-    case 11: return reduce_launch<11>(args, blocks, s);
-    case 12: return reduce_launch<12>(args, blocks, s);
-    case 13: return reduce_launch<13>(args, blocks, s);
-    case 14: return reduce_launch<14>(args, blocks, s);
-    case 15: return reduce_launch<15>(args, blocks, s);
-    default: return reduce_launch<16>(args, blocks, s);
+    case 1: return reduce_launch<1>(args, blocks, imm, s);
+    case 2: return reduce_launch<2>(args, blocks, imm, s);
+    case 3: return reduce_launch<3>(args, blocks, imm, s);
+    case 4: return reduce_launch<4>(args, blocks, imm, s);
+    case 5: return reduce_launch<5>(args, blocks, imm, s);
+    case 6: return reduce_launch<6>(args, blocks, imm, s);
+    case 7: return reduce_launch<7>(args, blocks, imm, s);
+    case 8: return reduce_launch<8>(args, blocks, imm, s);
+    case 9: return reduce_launch<9>(args, blocks, imm, s);
+    case 10: return reduce_launch<10>(args, blocks, imm, s);
+    case 11: return reduce_launch<11>(args, blocks, imm, s);
+    case 12: return reduce_launch<12>(args, blocks, imm, s);
+    case 13: return reduce_launch<13>(args, blocks, imm, s);
+    case 14: return reduce_launch<14>(args, blocks, imm, s);
+    case 15: return reduce_launch<15>(args, blocks, imm, s);
+    default: return reduce_launch<16>(args, blocks, imm, s);
   }
 }
 

@@ -198,6 +198,26 @@ def test_reduce_peers_with_different_tables():
     assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), ref)
 
 
+@pytest.mark.parametrize("k", [1, 2, 3, 5])
+def test_reduce_grid_beyond_four_blocks_per_sm(k):
+    # more half tiles than 4 per SM: for up to 5 peers the reduce then takes
+    # the instantiation whose hand-off barriers are immediates, since more of
+    # its blocks are resident and the grid runs in fewer waves; a ragged
+    # tail, a raw stretch in one peer, specials in another
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = (2 * sms + 5) * 32768 + 777
+    assert 2 * ((n + 32767) // 32768) > 4 * sms
+    xs = [workloads.gaussian_bf16(n, 0.002 * 1.9 ** p, 88, k, p) for p in range(k)]
+    xs[0][:5] = np.array([0x7F80, 0xFF80, 0x7FC1, 0x0001, 0x8001], np.uint16)
+    if k > 1:
+        xs[1][:70000] = np.random.default_rng(k).integers(0, 65536, size=70000, dtype=np.uint16)
+    chunks = oracle_chunks(xs)
+    ref = oracle.decompress_reduce(chunks, n)
+    y = zc.decompress_reduce(dev_chunks(chunks), n)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), ref)
+
+
 def test_reduce_raw_and_coded_tiles_mixed():
     n = 100000
     a = workloads.gaussian_bf16(n, 0.3, 1)
