@@ -381,6 +381,15 @@ def run_ours(args, rank: int, world: int):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index) as clk:
+        # the sampler's start leaves the GPU idle for a moment: the warm-up
+        # steps run again here, so that the timed steps follow them directly
+        for _ in range(args.warmup):
+            flush(0)
+            for _, f in stages:
+                f()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
         n0 = clk.lines()
         for i in range(args.steps):
             flush(i)                       # untimed: L2 flush
