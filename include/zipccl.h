@@ -232,6 +232,19 @@ zipccl_status zipccl_get_device_status(const void *d_ws, void *stream);
 zipccl_status zipccl_selftest_bounded_wait(int which, void *d_ws, uint64_t ws_bytes, void *stream);
 
 /*
+ * Measurement hook, for timing the encode kernel on its own.  While a pair
+ * of events is set, every zipccl_compress and zipccl_compress_send call
+ * records ev_before (a cudaEvent_t) on its stream immediately before it
+ * launches its encode kernel and ev_after immediately after, so that
+ * cudaEventElapsedTime(ev_before, ev_after) is that kernel's duration (the
+ * select kernel before it excluded).  The events belong to the caller, who
+ * creates them with timing enabled; two NULLs turn the hook off.  One NULL
+ * and one event: ZIPCCL_ERR_INVALID_ARG.  The setting is process-wide and
+ * meant for a benchmark driving calls from one host thread.
+ */
+zipccl_status zipccl_profile_encode_events(void *ev_before, void *ev_after);
+
+/*
  * Cost model of the switch between compressed and plain exchange ("ZipCCL:
  * Efficient Lossless Data Compression of Communication Collectives for
  * Accelerating LLM Training", abstract, technique (3): collectives switch

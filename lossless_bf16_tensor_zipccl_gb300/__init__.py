@@ -30,7 +30,8 @@ __all__ = [
     "zipccl_decompress_reduce",
     "zipccl_get_device_status", "zipccl_codebook_phase", "zipccl_codebook_rebuild_phase",
     "zipccl_decompress_reduce_noalloc",
-    "zipccl_predict_chunk_bytes", "zipccl_choose_compressed", "zipccl_selftest_bounded_wait", "compress", "decompress", "decompress_reduce",
+    "zipccl_predict_chunk_bytes", "zipccl_choose_compressed", "zipccl_selftest_bounded_wait",
+    "zipccl_profile_encode_events", "compress", "decompress", "decompress_reduce",
     "Compressed", "EXPORTED_SYMBOLS",
 ]
 
@@ -42,7 +43,7 @@ EXPORTED_SYMBOLS = [
     "zipccl_get_device_status", "zipccl_codebook_phase", "zipccl_codebook_rebuild_phase",
     "zipccl_decompress_reduce_noalloc",
     "zipccl_predict_chunk_bytes",
-    "zipccl_choose_compressed", "zipccl_selftest_bounded_wait",
+    "zipccl_choose_compressed", "zipccl_selftest_bounded_wait", "zipccl_profile_encode_events",
 ]
 
 _lock = threading.Lock()
@@ -115,6 +116,8 @@ def load(build_if_missing: bool = True):
         L.zipccl_predict_chunk_bytes.argtypes = [u64, ctypes.c_float, u64p, ctypes.POINTER(dbl)]
         L.zipccl_selftest_bounded_wait.restype = ctypes.c_int
         L.zipccl_selftest_bounded_wait.argtypes = [ctypes.c_int, vp, u64, vp]
+        L.zipccl_profile_encode_events.restype = ctypes.c_int
+        L.zipccl_profile_encode_events.argtypes = [vp, vp]
         L.zipccl_choose_compressed.restype = ctypes.c_int
         L.zipccl_choose_compressed.argtypes = [u64, ctypes.c_float, dbl, dbl, dbl, dbl, ctypes.POINTER(ctypes.c_int),
                                                ctypes.POINTER(dbl)]
@@ -241,6 +244,11 @@ def zipccl_codebook_rebuild_phase(phase: int) -> tuple[int, list[int]]:
 def zipccl_selftest_bounded_wait(which: int, ws_ptr: int, ws_bytes: int, stream_ptr: int) -> int:
     """Run one bounded wait that must give up (0: look-back, 1: mbarrier); returns the call's status."""
     return int(load().zipccl_selftest_bounded_wait(int(which), ws_ptr, int(ws_bytes), stream_ptr))
+
+
+def zipccl_profile_encode_events(ev_before: int, ev_after: int) -> int:
+    """Set (or, with two zeros, clear) the CUDA events every compress call records around its encode kernel."""
+    return int(load().zipccl_profile_encode_events(ev_before or None, ev_after or None))
 
 
 def zipccl_predict_chunk_bytes(n: int, sigma: float) -> tuple[int, float]:

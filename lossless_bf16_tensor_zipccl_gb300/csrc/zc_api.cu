@@ -6,6 +6,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <memory>
 
 #include "zipccl.h"
@@ -18,6 +19,11 @@ namespace zc {
 namespace {
 
 constexpr uint64_t kMaxChunkElems = (1ull << 31) - 1;
+
+// Measurement hook (zipccl_profile_encode_events): the caller's events that
+// compress records around its encode kernel, both null when off.
+std::atomic<void*> g_prof_before{nullptr};
+std::atomic<void*> g_prof_after{nullptr};
 
 uint64_t pad256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -213,7 +219,13 @@ zipccl_status compress_impl(const uint16_t* d_in, uint64_t n, const uint64_t* ch
   ea.hdr = sa->hdr;
   ea.n_chunks = n_chunks;
   ea.n_items = (uint32_t)L.n_items;
-  return cuda_status(launch_encode(ea, (uint32_t)L.n_items, s));
+  // measurement hook: the caller's events around the encode kernel alone
+  cudaEvent_t before = static_cast<cudaEvent_t>(g_prof_before.load(std::memory_order_acquire));
+  cudaEvent_t after = static_cast<cudaEvent_t>(g_prof_after.load(std::memory_order_acquire));
+  if (before && after && cudaEventRecord(before, s) != cudaSuccess) return ZIPCCL_ERR_CUDA;
+  const zipccl_status st = cuda_status(launch_encode(ea, (uint32_t)L.n_items, s));
+  if (st == ZIPCCL_OK && before && after && cudaEventRecord(after, s) != cudaSuccess) return ZIPCCL_ERR_CUDA;
+  return st;
 }
 
 }  // namespace
@@ -295,6 +307,14 @@ zipccl_status zipccl_decompress_reduce(const void* const* d_peer_chunks, const u
   ra.n = n;
   ra.k = k;
   return cuda_status(launch_reduce(ra, s));
+}
+
+zipccl_status zipccl_profile_encode_events(void* ev_before, void* ev_after) {
+  if ((ev_before == nullptr) != (ev_after == nullptr)) return ZIPCCL_ERR_INVALID_ARG;
+  g_prof_after.store(nullptr, std::memory_order_release);  // never one of a new pair with one of the old
+  g_prof_before.store(ev_before, std::memory_order_release);
+  g_prof_after.store(ev_after, std::memory_order_release);
+  return ZIPCCL_OK;
 }
 
 zipccl_status zipccl_get_device_status(const void* d_ws, void* stream) {

@@ -114,6 +114,14 @@ def test_compress_send_argument_errors_return_before_launch():
         zc.ERR_INVALID_ARG                                   # misaligned ready array
 
 
+def test_profile_hook_takes_both_events_or_none():
+    # the measurement hook is host-side state: one event without the other is
+    # refused, two nulls switch it off; nothing touches a device
+    assert zc.zipccl_profile_encode_events(0x1000, 0) == zc.ERR_INVALID_ARG
+    assert zc.zipccl_profile_encode_events(0, 0x1000) == zc.ERR_INVALID_ARG
+    assert zc.zipccl_profile_encode_events(0, 0) == zc.OK
+
+
 def test_selftest_argument_errors_return_before_launch():
     assert zc.zipccl_selftest_bounded_wait(3, FAKE, 512, 0) == zc.ERR_INVALID_ARG
     assert zc.zipccl_selftest_bounded_wait(2, FAKE, 335, 0) == zc.ERR_INVALID_ARG

@@ -349,6 +349,34 @@ def test_compress_send_gradient_bucket():
     assert torch.equal(send[: len(s)], c.data[: len(s)])
 
 
+def test_profile_events_time_the_encode_kernel_alone():
+    # the events the library records around its encode kernel: recorded on
+    # the call's stream, a positive interval inside the whole call's, and the
+    # hook off again leaves later calls untouched
+    x = workloads.gaussian_bf16(4 * 32768 + 99, 0.01, 31)
+    d = to_dev(x)
+    call0, call1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0.record()
+    k1.record()  # the handles exist once recorded
+    torch.cuda.synchronize()
+    assert zc.zipccl_profile_encode_events(k0.cuda_event, k1.cuda_event) == zc.OK
+    try:
+        call0.record()
+        c = zc.compress(d)
+        call1.record()
+    finally:
+        assert zc.zipccl_profile_encode_events(0, 0) == zc.OK
+    torch.cuda.synchronize()
+    kernel_ms, call_ms = k0.elapsed_time(k1), call0.elapsed_time(call1)
+    assert 0 < kernel_ms < call_ms
+    s, _ = stream_bytes(c)
+    assert s == oracle.compress(x)[0]
+    zc.compress(d)  # hook off: the events are not recorded again
+    torch.cuda.synchronize()
+    assert k0.elapsed_time(k1) == kernel_ms
+
+
 @pytest.mark.parametrize("which", [0, 1, 2])
 def test_bounded_wait_gives_up_and_context_stays_usable(which):
     # 0: the compressor's look-back on a predecessor that never publishes;
