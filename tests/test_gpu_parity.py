@@ -349,6 +349,70 @@ def test_compress_send_gradient_bucket():
     assert torch.equal(send[: len(s)], c.data[: len(s)])
 
 
+def test_calls_capture_into_a_cuda_graph_and_replay():
+    # a training loop's step, captured once and replayed with new data in the
+    # same buffers: compress-and-send, decompress and an allocation-free
+    # 3-peer reduce, every replay checked against the oracle
+    n, k = 3 * 32768 + 1000, 3
+    ce = [40000, 0, n - 40000]
+    x = torch.empty(n, dtype=torch.int16, device="cuda")
+    cap = zc.zipccl_max_compressed_bytes(ce)
+    out = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    send = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    ready = torch.zeros(len(ce) + 1, dtype=torch.int64, device="cuda")
+    offs = torch.empty(len(ce) + 1, dtype=torch.int64, device="cuda")
+    wsc = torch.empty(zc.zipccl_compress_workspace_bytes(ce), dtype=torch.uint8, device="cuda")
+    wsd = torch.empty(zc.zipccl_decompress_workspace_bytes(n, len(ce)), dtype=torch.uint8, device="cuda")
+    dec = torch.empty(n, dtype=torch.int16, device="cuda")
+    pn = 70001
+    peers = [torch.empty(zc.zipccl_max_compressed_bytes([pn]), dtype=torch.uint8, device="cuda") for _ in range(k)]
+    red = torch.empty(pn, dtype=torch.int16, device="cuda")
+    s = torch.cuda.Stream()
+    scratch = [0]
+
+    def step():
+        sp = s.cuda_stream
+        assert zc.zipccl_compress_send(x.data_ptr(), n, ce, None, out.data_ptr(), cap, offs.data_ptr(), send.data_ptr(),
+                                       cap, ready.data_ptr(), wsc.data_ptr(), wsc.numel(), sp) == zc.OK
+        assert zc.zipccl_decompress(out.data_ptr(), offs.data_ptr(), len(ce), dec.data_ptr(), n, wsd.data_ptr(),
+                                    wsd.numel(), sp) == zc.OK
+        st, scratch[0] = zc.zipccl_decompress_reduce_noalloc([t.data_ptr() for t in peers], [t.numel() for t in peers],
+                                                             k, pn, red.data_ptr(), sp)
+        assert st == zc.OK
+
+    def load(r):
+        xs = workloads.gaussian_bf16(n, 0.01 * (r + 1), 41, r)
+        x.copy_(torch.from_numpy(xs.view(np.int16)))
+        pcs = [oracle.compress(workloads.gaussian_bf16(pn, 0.003 * (p + 1), 42, r, p))[0] for p in range(k)]
+        for t, c in zip(peers, pcs):
+            t.zero_()
+            t[: len(c)].copy_(torch.from_numpy(np.frombuffer(c, dtype=np.uint8).copy()))
+        return xs, pcs
+
+    load(0)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        step()  # first-call set-up (kernel attributes, occupancy) outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for r in (1, 2):
+        xs, pcs = load(r)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        for ws in (wsc.data_ptr(), wsd.data_ptr(), scratch[0]):
+            assert zc.zipccl_get_device_status(ws, 0) == zc.OK
+        so, oo = oracle.compress(xs, ce)
+        o = offs.cpu().numpy().view(np.uint64)
+        assert np.array_equal(o, oo)
+        assert out[: int(o[-1])].cpu().numpy().tobytes() == so
+        assert torch.equal(send[: int(o[-1])], out[: int(o[-1])])
+        assert torch.equal(dec, x)
+        assert np.array_equal(red.cpu().numpy().view(np.uint16), oracle.decompress_reduce(pcs, pn))
+
+
 def test_profile_events_time_the_encode_kernel_alone():
     # the events the library records around its encode kernel: recorded on
     # the call's stream, a positive interval inside the whole call's, and the
