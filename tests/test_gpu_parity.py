@@ -198,12 +198,13 @@ def test_reduce_peers_with_different_tables():
     assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), ref)
 
 
-@pytest.mark.parametrize("k", [1, 2, 3, 5])
+@pytest.mark.parametrize("k", [1, 2, 3, 5, 8, 16])
 def test_reduce_grid_beyond_four_blocks_per_sm(k):
     # more half tiles than 4 per SM: for up to 5 peers the reduce then takes
     # the instantiation whose hand-off barriers are immediates, since more of
-    # its blocks are resident and the grid runs in fewer waves; a ragged
-    # tail, a raw stretch in one peer, specials in another
+    # its blocks are resident and the grid runs in fewer waves; 8 peers (named
+    # barriers) and 16 (mbarrier hand-offs) run it in more than one wave; a
+    # ragged tail, a raw stretch in one peer, specials in another
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     n = (2 * sms + 5) * 32768 + 777
     assert 2 * ((n + 32767) // 32768) > 4 * sms
