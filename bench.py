@@ -414,8 +414,10 @@ def run_ours(args, rank: int, world: int):
                 for j, (name, _) in enumerate(stages)}
 
     # The encode kernel's own launch duration, in a loop of its own so that
-    # the step above carries no instrumentation: the library records these
-    # events on the call's stream right before and after the encode launch.
+    # the step above carries no instrumentation (recording the events adds a
+    # few microseconds to the call outside the interval they bracket): the
+    # library records them on the call's stream right before and after the
+    # encode launch.
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a, b in kev:
         a.record(stream)  # the event handles exist once recorded
