@@ -24,10 +24,14 @@
  *   - Argument errors are returned synchronously, before any launch.
  *   - Data-dependent errors (a corrupt stream, a look-back that timed out)
  *     are recorded by the kernels in a status word at the start of the
- *     workspace; zipccl_get_device_status reads it.  Each compress,
- *     decompress or decompress_reduce call clears it first, so read it after
- *     the call you want to check.  On such an error outputs are undefined
- *     but every access stays inside the caller's buffers.
+ *     workspace; zipccl_get_device_status reads it and reports the last
+ *     call made on that workspace, so read it after the call you want to
+ *     check.  A compress call clears it first; a decompress or
+ *     decompress_reduce call does not clear anything but tags its errors
+ *     with a 56-bit number of its own, so that an earlier call's code (or
+ *     whatever the memory held) never reads as its status.  No
+ *     initialisation of a workspace is needed.  On such an error outputs
+ *     are undefined but every access stays inside the caller's buffers.
  *   - A workspace must not be shared by calls that may run concurrently.
  */
 #ifndef ZIPCCL_H

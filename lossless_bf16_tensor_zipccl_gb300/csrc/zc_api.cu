@@ -25,6 +25,20 @@ constexpr uint64_t kMaxChunkElems = (1ull << 31) - 1;
 std::atomic<void*> g_prof_before{nullptr};
 std::atomic<void*> g_prof_after{nullptr};
 
+// Status tag of one decompress or reduce call (see WsHeader): 56 bits, never
+// 0, spread by a splitmix64 step so that a workspace's leftover bytes match
+// a tag only by a 2^-56 chance.
+std::atomic<uint64_t> g_tag_counter{0};
+uint64_t next_status_tag() {
+  for (;;) {
+    uint64_t z = g_tag_counter.fetch_add(1, std::memory_order_relaxed) + 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z = (z ^ (z >> 31)) & kTagMask;
+    if (z) return z;
+  }
+}
+
 uint64_t pad256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -259,8 +273,7 @@ zipccl_status zipccl_decompress(const void* d_stream, const uint64_t* d_chunk_of
   if (ws_bytes < L.total) return ZIPCCL_ERR_CAPACITY;
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(WsHeader), s);
-  if (e != cudaSuccess) return ZIPCCL_ERR_CUDA;
+  const uint64_t tag = next_status_tag();  // no clear of the header: errors carry this call's tag
   DprepArgs pa;
   pa.stream = static_cast<const uint8_t*>(d_stream);
   pa.offsets = d_chunk_offsets;
@@ -271,6 +284,7 @@ zipccl_status zipccl_decompress(const void* d_stream, const uint64_t* d_chunk_of
   pa.n_chunks = n_chunks;
   pa.max_items = (uint32_t)max_items;
   pa.n = n;
+  pa.tag = tag;
   DecodeArgs da;
   da.stream = pa.stream;
   da.offsets = d_chunk_offsets;
@@ -280,6 +294,7 @@ zipccl_status zipccl_decompress(const void* d_stream, const uint64_t* d_chunk_of
   da.out = d_out;
   da.hdr = pa.hdr;
   da.n_chunks = n_chunks;
+  da.tag = tag;
   return cuda_status(launch_decode(pa, da, (uint32_t)max_items, s));
 }
 
@@ -298,8 +313,7 @@ zipccl_status zipccl_decompress_reduce(const void* const* d_peer_chunks, const u
   if (ws_bytes < red_ws(k)) return ZIPCCL_ERR_CAPACITY;
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(WsHeader), s);
-  if (e != cudaSuccess) return ZIPCCL_ERR_CUDA;
+  ra.tag = next_status_tag();  // no clear of the header: errors carry this call's tag
   ra.hdr = reinterpret_cast<WsHeader*>(ws);
   ra.chunks = reinterpret_cast<DecChunk*>(ws + sizeof(WsHeader));
   ra.luts = reinterpret_cast<uint32_t*>(ws + sizeof(WsHeader) + pad256(sizeof(DecChunk) * (uint64_t)k));
@@ -321,9 +335,12 @@ zipccl_status zipccl_get_device_status(const void* d_ws, void* stream) {
   if (!d_ws) return ZIPCCL_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return ZIPCCL_ERR_CUDA;
-  uint32_t st = 0;
-  if (cudaMemcpy(&st, d_ws, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return ZIPCCL_ERR_CUDA;
-  return static_cast<zipccl_status>(st);
+  WsHeader h;
+  if (cudaMemcpy(&h, d_ws, 24, cudaMemcpyDeviceToHost) != cudaSuccess) return ZIPCCL_ERR_CUDA;
+  if (h.epoch == 0) return static_cast<zipccl_status>(h.status);  // compress, self-test: plain code
+  // decompress, reduce: the code counts only if it carries the last call's tag
+  const uint64_t w = ((uint64_t)h.status_hi << 32) | h.status;
+  return (w >> 8) == h.epoch ? static_cast<zipccl_status>(w & 0xFFu) : ZIPCCL_OK;
 }
 
 zipccl_status zipccl_predict_chunk_bytes(uint64_t n, float sigma, uint64_t* out_bytes, double* out_bits_per_value) {

@@ -203,6 +203,7 @@ constexpr uint32_t kLutPart = kLutEntries / kLutParts;
 __global__ void __launch_bounds__(256) zc_dprep_kernel(DprepArgs a) {
   pdl_trigger();
   const uint32_t tid = threadIdx.x;
+  if (blockIdx.x == 0 && tid == 0) a.hdr->epoch = a.tag;  // the call's tag, before anything can fail
   if (blockIdx.x < a.n_chunks * kLutParts) {
     const uint32_t c = blockIdx.x / kLutParts, part = blockIdx.x % kLutParts;
     const uint64_t o0 = a.offsets[c], o1 = a.offsets[c + 1], total = a.offsets[a.n_chunks];
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(256) zc_dprep_kernel(DprepArgs a) {
     uint32_t st = (o1 < o0 || o1 > total || (o0 & 15)) ? kStCorrupt : check_header(a.stream + o0, o1 - o0, h);
     if (st) {
       if (tid == 0 && part == 0) {
-        set_status(a.hdr, st);
+        set_status_tagged(a.hdr, a.tag, st);
         a.chunks[c].ok = 0;
       }
       return;
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(256) zc_dprep_kernel(DprepArgs a) {
   if (tid == 0) {
     a.item_start[a.n_chunks] = (uint32_t)min(carry_t, (uint64_t)a.max_items);
     a.hdr->total_items = (uint32_t)min(carry_t, (uint64_t)a.max_items);
-    if (s_bad || carry_n != a.n || carry_t > a.max_items) set_status(a.hdr, kStCorrupt);
+    if (s_bad || carry_n != a.n || carry_t > a.max_items) set_status_tagged(a.hdr, a.tag, kStCorrupt);
   }
 }
 
@@ -457,7 +458,7 @@ __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
 
   pdl_wait();  // chunk records and tables come from the prep kernel
   // one read of the status word per block, so both warps take the same path
-  if (tid == 0) s_flag[0] = *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0 || item >= a.hdr->total_items;
+  if (tid == 0) s_flag[0] = status_tagged_set(a.hdr, a.tag) || item >= a.hdr->total_items;
   __syncthreads();
   if (s_flag[0]) {
     if (tid == 0 && (sbytes || pbytes)) mbar_wait(&s_xbar, 0);  // nothing left in flight
@@ -493,7 +494,7 @@ __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
   const bool timeout = (sbytes || pbytes) && __any_sync(kFull, !mbar_wait(&s_xbar, 0));
   if (bad || timeout) {
     // the copy has arrived or was given up on; the status tells the caller
-    if (lane == 0) set_status(a.hdr, bad ? kStCorrupt : kStTimeout);
+    if (lane == 0) set_status_tagged(a.hdr, a.tag, bad ? kStCorrupt : kStTimeout);
     return;
   }
   const uint64_t e0 = d.elem_start + (uint64_t)k * kTile;
@@ -522,13 +523,14 @@ __global__ void __launch_bounds__(64) zc_decode_kernel(DecodeArgs a) {
 // Blocks p * kLutParts + j: validate peer p's header, build part j of its table.
 __global__ void __launch_bounds__(256) zc_rprep_kernel(ReduceArgs a) {
   pdl_trigger();
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.hdr->epoch = a.tag;  // the call's tag, before anything can fail
   const uint32_t p = blockIdx.x / kLutParts, part = blockIdx.x % kLutParts;
   HeaderInfo h;
   uint32_t st = check_header(a.peers[p], a.bytes[p], h);
   if (!st && h.n != a.n) st = kStCorrupt;
   if (st) {
     if (threadIdx.x == 0 && part == 0) {
-      set_status(a.hdr, st);
+      set_status_tagged(a.hdr, a.tag, st);
       a.chunks[p].ok = 0;
     }
     return;
@@ -786,12 +788,12 @@ __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
   const DecChunk d = a.chunks[p];
   const bool ok = located && d.ok && d.n_tiles == n_tiles;
   // one read of the status word per block, so every thread takes the same path
-  if (tid == 0 && *reinterpret_cast<volatile uint32_t*>(&a.hdr->status) != 0) s_bad = 1;
+  if (tid == 0 && status_tagged_set(a.hdr, a.tag)) s_bad = 1;
   if (lane == 0) {
     s_own[p] = d.item_start;  // the peer owning this peer's table
     if (!ok || timeout) {
       s_bad = 1;
-      set_status(a.hdr, ok ? kStTimeout : kStCorrupt);
+      set_status_tagged(a.hdr, a.tag, ok ? kStTimeout : kStCorrupt);
     }
   }
   // Decoders for the whole block: staged when every coded peer is staged (a
@@ -828,7 +830,7 @@ __global__ void __launch_bounds__(32 * K) zc_reduce_kernel(ReduceArgs a) {
     src.start(tv, nt, col, a.luts + (size_t)d.item_start * kLutEntries, d.base, xs);
     live = reduce_rows<K, kImm>(src, smp, acc, done, y, sq);
   }
-  if (!live && lane == 0) set_status(a.hdr, kStTimeout);
+  if (!live && lane == 0) set_status_tagged(a.hdr, a.tag, kStTimeout);
 }
 
 // ---------------------------------------------------------------- launchers

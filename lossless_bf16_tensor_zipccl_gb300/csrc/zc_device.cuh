@@ -50,6 +50,27 @@ __device__ __forceinline__ void set_status(WsHeader* h, uint32_t code) {
   atomicCAS(&h->status, 0u, code);
 }
 
+// Tagged status of a decompress or reduce call (tag: 56 bits, nonzero): the
+// call's first error wins; a word with another tag is stale and is replaced.
+// Only the call's own threads write the word, so after one stale word is
+// replaced every further attempt finds this call's tag and stops.
+__device__ __forceinline__ void set_status_tagged(WsHeader* h, uint64_t tag, uint32_t code) {
+  unsigned long long* w = reinterpret_cast<unsigned long long*>(&h->status);
+  const unsigned long long want = (tag << 8) | code;
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(w);
+  for (int i = 0; i < 64; ++i) {
+    if ((old >> 8) == tag && (old & 0xFFu) != 0) return;
+    const unsigned long long prev = atomicCAS(w, old, want);
+    if (prev == old) return;
+    old = prev;
+  }
+}
+
+__device__ __forceinline__ bool status_tagged_set(const WsHeader* h, uint64_t tag) {
+  const unsigned long long v = *reinterpret_cast<const volatile unsigned long long*>(&h->status);
+  return (v >> 8) == tag && (v & 0xFFu) != 0;
+}
+
 // Programmatic dependent launch.  A prep kernel lets the kernel after it in
 // the stream be scheduled at once (pdl_trigger); that kernel, launched with
 // programmatic stream serialisation, waits for the prep kernel to finish

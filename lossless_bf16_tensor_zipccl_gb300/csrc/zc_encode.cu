@@ -45,7 +45,8 @@ __global__ void __launch_bounds__(256) zc_select_kernel(const __grid_constant__ 
   __shared__ int s_q;
   if (ci == 0 && threadIdx.x == 0) {
     a.hdr->status = 0;
-    a.hdr->counter = 0;
+    a.hdr->status_hi = 0;
+    a.hdr->epoch = 0;
   }
   if (ca.has_hint) {
     if (threadIdx.x == 0) s_q = ca.q_hint;

@@ -88,15 +88,23 @@ constexpr uint64_t kSlotValid = 1ull << 63;
 // Device status codes (match zipccl_status).
 constexpr uint32_t kStCorrupt = 3, kStVersion = 4, kStTimeout = 5, kStCapacity = 2;
 
-// Workspace header, at the start of every workspace.
+// Workspace header, at the start of every workspace.  Compress (and the
+// bounded-wait self-test) clear it first and keep a plain code in `status`.
+// Decompress and reduce do not clear it: each call draws a 56-bit tag, its
+// prep kernel stores the tag in `epoch`, and its kernels record an error as
+// the 64-bit word (tag << 8 | code) over `status` and `status_hi`, so that a
+// code left by an earlier call (or by whatever the memory held) reads as no
+// error.  `epoch` = 0 marks the plain form.
 struct alignas(256) WsHeader {
   uint32_t status;
-  uint32_t counter;     // dynamic tile counter (compress)
+  uint32_t status_hi;   // upper half of a tagged status (decompress, reduce)
   uint32_t total_items; // decode work items (decompress)
   uint32_t pad0;
-  uint64_t pad[30];
+  uint64_t epoch;       // the last decompress or reduce call's tag; 0: plain status
+  uint64_t pad[29];
 };
 static_assert(sizeof(WsHeader) == 256, "ws header");
+constexpr uint64_t kTagMask = (1ull << 56) - 1;
 
 // Per-chunk record of the compress workspace.
 struct alignas(64) EncChunk {

@@ -63,6 +63,7 @@ struct DprepArgs {
   uint32_t n_chunks;
   uint32_t max_items;
   uint64_t n;
+  uint64_t tag;  // the call's status tag (see WsHeader)
 };
 
 struct DecodeArgs {
@@ -74,6 +75,7 @@ struct DecodeArgs {
   uint16_t* out;
   WsHeader* hdr;
   uint32_t n_chunks;
+  uint64_t tag;
 };
 
 struct ReduceArgs {
@@ -85,6 +87,7 @@ struct ReduceArgs {
   uint16_t* out;
   uint64_t n;
   uint32_t k;
+  uint64_t tag;
 };
 
 // Launch configuration of a kernel that follows a prep kernel in the same

@@ -265,6 +265,66 @@ def test_corrupt_streams_report_status():
     assert corrupt_status(s[: int(short[-1])], short, n) == zc.ERR_CORRUPT  # truncated
 
 
+@pytest.mark.parametrize("fill", ["ones", "zeros", "random"])
+def test_status_belongs_to_the_last_call_on_a_workspace(fill):
+    # decompress and reduce do not clear their workspace header: each call's
+    # errors carry its own tag, so whatever the workspace held before (any
+    # bytes, or an earlier call's error) never reads as this call's status
+    x = workloads.gaussian_bf16(70000, 0.05, 3)
+    good, offs = oracle.compress(x)
+    bad = bytearray(good); bad[0] ^= 1
+    n = x.size
+    o = torch.from_numpy(np.asarray(offs, dtype=np.uint64).view(np.int64).copy()).cuda()
+    out = torch.empty(n, dtype=torch.int16, device="cuda")
+    wsb = zc.zipccl_decompress_workspace_bytes(n, 1)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    if fill == "ones":
+        ws.fill_(0xFF)
+    elif fill == "zeros":
+        ws.zero_()
+    else:
+        ws.copy_(torch.from_numpy(np.random.default_rng(5).integers(0, 256, wsb, dtype=np.uint8)))
+    s = torch.cuda.current_stream().cuda_stream
+
+    def dec(buf):
+        d = torch.from_numpy(np.frombuffer(bytes(buf), dtype=np.uint8).copy()).cuda()
+        assert zc.zipccl_decompress(d.data_ptr(), o.data_ptr(), 1, out.data_ptr(), n, ws.data_ptr(), wsb, s) == zc.OK
+        return zc.zipccl_get_device_status(ws.data_ptr(), s)
+
+    assert dec(good) == zc.OK
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), x)
+    assert dec(bad) == zc.ERR_CORRUPT
+    assert dec(good) == zc.OK                       # the earlier error is not this call's
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), x)
+    assert dec(bad) == zc.ERR_CORRUPT
+    # the reduce on a workspace of its own, the same way
+    pn, k = 40000, 3
+    pcs = [oracle.compress(workloads.gaussian_bf16(pn, 0.01, 8, p))[0] for p in range(k)]
+    wr = zc.zipccl_reduce_workspace_bytes(k)
+    wsr = torch.full((wr,), 0xFF if fill == "ones" else 0, dtype=torch.uint8, device="cuda")
+    red = torch.empty(pn, dtype=torch.int16, device="cuda")
+
+    def reduce(chunks):
+        dch = [torch.from_numpy(np.frombuffer(bytes(c), dtype=np.uint8).copy()).cuda() for c in chunks]
+        assert zc.zipccl_decompress_reduce([t.data_ptr() for t in dch], [t.numel() for t in dch], k, pn,
+                                           red.data_ptr(), wsr.data_ptr(), wr, s) == zc.OK
+        return zc.zipccl_get_device_status(wsr.data_ptr(), s)
+
+    broken = bytearray(pcs[1]); broken[0] ^= 1
+    assert reduce([pcs[0], broken, pcs[2]]) == zc.ERR_CORRUPT
+    assert reduce(pcs) == zc.OK
+    assert np.array_equal(red.cpu().numpy().view(np.uint16), oracle.decompress_reduce(pcs, pn))
+    # a compress on the same workspace afterwards reads back in its plain form
+    wc = zc.zipccl_compress_workspace_bytes([n])
+    if wc <= wsb:
+        d = to_dev(x)
+        cap = zc.zipccl_max_compressed_bytes([n])
+        cb = torch.empty(cap, dtype=torch.uint8, device="cuda")
+        assert zc.zipccl_compress(d.data_ptr(), n, [n], None, cb.data_ptr(), cap, o.data_ptr(), ws.data_ptr(), wc,
+                                  s) == zc.OK
+        assert zc.zipccl_get_device_status(ws.data_ptr(), s) == zc.OK
+
+
 def test_side_stream_calls_with_library_allocated_buffers():
     # Every buffer the helpers allocate is recorded on the call's stream, so
     # work queued on the current stream meanwhile cannot take its memory.
