@@ -223,10 +223,13 @@ __device__ __forceinline__ void bar_wait(uint32_t id, uint32_t n) {
 
 // Decoupled look-back over the flat tile list (warp-wide).  Each tile
 // publishes its byte count (aggregate), then its inclusive prefix.  One pass
-// reads the 256 nearest unfolded predecessors (8 per lane), folds them up to
+// reads the 64 nearest unfolded predecessors (2 per lane), folds them up to
 // and including the nearest inclusive prefix, and stops there.  Returns the
-// exclusive prefix; sets err on a timed-out wait or an upstream error.
-constexpr int kLookbackDepth = 8;  // states per lane per pass
+// exclusive prefix; sets err on a timed-out wait or an upstream error.  The
+// nearest inclusive prefix is usually a few tiles back, and every pass costs
+// the store warp issue slots its scheduler's row warps would use: passes of
+// 64 compress faster than passes of 256 (measured: -4 to -5%).
+constexpr int kLookbackDepth = 2;  // states per lane per pass
 
 __device__ uint64_t lookback(const uint64_t* state, uint32_t item, uint32_t lane, bool& err) {
   uint64_t excl = 0;
